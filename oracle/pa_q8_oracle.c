@@ -1,0 +1,244 @@
+/*
+ * pa_q8 oracle -- a plain, slow CPU statement of the int8 paged-KV decode
+ * path, used ONLY as test infrastructure: by the tests, by the package's
+ * smoke check and by the benchmark's CPU-baseline leg.  The product path
+ * never links, loads or calls this file, and it shares no code, header,
+ * table or constant with the CUDA kernels.
+ *
+ * What it restates (from the pages' own descriptions, in its own code):
+ *
+ *  - reshape_and_cache_q8.comp (hanzo-ml 0.11.93), header comment and main():
+ *    per (token, kv_head) vector, amax = max |x| starting from 0;
+ *    inv = 127/amax (0 when amax is 0); code = clamp(round(x * inv), -127, 127);
+ *    4 codes per u32 word in little-endian byte lanes (two's complement);
+ *    then one word holding the f32 bit pattern of amax/127 (1.0 when amax
+ *    is 0); the token vector lands at
+ *    [block, kv_head, offset, word] of a [num_blocks, num_kv_heads,
+ *    block_size, head_size/4 + 1] u32 cache; slot 0xFFFFFFFF is skipped.
+ *
+ *  - paged_attn_q8.comp (hanzo-ml 0.11.92), header comment ("output =
+ *    softmax(scale*Q.K^T).V", dequantise as code * token_scale) and main()
+ *    (GQA head map kv_head = head / (num_heads / num_kv_heads); logical
+ *    token t sits in block_tables[seq][t / block_size] at offset
+ *    t % block_size; context_len clamped).
+ *
+ *  - attention.rs (cherenkov qwen4_exp gpu), attention_b: a context split
+ *    into parts whose partial results are merged by a combine step.  The
+ *    merge of (max, sum, weighted sum) partials by their log-sum-exp is
+ *    written out in oracle_combine below.
+ *
+ * Arithmetic.  The writer is bit-exact by construction: every f32 operation
+ * of the shader (one division, one product, one division for the scale) is
+ * done in double and rounded once to float.  For +, -, *, / of two floats
+ * that equals the correctly rounded f32 result, because a double carries
+ * 53 >= 2*24 + 2 bits.  Rounding is half away from zero (C round()), the
+ * reading taken for the shader's round().  The decode is computed in double
+ * from the dequantised cache; no blocking, no online rescaling, no
+ * reassociation beyond summing in logical token / dimension order.
+ *
+ * Readings where the pages leave a step open:
+ *  - no epsilon in the softmax denominator (the decode shader adds 1e-6);
+ *  - context_len is clamped to max_blocks_per_seq * block_size;
+ *  - context_len == 0 gives an all-zero output row;
+ *  - a NaN product x * inv (only 0 * inf, when 127/amax overflowed for a
+ *    tiny amax) gives code 0; +-inf clamps to +-127 in the float domain.
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -fopenmp -ffp-contract=off
+ *        -fno-fast-math pa_q8_oracle.c -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PAD_SLOT 0xFFFFFFFFu
+
+static float float_from_bits(uint32_t u) { float f; memcpy(&f, &u, sizeof f); return f; }
+static uint32_t bits_from_float(float f) { uint32_t u; memcpy(&u, &f, sizeof u); return u; }
+
+/* Byte lane `lane` of a packed word as a signed code (two's complement). */
+static int code_at(uint32_t word, int lane)
+{
+    int v = (int)((word >> (8 * lane)) & 0xFFu);
+    return v >= 128 ? v - 256 : v;
+}
+
+/* round-half-away-from-zero, then clamp to [-127, 127] in the float domain */
+static int quantise_one(float t)
+{
+    if (t != t) return 0;
+    double r = round((double)t);
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    return (int)r;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Quantise one head_size-long f32 vector into head_size/4 code words plus
+ * one scale word (reshape_and_cache_q8.comp, main(): amax reduce -> scale ->
+ * pack).  words must hold head_size/4 + 1 entries. */
+void oracle_quantize_vector(const float *x, int head_size, uint32_t *words)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < head_size; ++d) {
+        float a = fabsf(x[d]);
+        if (a > amax) amax = a;
+    }
+    float inv = amax > 0.0f ? (float)(127.0 / (double)amax) : 0.0f;
+    for (int w = 0; w < head_size / 4; ++w) {
+        uint32_t word = 0;
+        for (int l = 0; l < 4; ++l) {
+            float t = (float)((double)x[4 * w + l] * (double)inv);
+            int q = quantise_one(t);
+            word |= ((uint32_t)q & 0xFFu) << (8 * l);
+        }
+        words[w] = word;
+    }
+    float scale = amax > 0.0f ? (float)((double)amax / 127.0) : 1.0f;
+    words[head_size / 4] = bits_from_float(scale);
+}
+
+/* reshape_and_cache_q8.comp, main(): one writer call.  key/value rows are
+ * [num_tokens, num_kv_heads, head_size] f32 with row strides key_stride /
+ * value_stride (f32 elements). */
+void oracle_reshape_and_cache(const float *key, const float *value,
+                              uint32_t *key_cache, uint32_t *value_cache,
+                              const uint32_t *slot_mapping, int64_t num_tokens,
+                              int64_t key_stride, int64_t value_stride,
+                              int num_kv_heads, int head_size, int block_size)
+{
+    const int64_t wpt = head_size / 4 + 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        uint32_t slot = slot_mapping[i];
+        if (slot == PAD_SLOT) continue;
+        int64_t block = (int64_t)(slot / (uint32_t)block_size);
+        int64_t off = (int64_t)(slot % (uint32_t)block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t dst = ((block * num_kv_heads + h) * block_size + off) * wpt;
+            oracle_quantize_vector(key + i * key_stride + (int64_t)h * head_size, head_size,
+                                   key_cache + dst);
+            oracle_quantize_vector(value + i * value_stride + (int64_t)h * head_size, head_size,
+                                   value_cache + dst);
+        }
+    }
+}
+
+/* The dequantised vector (code * token scale, exact in double) of logical
+ * token t of sequence s, kv head g. */
+static void dequant_token(const uint32_t *cache, const uint32_t *block_tables,
+                          int max_blocks_per_seq, int num_kv_heads, int head_size,
+                          int block_size, int s, int g, int64_t t, double *out)
+{
+    const int64_t wpt = head_size / 4 + 1;
+    uint32_t block = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+    int64_t off = t % block_size;
+    const uint32_t *vec = cache + (((int64_t)block * num_kv_heads + g) * block_size + off) * wpt;
+    double scale = (double)float_from_bits(vec[head_size / 4]);
+    for (int d = 0; d < head_size; ++d)
+        out[d] = (double)code_at(vec[d / 4], d % 4) * scale;
+}
+
+static int64_t clamped_len(const uint32_t *context_lens, int s, int max_blocks_per_seq, int block_size)
+{
+    int64_t c = context_lens[s];
+    int64_t cap = (int64_t)max_blocks_per_seq * block_size;
+    return c < cap ? c : cap;
+}
+
+/* Partial attention of query row (s, h) over logical tokens [t0, t1):
+ * m = max_t z_t, l = sum_t e^(z_t - m), acc[d] = sum_t e^(z_t - m) v_t[d],
+ * z_t = scale * q . k_t.  An empty range gives m = -inf, l = 0, acc = 0. */
+void oracle_decode_partial(const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                           const uint32_t *block_tables, int num_heads, int num_kv_heads,
+                           int head_size, int block_size, int max_blocks_per_seq, double scale,
+                           int s, int h, int64_t t0, int64_t t1,
+                           double *m_out, double *l_out, double *acc)
+{
+    const int g = h / (num_heads / num_kv_heads);
+    const float *qv = q + ((int64_t)s * num_heads + h) * head_size;
+    for (int d = 0; d < head_size; ++d) acc[d] = 0.0;
+    *l_out = 0.0;
+    *m_out = -INFINITY;
+    if (t1 <= t0) return;
+
+    double *z = (double *)malloc(sizeof(double) * (size_t)(t1 - t0));
+    double *vec = (double *)malloc(sizeof(double) * (size_t)head_size);
+    double m = -INFINITY;
+    for (int64_t t = t0; t < t1; ++t) {
+        dequant_token(key_cache, block_tables, max_blocks_per_seq, num_kv_heads, head_size,
+                      block_size, s, g, t, vec);
+        double dot = 0.0;
+        for (int d = 0; d < head_size; ++d) dot += (double)qv[d] * vec[d];
+        z[t - t0] = scale * dot;
+        if (z[t - t0] > m) m = z[t - t0];
+    }
+    double l = 0.0;
+    for (int64_t t = t0; t < t1; ++t) {
+        double p = exp(z[t - t0] - m);
+        l += p;
+        dequant_token(value_cache, block_tables, max_blocks_per_seq, num_kv_heads, head_size,
+                      block_size, s, g, t, vec);
+        for (int d = 0; d < head_size; ++d) acc[d] += p * vec[d];
+    }
+    *m_out = m;
+    *l_out = l;
+    free(vec);
+    free(z);
+}
+
+/* Merge n partials (m_i, l_i, acc_i[D]) of one query row by their
+ * log-sum-exp: M = max m_i; L = sum l_i e^(m_i - M);
+ * out = sum acc_i e^(m_i - M) / L.  L == 0 (no tokens) gives zeros. */
+void oracle_combine(const double *m, const double *l, const double *acc, int n, int head_size,
+                    double *out)
+{
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i) if (m[i] > M) M = m[i];
+    for (int d = 0; d < head_size; ++d) out[d] = 0.0;
+    if (M == -INFINITY) return;
+    double L = 0.0;
+    for (int i = 0; i < n; ++i) {
+        if (l[i] == 0.0) continue;
+        double w = exp(m[i] - M);
+        L += l[i] * w;
+        for (int d = 0; d < head_size; ++d) out[d] += acc[(int64_t)i * head_size + d] * w;
+    }
+    for (int d = 0; d < head_size; ++d) out[d] /= L;
+}
+
+/* Decode: out[s, h, :] = softmax(scale * q[s,h] . K^T) V over the clamped
+ * context of sequence s.  rows == NULL computes every (s, h); otherwise
+ * rows holds n_rows (s, h) pairs and out is [n_rows, head_size]. */
+void oracle_decode(double *out, const float *q, const uint32_t *key_cache,
+                   const uint32_t *value_cache, const uint32_t *block_tables,
+                   const uint32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                   int head_size, int block_size, int max_blocks_per_seq, double scale,
+                   const int32_t *rows, int64_t n_rows)
+{
+    int64_t n = rows ? n_rows : (int64_t)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        int s = rows ? rows[2 * i] : (int)(i / num_heads);
+        int h = rows ? rows[2 * i + 1] : (int)(i % num_heads);
+        double *o = out + i * head_size;
+        double m, l;
+        int64_t c = clamped_len(context_lens, s, max_blocks_per_seq, block_size);
+        oracle_decode_partial(q, key_cache, value_cache, block_tables, num_heads, num_kv_heads,
+                              head_size, block_size, max_blocks_per_seq, scale, s, h, 0, c,
+                              &m, &l, o);
+        if (c == 0) continue;           /* all zeros */
+        for (int d = 0; d < head_size; ++d) o[d] /= l;
+    }
+}
