@@ -1,0 +1,187 @@
+/*
+ * pa_q8 -- int8 paged-KV attention decode for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libpa_q8.so.  Plain pointers and sizes only; every pointer named
+ * "device" is a CUDA device address the caller allocated and owns.  The
+ * library keeps no per-call state and allocates no device memory: scratch
+ * (the split-context partials) lives in a workspace the caller passes in.
+ * All work is queued on the caller's CUDA stream (a cudaStream_t passed as
+ * void*; NULL = the legacy default stream) and no function synchronises,
+ * except pa_q8_device_status which reads a flag back.
+ *
+ * Data layout (header comments of the "paged_attn_q8.comp" and
+ * "reshape_and_cache_q8.comp" pages, hanzo-ml 0.11.92 / 0.11.93):
+ *
+ *   key_cache, value_cache : u32 [num_blocks][num_kv_heads][block_size][W],
+ *                            W = head_size/4 + 1.  A token vector holds
+ *                            head_size/4 code words (4 int8 codes per word,
+ *                            code l in bits 8l..8l+7, two's complement)
+ *                            followed by one word with the f32 bit pattern of
+ *                            the token's scale.  value = code * scale.
+ *   block_tables           : u32 [num_seqs][max_blocks_per_seq]; logical
+ *                            token t of a sequence is in physical block
+ *                            block_tables[s][t / block_size], offset
+ *                            t % block_size.  Entries past a sequence's last
+ *                            block are never read.
+ *   context_lens           : u32 [num_seqs]; clamped to
+ *                            max_blocks_per_seq * block_size.
+ *   q, out                 : f32 [num_seqs][num_heads][head_size], contiguous.
+ *   query head h reads kv head h / (num_heads / num_kv_heads).
+ *
+ * Return values: PA_Q8_OK or a negative pa_q8_status; nothing throws.
+ * Argument errors are found on the host before anything is queued.  Errors
+ * a kernel finds while running (a block id or slot out of range, a wait
+ * that gave up) set sticky bits in a per-device status word that
+ * pa_q8_device_status reads; the offending access is skipped, never made.
+ */
+#ifndef PA_Q8_H
+#define PA_Q8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_q8_status {
+    PA_Q8_OK = 0,
+    PA_Q8_EINVAL = -1,        /* a size <= 0, a NULL pointer, H % Hk != 0, D or B not a multiple of 4 */
+    PA_Q8_EUNSUPPORTED = -2,  /* valid but without a kernel: head_size not in {64,128,256},
+                                 block_size not a power of two in [4,128], ... */
+    PA_Q8_EALIGN = -3,        /* a pointer or stride without the alignment stated below */
+    PA_Q8_ECUDA = -4,         /* the CUDA runtime refused a launch or query */
+    PA_Q8_EWORKSPACE = -5     /* workspace_bytes below pa_q8_decode_workspace_size() */
+} pa_q8_status;
+
+/* Sticky device-side error bits (pa_q8_device_status). */
+#define PA_Q8_DEV_BAD_BLOCK    0x1u  /* a block_tables entry >= num_blocks was skipped      */
+#define PA_Q8_DEV_BAD_SLOT     0x2u  /* a slot_mapping entry >= num_blocks*block_size (not PAD) */
+#define PA_Q8_DEV_WAIT_TIMEOUT 0x4u  /* a bounded in-kernel wait gave up; the output is void */
+
+/* Kernel families for pa_q8_decode_ex. */
+#define PA_Q8_KERNEL_AUTO 0
+#define PA_Q8_KERNEL_CUDA_CORE 1     /* f32 FMA dot products and weighted sums      */
+#define PA_Q8_KERNEL_TENSOR_CORE 2   /* mma.sync f16 tiles with hi/lo split operands */
+
+typedef struct pa_q8_decode_options {
+    int kernel;            /* PA_Q8_KERNEL_*                                           */
+    int partition_tokens;  /* context tokens per split-context partition; 0 = automatic;
+                              otherwise a multiple of 128 and of block_size            */
+} pa_q8_decode_options;
+
+/*
+ * pa_q8_reshape_and_cache -- quantise new K/V rows and scatter them into the
+ * paged int8 caches ("reshape_and_cache_q8.comp", main()).
+ *
+ * For every row i with slot_mapping[i] != 0xFFFFFFFF and every kv head h,
+ * separately for K and V: amax = max_d |x_d|; inv = 127/amax (0 if amax is
+ * 0); code_d = clamp(round(x_d * inv), -127, 127) with halves rounded away
+ * from zero; the codes and the scale word (f32 bits of amax/127, or of 1.0
+ * when amax is 0) are written to the token vector at [slot / block_size,
+ * h, slot % block_size].  Each f32 operation is IEEE round-to-nearest, so
+ * the words are reproducible bit for bit.
+ *
+ *   key, value      device f32; row i, head h starts at key + i*key_stride + h*head_size
+ *   key_stride,
+ *   value_stride    f32 elements between consecutive rows (>= num_kv_heads*head_size)
+ *   key_cache,
+ *   value_cache     device u32 caches (layout above), 4-byte aligned; written in place
+ *   slot_mapping    device u32 [num_tokens]; 0xFFFFFFFF = skip the row; duplicate
+ *                   non-PAD slots are a caller error (unspecified result)
+ *   num_tokens      rows; 0 is a no-op
+ *   num_blocks      physical blocks in each cache; slots >= num_blocks*block_size are
+ *                   skipped and flagged PA_Q8_DEV_BAD_SLOT
+ *   stream          cudaStream_t or NULL
+ * Alignment: none required; 16-byte aligned rows (key/value pointers and strides
+ * multiples of 4 floats) take the vector-load kernel.
+ */
+int pa_q8_reshape_and_cache(const float *key, const float *value,
+                            uint32_t *key_cache, uint32_t *value_cache,
+                            const uint32_t *slot_mapping, int64_t num_tokens,
+                            int64_t key_stride, int64_t value_stride,
+                            int num_kv_heads, int head_size, int block_size,
+                            int64_t num_blocks, void *stream);
+
+/*
+ * pa_q8_decode -- single-query paged attention over the int8 caches
+ * ("paged_attn_q8.comp": output = softmax(scale * q . K^T) . V per (seq,
+ * head), K and V dequantised as code * token scale; the split-context
+ * partials and their log-sum-exp merge follow the split-T decode and
+ * attn_combine steps of "attention.rs", attention_b).
+ *
+ *   out             device f32 [num_seqs][num_heads][head_size] (written; 16-byte aligned)
+ *   q               device f32 [num_seqs][num_heads][head_size] (16-byte aligned)
+ *   key_cache,
+ *   value_cache     device u32 caches, 16-byte aligned; block_size % 4 == 0 makes every
+ *                   (block, kv head) tile a 16-byte aligned run of block_size*(head_size+4)
+ *                   bytes, which the kernels copy whole
+ *   block_tables    device u32 [num_seqs][max_blocks_per_seq]
+ *   context_lens    device u32 [num_seqs]; 0 gives a zero output row
+ *   num_blocks      physical blocks; table entries >= num_blocks are skipped and flagged
+ *   scale           softmax scale (e.g. 1/sqrt(head_size))
+ *   workspace       device scratch of >= pa_q8_decode_workspace_size() bytes,
+ *                   16-byte aligned (may be NULL when that size is 0); its contents
+ *                   need no initialisation and are overwritten
+ *   stream          cudaStream_t or NULL
+ * Concurrent calls on different streams need different workspaces.
+ */
+int pa_q8_decode(float *out, const float *q,
+                 const uint32_t *key_cache, const uint32_t *value_cache,
+                 const uint32_t *block_tables, const uint32_t *context_lens,
+                 int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                 int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                 float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes pa_q8_decode needs for these sizes (0 when no sequence can
+ * span more than one partition).  Returns 0 as well for invalid sizes; the
+ * decode call reports those. */
+size_t pa_q8_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                   int head_size, int block_size, int max_blocks_per_seq);
+
+/* pa_q8_decode with an explicit kernel family and partition size (opts may
+ * be NULL = automatic).  Every choice computes the same result within f32
+ * rounding. */
+int pa_q8_decode_ex(float *out, const float *q,
+                    const uint32_t *key_cache, const uint32_t *value_cache,
+                    const uint32_t *block_tables, const uint32_t *context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                    int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                    float scale, void *workspace, size_t workspace_bytes, void *stream,
+                    const pa_q8_decode_options *opts);
+
+size_t pa_q8_decode_workspace_size_ex(int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_size, int block_size, int max_blocks_per_seq,
+                                      const pa_q8_decode_options *opts);
+
+/* The launch plan pa_q8_decode_ex would use (no launch): kernel family,
+ * tokens per partition, partitions per sequence (grid x), CTAs launched for
+ * the attention kernel.  Any output pointer may be NULL.  Needs a current
+ * CUDA device (it reads the SM count). */
+int pa_q8_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                      int block_size, int max_blocks_per_seq,
+                      const pa_q8_decode_options *opts, int *kernel, int *partition_tokens,
+                      int *num_partitions, int64_t *num_ctas);
+
+/* Read (and with clear != 0, reset) the sticky device status bits of the
+ * current device.  Synchronises `stream` first. */
+int pa_q8_device_status(uint32_t *bits, int clear, void *stream);
+
+/* Launch a one-CTA kernel that waits on a barrier nothing will release,
+ * with the given limit in microseconds (1..10^6).  The kernel gives up,
+ * sets PA_Q8_DEV_WAIT_TIMEOUT and exits; the context stays usable.  This
+ * is how the bounded-wait path of the decode kernels is exercised without
+ * faulting or hanging a GPU. */
+int pa_q8_selftest_wait_timeout(uint32_t timeout_us, void *stream);
+
+/* Human-readable text for a pa_q8_status value (static storage). */
+const char *pa_q8_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_q8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_Q8_H */

@@ -1,0 +1,259 @@
+// C ABI of libpa_q8.so: argument checks, launch planning, status strings.
+// Every check happens on the host before anything is queued; the kernels
+// are in writer.cu and decode.cu.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pa_q8.h"
+#include "kernels.h"
+
+namespace {
+
+// Per-device sticky status bits written by the kernels.
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t *g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+// Device address of the status word and the SM count of the current device,
+// looked up once per device.
+int device_info(uint32_t **status, int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        int sms = 0;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_Q8_ECUDA;
+        }
+        g_status_ptr[dev] = static_cast<uint32_t *>(p);
+        g_num_sms[dev] = sms;
+    }
+    if (status) *status = g_status_ptr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return PA_Q8_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+bool head_size_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
+                       int max_blocks_per_seq) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
+        max_blocks_per_seq <= 0)
+        return PA_Q8_EINVAL;
+    if (num_heads % num_kv_heads != 0 || head_size % 4 != 0 || block_size % 4 != 0) return PA_Q8_EINVAL;
+    if (!head_size_ok(head_size) || !pow2(block_size) || block_size > 1024) return PA_Q8_EUNSUPPORTED;
+    if (num_seqs > 65535) return PA_Q8_EUNSUPPORTED;            // grid z
+    if ((int64_t)num_kv_heads * ((num_heads / num_kv_heads + 15) / 16 + 1) > 65535)
+        return PA_Q8_EUNSUPPORTED;                              // grid y
+    if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30) return PA_Q8_EUNSUPPORTED;
+    return PA_Q8_OK;
+}
+
+int plan_for(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int num_sms) {
+    const int kernel = opts ? opts->kernel : PA_Q8_KERNEL_AUTO;
+    const int pt = opts ? opts->partition_tokens : 0;
+    if (kernel < PA_Q8_KERNEL_AUTO || kernel > PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
+    if (pt < 0 || (pt > 0 && pt % 128 != 0)) return PA_Q8_EINVAL;
+    if (!pa_q8::make_plan(a, kernel, pt, num_sms)) return PA_Q8_EUNSUPPORTED;
+    return PA_Q8_OK;
+}
+
+void fill_shape(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                int block_size, int max_blocks_per_seq) {
+    std::memset(&a, 0, sizeof a);
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.block_size = block_size;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_q8_version(void) { return 10000; }
+
+const char *pa_q8_status_string(int status) {
+    switch (status) {
+        case PA_Q8_OK: return "ok";
+        case PA_Q8_EINVAL: return "invalid argument";
+        case PA_Q8_EUNSUPPORTED: return "unsupported shape (head_size 64/128/256, block_size a power of two 4..1024)";
+        case PA_Q8_EALIGN: return "misaligned pointer or stride";
+        case PA_Q8_ECUDA: return "CUDA runtime error";
+        case PA_Q8_EWORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+int pa_q8_reshape_and_cache(const float *key, const float *value, uint32_t *key_cache,
+                            uint32_t *value_cache, const uint32_t *slot_mapping, int64_t num_tokens,
+                            int64_t key_stride, int64_t value_stride, int num_kv_heads, int head_size,
+                            int block_size, int64_t num_blocks, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_Q8_EINVAL;
+    if (head_size % 4 != 0 || block_size % 4 != 0) return PA_Q8_EINVAL;
+    if (!head_size_ok(head_size)) return PA_Q8_EUNSUPPORTED;
+    if (key_stride < (int64_t)num_kv_heads * head_size || value_stride < (int64_t)num_kv_heads * head_size)
+        return PA_Q8_EINVAL;
+    if (num_blocks * block_size > (int64_t)0xFFFFFFFFu) return PA_Q8_EUNSUPPORTED;
+    if (num_tokens == 0) return PA_Q8_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_Q8_EINVAL;
+    if (!aligned4(key) || !aligned4(value) || !aligned4(key_cache) || !aligned4(value_cache) ||
+        !aligned4(slot_mapping))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int rc = device_info(&status, nullptr);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::WriterArgs a{key, value, key_cache, value_cache, slot_mapping, num_tokens, key_stride,
+                        value_stride, num_kv_heads, head_size, block_size, num_blocks, status};
+    if (pa_q8::launch_writer(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
+size_t pa_q8_decode_workspace_size_ex(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                      int block_size, int max_blocks_per_seq,
+                                      const pa_q8_decode_options *opts) {
+    if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq) !=
+        PA_Q8_OK)
+        return 0;
+    pa_q8::DecodeArgs a;
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
+    int sms = 0;
+    if (device_info(nullptr, &sms) != PA_Q8_OK) sms = 152;     // size query without a device
+    if (plan_for(a, opts, sms) != PA_Q8_OK) return 0;
+    return pa_q8::plan_workspace_bytes(a);
+}
+
+size_t pa_q8_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                   int block_size, int max_blocks_per_seq) {
+    return pa_q8_decode_workspace_size_ex(num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                          max_blocks_per_seq, nullptr);
+}
+
+int pa_q8_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
+                      int max_blocks_per_seq, const pa_q8_decode_options *opts, int *kernel,
+                      int *partition_tokens, int *num_partitions, int64_t *num_ctas) {
+    int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
+    if (rc != PA_Q8_OK) return rc;
+    int sms = 0;
+    rc = device_info(nullptr, &sms);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::DecodeArgs a;
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
+    rc = plan_for(a, opts, sms);
+    if (rc != PA_Q8_OK) return rc;
+    if (kernel) *kernel = a.kernel;
+    if (partition_tokens) *partition_tokens = a.partition_tokens;
+    if (num_partitions) *num_partitions = a.num_partitions;
+    if (num_ctas) *num_ctas = pa_q8::plan_num_ctas(a);
+    return PA_Q8_OK;
+}
+
+int pa_q8_decode_ex(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                    const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_heads,
+                    int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                    int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
+                    const pa_q8_decode_options *opts) {
+    int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
+    if (rc != PA_Q8_OK) return rc;
+    if (num_blocks <= 0) return PA_Q8_EINVAL;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens) return PA_Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        !aligned4(block_tables) || !aligned4(context_lens))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int sms = 0;
+    rc = device_info(&status, &sms);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::DecodeArgs a;
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
+    rc = plan_for(a, opts, sms);
+    if (rc != PA_Q8_OK) return rc;
+    const size_t need = pa_q8::plan_workspace_bytes(a);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return PA_Q8_EWORKSPACE;
+        if (!aligned16(workspace)) return PA_Q8_EALIGN;
+        const size_t rows = (size_t)num_seqs * num_heads * a.num_partitions;
+        const size_t ml_bytes = ((rows * 2 * sizeof(float) + 255) / 256) * 256;
+        a.partial_ml = static_cast<float *>(workspace);
+        a.partial_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + ml_bytes);
+    }
+    a.out = out;
+    a.q = q;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.status = status;
+    if (pa_q8::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
+int pa_q8_decode(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                 const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_heads,
+                 int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                 float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    return pa_q8_decode_ex(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs, num_heads,
+                           num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale, workspace,
+                           workspace_bytes, stream, nullptr);
+}
+
+int pa_q8_device_status(uint32_t *bits, int clear, void *stream) {
+    if (!bits) return PA_Q8_EINVAL;
+    uint32_t *status = nullptr;
+    int rc = device_info(&status, nullptr);
+    if (rc != PA_Q8_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(bits, status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    if (clear && *bits) {
+        if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess) {
+            cudaGetLastError();
+            return PA_Q8_ECUDA;
+        }
+    }
+    return PA_Q8_OK;
+}
+
+int pa_q8_selftest_wait_timeout(uint32_t timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return PA_Q8_EINVAL;
+    uint32_t *status = nullptr;
+    int rc = device_info(&status, nullptr);
+    if (rc != PA_Q8_OK) return rc;
+    if (pa_q8::launch_wait_selftest(timeout_us, status, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
+}  // extern "C"

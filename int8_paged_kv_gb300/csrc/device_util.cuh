@@ -1,0 +1,180 @@
+// Device helpers for the pa_q8 kernels (sm_103a): mbarriers, 1-D bulk
+// copies global -> shared, bounded waits, warp reductions and the f16 tensor
+// core tile.  Inline PTX only; no library code.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace pa_q8 {
+
+constexpr uint32_t kPadSlot = 0xFFFFFFFFu;
+constexpr uint32_t kDevBadBlock = 0x1u;
+constexpr uint32_t kDevBadSlot = 0x2u;
+constexpr uint32_t kDevWaitTimeout = 0x4u;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a stage wait normally takes microseconds
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void flag_error(uint32_t *status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.release.cta.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// limit_ns of global time.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------ bulk copies
+
+// One contiguous run of `bytes` (multiple of 16; both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory; completion is
+// counted on `bar` as transaction bytes.  Streaming data: evict-first in L2.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ------------------------------------------------------------------- misc
+
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// bar.sync over `threads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// (a & b) ^ c in one LOP3
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Two f16 lanes 0x64XX (= 1024 + XX) minus 1152 -> the signed codes XX - 128.
+__device__ __forceinline__ uint32_t sub_1152_x2(uint32_t v) {
+    uint32_t d;
+    const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(bias));
+    return d;
+}
+
+// Codes in byte lanes 0,1 (lo) and 2,3 (hi) of a word -> two f16x2 values.
+// Exact: every int8 is an f16.
+__device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;         // two's complement -> offset binary
+    lo = sub_1152_x2(prmt(u, 0x64646464u, 0x4140u));
+    hi = sub_1152_x2(prmt(u, 0x64646464u, 0x4342u));
+}
+
+// Byte lane e of a and of b -> f16x2 (code_a[e], code_b[e]).
+template <int E>
+__device__ __forceinline__ uint32_t codes_pair_to_f16x2(uint32_t a, uint32_t b) {
+    // d = [a.e, a.e, b.e, b.e]; bytes 1 and 3 are then replaced by 0x64
+    constexpr uint32_t sel = (uint32_t)E | ((uint32_t)E << 4) | ((uint32_t)(E + 4) << 8) |
+                             ((uint32_t)(E + 4) << 12);
+    return sub_1152_x2(and_xor(prmt(a, b, sel), 0x00FF00FFu, 0x64806480u));
+}
+
+// D = A(16x16, f16, row) * B(16x8, f16, col) + D, f32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// x = hi + lo with hi = f16(x), lo = f16(x - hi): 22 significant bits.
+__device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
+    hi = __float2half_rn(x);
+    lo = __float2half_rn(x - __half2float(hi));
+}
+
+}  // namespace pa_q8

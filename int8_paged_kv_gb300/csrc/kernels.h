@@ -1,0 +1,76 @@
+// Internal launch interface between the C-ABI layer (abi.cu) and the
+// kernels.  Host-side structs only; argument checking happens in abi.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa_q8 {
+
+struct WriterArgs {
+    const float *key;
+    const float *value;
+    uint32_t *key_cache;
+    uint32_t *value_cache;
+    const uint32_t *slot_mapping;
+    int64_t num_tokens;
+    int64_t key_stride;
+    int64_t value_stride;
+    int num_kv_heads;
+    int head_size;
+    int block_size;
+    int64_t num_blocks;
+    uint32_t *status;
+};
+
+cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream);
+
+enum KernelFamily { kAuto = 0, kCudaCore = 1, kTensorCore = 2 };
+
+struct DecodeArgs {
+    float *out;
+    const float *q;
+    const uint32_t *key_cache;
+    const uint32_t *value_cache;
+    const uint32_t *block_tables;
+    const uint32_t *context_lens;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int head_size;
+    int block_size;
+    int max_blocks_per_seq;
+    int64_t num_blocks;
+    float scale;
+    // plan (filled by make_plan)
+    int kernel;            // kCudaCore or kTensorCore
+    int partition_tokens;  // tokens per partition
+    int num_partitions;    // partitions per sequence (grid x)
+    int heads_per_cta;     // query heads one CTA serves (one kv head's group, or part of it)
+    int head_groups;       // CTAs per (seq, kv head, partition) along the group
+    // split-context scratch: m,l [S][H][P][2] then acc [S][H][P][D] (f32)
+    float *partial_ml;
+    float *partial_acc;
+    uint32_t *status;
+};
+
+struct DecodePlanLimits {
+    int num_sms;
+};
+
+// Fill the plan fields of `a` (kernel family, partition size, grid).
+// Returns false if no kernel serves these sizes.
+bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int num_sms);
+
+// Workspace bytes for a plan (0 when num_partitions == 1).
+size_t plan_workspace_bytes(const DecodeArgs &a);
+
+// Grid size of the attention kernel for a plan.
+int64_t plan_num_ctas(const DecodeArgs &a);
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(uint32_t timeout_us, uint32_t *status, cudaStream_t stream);
+
+}  // namespace pa_q8

@@ -1,0 +1,80 @@
+"""Shared pieces of the GPU parity tests: moving workloads to the device,
+running the library through its binding, and running the oracle on the
+same inputs.  u32 buffers travel as int32 tensors (same bits)."""
+import numpy as np
+import torch
+
+import int8_paged_kv_gb300 as pk
+import oracle
+from int8_paged_kv_gb300 import workloads as wl
+
+POISON = 0xFFFFFFFF      # a NaN bit pattern: unused cache words must never be read
+
+
+def dev_u32(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).cuda()
+
+
+def host_u32(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint32)
+
+
+def poisoned_cache(w, fill=POISON):
+    return wl.empty_cache(w, fill)
+
+
+def gpu_write(key, value, slots, cache_k, cache_v, cfg, num_blocks=None):
+    """Run the writer on device copies; key/value: numpy f32 (2-D row views allowed)."""
+    kd = torch.from_numpy(np.ascontiguousarray(key)).cuda() if key.flags.c_contiguous else None
+    if kd is None:
+        raise ValueError("use gpu_write_rows for strided rows")
+    vd = torch.from_numpy(np.ascontiguousarray(value)).cuda()
+    kc, vc = dev_u32(cache_k), dev_u32(cache_v)
+    pk.pa_q8_reshape_and_cache(kd.reshape(kd.shape[0], -1), vd.reshape(vd.shape[0], -1), kc, vc,
+                               dev_u32(slots), num_kv_heads=cfg.num_kv_heads,
+                               head_size=cfg.head_size, block_size=cfg.block_size,
+                               num_blocks=num_blocks)
+    return kc, vc
+
+
+def oracle_write(key, value, slots, cache_k, cache_v, cfg):
+    oracle.reshape_and_cache(key, value, cache_k, cache_v, slots, num_kv_heads=cfg.num_kv_heads,
+                             head_size=cfg.head_size, block_size=cfg.block_size)
+
+
+def gpu_decode(w, kc, vc, *, kernel=0, partition_tokens=0, q=None, bt=None, cl=None, out=None):
+    q = torch.from_numpy(w.q if q is None else q).cuda()
+    bt = dev_u32(w.block_tables if bt is None else bt)
+    cl = dev_u32(w.context_lens if cl is None else cl)
+    out = torch.full_like(q, float("nan")) if out is None else out
+    pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=w.cfg.num_kv_heads,
+                    block_size=w.cfg.block_size, scale=w.scale, kernel=kernel,
+                    partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def oracle_decode(w, kc, vc, rows=None, q=None, bt=None, cl=None):
+    return oracle.decode(w.q if q is None else q, kc, vc,
+                         w.block_tables if bt is None else bt,
+                         w.context_lens if cl is None else cl,
+                         num_kv_heads=w.cfg.num_kv_heads, block_size=w.cfg.block_size,
+                         scale=w.scale, rows=rows)
+
+
+def assert_close(got, want, what=""):
+    """|got - want| <= 1e-5 + 1e-4 |want| elementwise (want from the oracle)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    bound = 1e-5 + 1e-4 * np.abs(want)
+    ratio = err / bound
+    worst = np.unravel_index(np.argmax(ratio), ratio.shape)
+    assert np.all(err <= bound), (f"{what}: {int((err > bound).sum())} of {err.size} outside "
+                                  f"tolerance; worst at {worst}: got {got[worst]}, want {want[worst]}")
+    return float(ratio.max())
+
+
+def device_status(clear=True):
+    return pk.pa_q8_device_status(clear=clear)

@@ -1,0 +1,208 @@
+"""GPU decode (pa_q8_decode) against the fp64 oracle:
+|gpu - oracle| <= 1e-5 + 1e-4 |oracle| elementwise, for both kernel
+families, on all five workloads (full-size ones on sampled rows, in the
+launch configuration the benchmark times), and on edge cases: empty and
+one-token contexts, ragged tails next to poisoned (NaN) cache words,
+clamped contexts, every supported block size, GQA ratios 1..32, partition
+sizes, a block id out of range, and the bounded-wait path."""
+import numpy as np
+import pytest
+
+from int8_paged_kv_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TC, CC = 2, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int8_paged_kv_gb300 import build
+    build.build()
+    import oracle
+    oracle.build()
+
+
+_CACHE = {}
+
+
+def _setup(name):
+    """Workload, oracle-written caches (numpy) and GPU-written caches (device)."""
+    if name in _CACHE:
+        return _CACHE[name]
+    from tests.gpu_helpers import gpu_write, host_u32, oracle_write, poisoned_cache
+    w = wl.build(name, with_append=False)
+    cfg = w.cfg
+    ok_, ov_ = poisoned_cache(w), poisoned_cache(w)
+    oracle_write(w.key, w.value, w.slot_mapping, ok_, ov_, cfg)
+    kc, vc = gpu_write(w.key, w.value, w.slot_mapping, poisoned_cache(w), poisoned_cache(w), cfg)
+    assert np.array_equal(host_u32(kc), ok_) and np.array_equal(host_u32(vc), ov_)
+    w.key = w.value = None                      # free host memory
+    _CACHE.clear()
+    _CACHE[name] = (w, ok_, ov_, kc, vc)
+    return _CACHE[name]
+
+
+def _rows(w, n, seed=0):
+    """n sampled (s, h) rows, always including the longest and shortest contexts."""
+    rng = np.random.default_rng(seed)
+    S, H = w.cfg.num_seqs, w.cfg.num_heads
+    pick = {(int(np.argmax(w.context_lens)), 0), (int(np.argmin(w.context_lens)), H - 1)}
+    while len(pick) < min(n, S * H):
+        pick.add((int(rng.integers(S)), int(rng.integers(H))))
+    return np.array(sorted(pick), dtype=np.int32)
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "edge"])
+def test_small_configs_all_rows(name, kernel):
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode, oracle_decode
+    w, ok_, ov_, kc, vc = _setup(name)
+    want = oracle_decode(w, ok_, ov_)
+    got = gpu_decode(w, kc, vc, kernel=kernel)
+    assert_close(got, want, f"{name} kernel {kernel}")
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [0, TC, CC])
+@pytest.mark.parametrize("name", ["long", "large"])
+def test_full_size_sampled_rows(name, kernel):
+    """Full-size workloads in the benchmark's launch configuration (kernel 0 =
+    the automatic plan); the oracle checks sampled rows."""
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode, oracle_decode
+    w, ok_, ov_, kc, vc = _setup(name)
+    rows = _rows(w, 48 if name == "long" else 160, seed=kernel)
+    want = oracle_decode(w, ok_, ov_, rows=rows)
+    got = gpu_decode(w, kc, vc, kernel=kernel)
+    assert_close(got[rows[:, 0], rows[:, 1]], want, f"{name} kernel {kernel}")
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("pt", [128, 256, 1024, 4096])
+def test_partition_invariance(kernel, pt):
+    """The split-context partition size changes nothing beyond tolerance."""
+    from tests.gpu_helpers import assert_close, gpu_decode, oracle_decode
+    w, ok_, ov_, kc, vc = _setup("llama8b")
+    want = oracle_decode(w, ok_, ov_)
+    got = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+    assert_close(got, want, f"pt {pt}")
+
+
+def _random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0):
+    """A poisoned paged cache written by both writers (checked equal)."""
+    import torch
+    import int8_paged_kv_gb300 as pk
+    from tests.gpu_helpers import dev_u32, host_u32
+    import oracle
+    rng = np.random.default_rng(seed)
+    nblk = [-(-int(c) // B) for c in lens]
+    Nb = Nb or max(1, max(nblk))
+    pool = sum(nblk) + 3
+    perm = rng.permutation(pool).astype(np.uint32)
+    bt = np.full((S, Nb), 0xFFFFFFFF, dtype=np.uint32)
+    pos = 0
+    for s in range(S):
+        bt[s, :nblk[s]] = perm[pos:pos + nblk[s]]
+        pos += nblk[s]
+    T = int(sum(lens))
+    key = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
+    val = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
+    slots = np.concatenate([(bt[s, np.arange(c) // B].astype(np.int64) * B + np.arange(c) % B)
+                            for s, c in enumerate(lens) if c > 0] or [np.zeros(0, np.int64)]).astype(np.uint32)
+    W = D // 4 + 1
+    ok_ = np.full((pool, Hk, B, W), 0xFFFFFFFF, dtype=np.uint32)
+    ov_ = ok_.copy()
+    oracle.reshape_and_cache(key, val, ok_, ov_, slots, num_kv_heads=Hk, head_size=D, block_size=B)
+    kc, vc = dev_u32(ok_.copy()), dev_u32(ov_.copy())
+    kc.fill_(-1)
+    vc.fill_(-1)
+    if T:
+        pk.pa_q8_reshape_and_cache(torch.from_numpy(key.reshape(T, -1)).cuda(),
+                                   torch.from_numpy(val.reshape(T, -1)).cuda(), kc, vc,
+                                   dev_u32(slots), num_kv_heads=Hk, head_size=D, block_size=B)
+    assert np.array_equal(host_u32(kc), ok_) and np.array_equal(host_u32(vc), ov_)
+    q = rng.standard_normal((S, H, D)).astype(np.float32)
+    cfg = wl.Config("case", 99, S, H, Hk, D, B, Nb * B)
+    w = wl.Workload(cfg=cfg, context_lens=np.asarray(lens, dtype=np.uint32), block_tables=bt,
+                    num_blocks=pool, q=q, scale=float(np.float32(scale_mult / np.sqrt(D))),
+                    key=None, value=None, slot_mapping=slots, row_seq=None)
+    return w, ok_, ov_, kc, vc
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("B", [4, 8, 16, 32, 64, 128, 256])
+def test_block_sizes_and_ragged_tails(kernel, B):
+    from tests.gpu_helpers import assert_close, gpu_decode, oracle_decode
+    lens = [1, B - 1, B + 1, 3 * B + 7, 700, 129, 0, 2 * B]
+    w, ok_, ov_, kc, vc = _random_case(len(lens), 8, 2, 128, B, lens, seed=B)
+    want = oracle_decode(w, ok_, ov_)
+    for pt in (0, 128, 384):
+        got = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+        assert_close(got, want, f"B {B} pt {pt}")
+        assert np.all(got[6] == 0.0)              # empty context -> zero rows
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("H,Hk,D", [(4, 4, 64), (8, 4, 64), (12, 1, 128), (16, 2, 128),
+                                    (32, 1, 128), (16, 1, 256), (8, 8, 256), (24, 2, 64)])
+def test_gqa_ratios_and_head_sizes(kernel, H, Hk, D):
+    from tests.gpu_helpers import assert_close, gpu_decode, oracle_decode
+    lens = [1, 17, 300, 1000]
+    w, ok_, ov_, kc, vc = _random_case(4, H, Hk, D, 16, lens, seed=H * 7 + Hk + D)
+    want = oracle_decode(w, ok_, ov_)
+    for pt in (0, 256):
+        assert_close(gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt), want,
+                     f"H {H} Hk {Hk} D {D} pt {pt}")
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+def test_clamped_context_and_value_ranges(kernel):
+    """context_len beyond max_blocks*B is clamped; large and tiny value
+    magnitudes and sharp softmax (scale x 30) stay within tolerance."""
+    from tests.gpu_helpers import assert_close, gpu_decode, oracle_decode
+    lens = [64, 200, 50]
+    for dist, sm in ((1.0, 1.0), (1e3, 1e-3), (1e-3, 1e3), (1.0, 30.0)):
+        w, ok_, ov_, kc, vc = _random_case(3, 8, 2, 128, 16, lens, seed=5, scale_mult=sm, dist=dist)
+        cl = np.array([64, 10_000, 50], dtype=np.uint32)   # seq 1 clamps to Nb*B = 208
+        want = oracle_decode(w, ok_, ov_, cl=cl)
+        got = gpu_decode(w, kc, vc, kernel=kernel, cl=cl)
+        assert_close(got, want, f"dist {dist} scale x{sm}")
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+def test_bad_block_id_is_skipped_and_flagged(kernel):
+    from tests.gpu_helpers import device_status, gpu_decode
+    import int8_paged_kv_gb300 as pk
+    w, ok_, ov_, kc, vc = _random_case(2, 8, 2, 128, 16, [40, 40], seed=9)
+    bt = w.block_tables.copy()
+    bt[1, 1] = 1 << 30                         # inside the context, out of the pool
+    device_status(clear=True)
+    out = gpu_decode(w, kc, vc, kernel=kernel, bt=bt)
+    assert device_status(clear=True) & pk.PA_Q8_DEV_BAD_BLOCK
+    # sequence 0 is unaffected
+    from tests.gpu_helpers import assert_close, oracle_decode
+    want = oracle_decode(w, ok_, ov_)
+    assert_close(out[0], want[0], "untouched sequence")
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    import torch
+    import int8_paged_kv_gb300 as pk
+    from tests.gpu_helpers import device_status
+    device_status(clear=True)
+    pk.pa_q8_selftest_wait_timeout(2000)       # 2 ms on a barrier nothing releases
+    torch.cuda.synchronize()
+    assert device_status(clear=True) & pk.PA_Q8_DEV_WAIT_TIMEOUT
+    x = torch.ones(1024, device="cuda")
+    assert float((x * 2).sum()) == 2048.0      # the context still works
+    assert device_status() == 0
+
+
+def test_plan_is_what_the_benchmark_times():
+    import int8_paged_kv_gb300 as pk
+    cfg = wl.CONFIGS["large"]
+    plan = pk.pa_q8_decode_plan(cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size,
+                                cfg.block_size, cfg.max_blocks_per_seq)
+    assert plan["kernel"] in (TC, CC) and plan["partition_tokens"] % 128 == 0
+    assert plan["num_partitions"] * plan["partition_tokens"] >= cfg.max_context
