@@ -87,6 +87,12 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// Order this thread's earlier shared-memory accesses (made visible to it by
+// a preceding __syncwarp / bar.sync) before its later async-proxy copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -175,6 +181,15 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 __device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
     hi = __float2half_rn(x);
     lo = __float2half_rn(x - __half2float(hi));
+}
+
+// The same split for a pair (a, b) -> packed f16x2 hi = (hi(a), hi(b)) and
+// lo = (lo(a), lo(b)); a sits in the low half.
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const __half2 l = __floats2half2_rn(a - __low2float(h), b - __high2float(h));
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 }  // namespace pa_q8

@@ -184,8 +184,10 @@ def build(name: str, *, with_kv: bool = True, with_append: bool = True,
     c = _context_lens(cfg, rng)
     nblk = -(-c.astype(np.int64) // B)
     n_ctx_blocks = int(nblk.sum())
-    T_append = 16384 if (cfg.name == "large" and with_append) else 0
-    n_extra = -(-(T_append * 5 // 4) // B) if T_append else 0
+    # the block pool (and so every block table) does not depend on with_append
+    T_planned = 16384 if cfg.name == "large" else 0
+    T_append = T_planned if with_append else 0
+    n_extra = -(-(T_planned * 5 // 4) // B) if T_planned else 0
     if cfg.name == "tiny":
         pool = 16
     else:
@@ -341,3 +343,45 @@ def algorithmic_writer_bytes(num_kv_heads: int, head_size: int, slot_mapping: np
     rd = n * num_kv_heads * head_size * 4 * 2
     wr = n * num_kv_heads * (head_size + 4) * 2
     return rd + wr + slot_mapping.size * 4
+
+
+def subset(w: Workload, n_seqs: int) -> Workload:
+    """The first n_seqs sequences of a workload with a compact block pool
+    (their blocks renumbered in pool order) and, if present, the matching
+    share of the append rows redirected into fresh free blocks.  Used for
+    small profiling captures of the same kernels."""
+    cfg = w.cfg
+    B = cfg.block_size
+    n = int(n_seqs)
+    c = w.context_lens[:n].copy()
+    bt_old = w.block_tables[:n]
+    used = bt_old[bt_old != UNUSED_BLOCK]
+    remap = {int(b): i for i, b in enumerate(np.sort(used))}
+    bt = np.full_like(bt_old, UNUSED_BLOCK)
+    for s in range(n):
+        k = -(-int(c[s]) // B)
+        bt[s, :k] = [remap[int(b)] for b in bt_old[s, :k]]
+    rows = w.row_seq < n
+    rows &= w.row_seq >= 0
+    slots = w.slot_mapping[rows].copy()
+    slots = np.array([remap[int(sl) // B] * B + int(sl) % B for sl in slots], dtype=np.uint32) \
+        if slots.size else slots
+    pool = len(remap)
+    append = None
+    if w.append is not None:
+        a = w.append
+        T = max(1, a.num_tokens * n // cfg.num_seqs)
+        sm = a.slot_mapping[:T].copy()
+        live = sm != PAD_SLOT
+        extra = -(-int(live.sum()) // B)
+        sm[live] = (pool * B + np.random.default_rng([cfg.seed, 7]).permutation(extra * B)[:int(live.sum())]
+                    ).astype(np.uint32)
+        append = Append(fused=a.fused[:T], key_offset=a.key_offset, value_offset=a.value_offset,
+                        row_stride=a.row_stride, slot_mapping=sm)
+        pool += extra
+    sub_cfg = Config(cfg.name, cfg.index, n, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, B,
+                     cfg.max_context, cfg.description + f" (first {n} sequences)")
+    return Workload(cfg=sub_cfg, context_lens=c, block_tables=bt, num_blocks=pool, q=w.q[:n].copy(),
+                    scale=w.scale, key=None if w.key is None else w.key[rows],
+                    value=None if w.value is None else w.value[rows], slot_mapping=slots,
+                    row_seq=w.row_seq[rows].copy(), append=append, notes=dict(w.notes))
