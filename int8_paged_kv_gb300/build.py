@@ -40,7 +40,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "pa_q8.h"))
     cc = nvcc()
-    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
+    include = os.path.join(os.path.dirname(HERE), "include")
+    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-I", include, "-Xcompiler", "-fPIC",
+                    "-Xcompiler", "-O2"]
+    flags += os.environ.get("PA_Q8_NVCC_FLAGS", "").split()
     if verbose:
         flags += ["-Xptxas", "-v"]
 

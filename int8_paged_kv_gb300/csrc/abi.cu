@@ -7,7 +7,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/pa_q8.h"
+#include "pa_q8.h"
 #include "kernels.h"
 
 namespace {

@@ -39,7 +39,8 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kChunk = 32;                 // tokens per warp chunk
-constexpr int kVScaleBias = 139;           // weights carry 2^(139 - E): below 2^13
+constexpr int kLazy = 8;                   // rescale only when a logit passes the reference max by 2^8
+constexpr int kVScaleBias = 131;           // weights carry 2^(131 - E): p * vs * 2^(131-E) < 2^13
 
 #ifndef PA_Q8_TC_SLOTS
 #define PA_Q8_TC_SLOTS 4                   // token-slot warps per head tile
@@ -65,6 +66,8 @@ struct Params {
     const uint32_t *bt;
     const uint32_t *cl;
     int S, H, Hk, B, Nb;
+    int log2B;              // block_size is a power of two
+    int log2ptok;           // piece = min(block_size, 32) tokens
     int64_t num_blocks;
     float scale_log2;       // scale * log2(e)
     int PT;                 // tokens per partition
@@ -142,12 +145,11 @@ __host__ __device__ inline Layout make_layout(int D, int streams, int ring, int 
 // Load the partition's block-table slice (one entry per piece of
 // min(B, 32) tokens); entries out of range become kPadSlot and are flagged.
 __device__ void load_table(const Params &P, const Work &w, uint32_t *table) {
-    const int ptok = P.B < kChunk ? P.B : kChunk;
-    const int n = (w.len + ptok - 1) / ptok;
+    const int n = (w.len + (1 << P.log2ptok) - 1) >> P.log2ptok;
     const uint32_t *row = P.bt + (int64_t)w.s * P.Nb;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int tabs = w.t_begin + i * ptok;
-        uint32_t pb = __ldg(row + tabs / P.B);
+        const int tabs = w.t_begin + (i << P.log2ptok);
+        uint32_t pb = __ldg(row + (tabs >> P.log2B));
         if ((int64_t)pb >= P.num_blocks) {
             flag_error(P.status, kDevBadBlock);
             pb = kPadSlot;
@@ -164,16 +166,15 @@ __device__ __forceinline__ void issue_chunk(const Params &P, const Work &w, cons
                                             int c, uint32_t slot, uint32_t bar, uint64_t policy) {
     constexpr int W = D / 4 + 1;
     const int lane = threadIdx.x & 31;
-    const int ptok = P.B < kChunk ? P.B : kChunk;
-    const int t = c * kChunk + lane * ptok;            // partition-relative token
+    const int t = c * kChunk + (lane << P.log2ptok);   // partition-relative token
     uint32_t bytes = 0;
     int64_t base = 0;
-    if (lane < kChunk / ptok && t < w.len) {
-        const uint32_t pb = table[t / ptok];
+    if (lane < (kChunk >> P.log2ptok) && t < w.len) {
+        const uint32_t pb = table[t >> P.log2ptok];
         if (pb != kPadSlot) {
-            const int tabs = w.t_begin + t;
-            base = ((int64_t)pb * P.Hk + w.g) * ((int64_t)P.B * W) + (int64_t)(tabs % P.B) * W;
-            bytes = (uint32_t)ptok * W * 4;
+            const int off = (w.t_begin + t) & (P.B - 1);
+            base = (((int64_t)pb * P.Hk + w.g) << P.log2B) * W + (int64_t)off * W;
+            bytes = (uint32_t)W * 4 << P.log2ptok;
         }
     }
     const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes) * 2u;
@@ -181,7 +182,7 @@ __device__ __forceinline__ void issue_chunk(const Params &P, const Work &w, cons
     __syncwarp();
     if (bytes) {
         fence_proxy_async_smem();
-        const uint32_t dst = slot + (uint32_t)lane * ptok * W * 4;
+        const uint32_t dst = slot + (((uint32_t)lane * W * 4) << P.log2ptok);
         bulk_copy_g2s(dst, P.kc + base, bytes, bar, policy);
         bulk_copy_g2s(dst + kChunk * W * 4, P.vc + base, bytes, bar, policy);
     }
@@ -205,32 +206,42 @@ __device__ void drain(const Params &P, uint32_t bars, int ring, int consumed, in
 // partition's partial (M, L, A) for the combine kernel.
 template <int D>
 __device__ void merge_and_store(const Params &P, const Work &w, const float *ml, const float *accs,
-                                int n_slots, int heads_stride) {
-    // ml: [slot][head][3] = (m, l, E); accs: [slot][head][D]
-    for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
-        const int hh = i / D, d = i % D;
+                                int n_slots, int heads_stride, float *fac) {
+    // ml: [slot][head][3] = (m, l, E); accs: [slot][head][D]; fac: scratch
+    // [head][n_slots + 2] = per-slot factors, M, L.  Called by every thread.
+    for (int hh = threadIdx.x; hh < w.nh; hh += blockDim.x) {
         float M = -INFINITY;
         for (int sl = 0; sl < n_slots; ++sl) M = fmaxf(M, ml[(sl * heads_stride + hh) * 3]);
-        float Lsum = 0.0f, A = 0.0f;
-        if (M != -INFINITY) {
-            for (int sl = 0; sl < n_slots; ++sl) {
-                const float *e = ml + (sl * heads_stride + hh) * 3;
-                if (e[0] == -INFINITY) continue;
+        float Lsum = 0.0f;
+        float *f = fac + hh * (n_slots + 2);
+        for (int sl = 0; sl < n_slots; ++sl) {
+            const float *e = ml + (sl * heads_stride + hh) * 3;
+            float x = 0.0f;
+            if (e[0] != -INFINITY) {
                 const float wgt = fast_exp2(e[0] - M);
-                const float unscale = ldexpf(1.0f, __float2int_rn(e[2]) - kVScaleBias);
                 Lsum += e[1] * wgt;
-                A += accs[(sl * heads_stride + hh) * D + d] * (wgt * unscale);
+                x = wgt * ldexpf(1.0f, __float2int_rn(e[2]) - kVScaleBias);
             }
+            f[sl] = x;
         }
+        f[n_slots] = M;
+        f[n_slots + 1] = Lsum;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
+        const int hh = i / D, d = i % D;
+        const float *f = fac + hh * (n_slots + 2);
+        float A = 0.0f;
+        for (int sl = 0; sl < n_slots; ++sl) A = fmaf(accs[(sl * heads_stride + hh) * D + d], f[sl], A);
         const int h = w.h0 + hh;
         if (w.single) {
-            P.out[((int64_t)w.s * P.H + h) * D + d] = A / Lsum;
+            P.out[((int64_t)w.s * P.H + h) * D + d] = A / f[n_slots + 1];
         } else {
             const int64_t row = ((int64_t)w.s * P.H + h) * P.NP + w.p;
             P.pacc[row * D + d] = A;
             if (d == 0) {
-                P.pml[row * 2] = M;
-                P.pml[row * 2 + 1] = Lsum;
+                P.pml[row * 2] = f[n_slots];
+                P.pml[row * 2 + 1] = f[n_slots + 1];
             }
         }
     }
@@ -364,6 +375,7 @@ decode_tc_kernel(Params P) {
     int E = 12;                       // running max biased exponent of V scales (>= 12)
     float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
 
+    const F16Consts fk;
     bool ok = true;
     int i = 0;
     for (; i < my_n; ++i) {
@@ -398,14 +410,13 @@ decode_tc_kernel(Params P) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t b0, b1;
-                codes4_to_f16x2(sK[(8 * j + gq) * W + wd], b0, b1);
+                codes4_to_f16x2(sK[(8 * j + gq) * W + wd], b0, b1, fk);
                 mma_16816(s[j], a, b0, b1);
             }
         }
         // ---- online softmax over this thread's 8 tokens: 8j + 2cq + e
         float z[8], vs[8];
-        float cmax = -INFINITY;
-        uint32_t vbits = 0;
+        float cmax = -INFINITY, vmax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -422,19 +433,23 @@ decode_tc_kernel(Params P) {
                 z[2 * j + e] = zz;
                 vs[2 * j + e] = vv;
                 cmax = fmaxf(cmax, zz);
-                vbits = max(vbits, __float_as_uint(vv) & 0x7FFFFFFFu);
+                vmax = fmaxf(vmax, vv);
             }
         }
         cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 1));
         cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 2));
-        vbits = max(vbits, __shfl_xor_sync(0xFFFFFFFFu, vbits, 1));
-        vbits = max(vbits, __shfl_xor_sync(0xFFFFFFFFu, vbits, 2));
-        const float m_new = fmaxf(m, cmax);
-        const int E_new = max(E, (int)(vbits >> 23));
-        if (__any_sync(0xFFFFFFFFu, m_new != m || E_new != E)) {
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 2));
+        // Lazy reference max: weights 2^(z - m) may reach 2^kLazy before the
+        // accumulators are rescaled; kVScaleBias leaves room for that in f16.
+        const int Ec = (int)(__float_as_uint(vmax) >> 23);
+        if (__any_sync(0xFFFFFFFFu, cmax > m + (float)kLazy || Ec > E)) {
+            const float m_new = fmaxf(m, cmax);
+            const int E_new = max(E, Ec);
             const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
             const float ea = (E - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - E_new) << 23);
             const float fa = alpha * ea;
+            // rows whose max did not move keep alpha = 1, ea may still shrink them
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 acc[n][0] *= fa; acc[n][1] *= fa; acc[n][2] *= fa; acc[n][3] *= fa;
@@ -447,7 +462,7 @@ decode_tc_kernel(Params P) {
         float pw[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const float p = fast_exp2(z[u] - m);        // masked tokens: 2^-inf = 0
+            const float p = fast_exp2(z[u] - m);        // <= 2^kLazy; masked tokens: 2^-inf = 0
             lsum += p;
             pw[u] = p * vs[u] * wscale;
         }
@@ -462,10 +477,10 @@ decode_tc_kernel(Params P) {
             for (int jj = 0; jj < NJ; ++jj) {
                 const int wd = vword<D>(gq, jj);
                 const uint32_t x0 = r0[wd], x1 = r0[W + wd], x8 = r0[8 * W + wd], x9 = r0[9 * W + wd];
-                mma_16816(acc[4 * jj + 0], ap, codes_pair_to_f16x2<0>(x0, x1), codes_pair_to_f16x2<0>(x8, x9));
-                mma_16816(acc[4 * jj + 1], ap, codes_pair_to_f16x2<1>(x0, x1), codes_pair_to_f16x2<1>(x8, x9));
-                mma_16816(acc[4 * jj + 2], ap, codes_pair_to_f16x2<2>(x0, x1), codes_pair_to_f16x2<2>(x8, x9));
-                mma_16816(acc[4 * jj + 3], ap, codes_pair_to_f16x2<3>(x0, x1), codes_pair_to_f16x2<3>(x8, x9));
+                mma_16816(acc[4 * jj + 0], ap, codes_pair_to_f16x2<0>(x0, x1, fk), codes_pair_to_f16x2<0>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 1], ap, codes_pair_to_f16x2<1>(x0, x1, fk), codes_pair_to_f16x2<1>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 2], ap, codes_pair_to_f16x2<2>(x0, x1, fk), codes_pair_to_f16x2<2>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 3], ap, codes_pair_to_f16x2<3>(x0, x1, fk), codes_pair_to_f16x2<3>(x8, x9, fk));
             }
         }
         // ---- release the buffer, refill it with this slot's chunk i + RING
@@ -496,7 +511,7 @@ decode_tc_kernel(Params P) {
         arow[4 * vword<D>(2 * cq + 1, n / 4) + (n & 3)] = acc[n][1] + acc[n][3];
     }
     __syncthreads();
-    merge_and_store<D>(P, w, ml, accs, SLOTS, HT * 8);
+    merge_and_store<D>(P, w, ml, accs, SLOTS, HT * 8, accs + SLOTS * HT * 8 * D);
 }
 
 // ============================================================== CUDA cores
@@ -514,10 +529,11 @@ __host__ __device__ constexpr int cc_ring() { return D == 256 ? 2 : 3; }
 __device__ __forceinline__ void codes4_to_f32(uint32_t x, float &a, float &b, float &c, float &d) {
     // offset-binary byte under 0x4B000000 is 2^23 + code + 128 exactly
     const uint32_t u = x ^ 0x80808080u;
-    a = __uint_as_float(prmt(u, 0x4B000000u, 0x7650u)) - 8388736.0f;
-    b = __uint_as_float(prmt(u, 0x4B000000u, 0x7651u)) - 8388736.0f;
-    c = __uint_as_float(prmt(u, 0x4B000000u, 0x7652u)) - 8388736.0f;
-    d = __uint_as_float(prmt(u, 0x4B000000u, 0x7653u)) - 8388736.0f;
+    const uint32_t hi = 0x4B000000u;
+    a = __uint_as_float(prmt_i<0x7650u>(u, hi)) - 8388736.0f;
+    b = __uint_as_float(prmt_i<0x7651u>(u, hi)) - 8388736.0f;
+    c = __uint_as_float(prmt_i<0x7652u>(u, hi)) - 8388736.0f;
+    d = __uint_as_float(prmt_i<0x7653u>(u, hi)) - 8388736.0f;
 }
 
 template <int D, int NH>
@@ -686,7 +702,7 @@ decode_cc_kernel(Params P) {
         }
     }
     __syncthreads();
-    merge_and_store<D>(P, w, ml, accs, kCcSlots, NH);
+    merge_and_store<D>(P, w, ml, accs, kCcSlots, NH, accs + kCcSlots * NH * D);
 }
 
 // ================================================================= combine
@@ -758,6 +774,9 @@ Params make_params(const DecodeArgs &a) {
     P.out = a.out; P.q = a.q; P.kc = a.key_cache; P.vc = a.value_cache;
     P.bt = a.block_tables; P.cl = a.context_lens;
     P.S = a.num_seqs; P.H = a.num_heads; P.Hk = a.num_kv_heads; P.B = a.block_size;
+    P.log2B = 0;
+    while ((1 << P.log2B) < a.block_size) ++P.log2B;
+    P.log2ptok = P.log2B < 5 ? P.log2B : 5;
     P.Nb = a.max_blocks_per_seq; P.num_blocks = a.num_blocks;
     P.scale_log2 = a.scale * kLog2e;
     P.PT = a.partition_tokens; P.NP = a.num_partitions;
@@ -831,9 +850,14 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     const int64_t max_ctx = (int64_t)a.max_blocks_per_seq * a.block_size;
     int pt = requested_partition;
     if (pt <= 0) {
+        // Long partitions amortise each CTA's start-up (table, q, first copies)
+        // and epilogue; short ones balance ragged contexts.  Start at 4096
+        // tokens for long-context shapes, 2048 otherwise, and halve while the
+        // expected number of work units (contexts taken at half their maximum)
+        // would leave fewer than two waves of resident CTAs (3 per SM).
         const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-        const int64_t target = 4LL * num_sms;
-        pt = 2048;
+        const int64_t target = 2LL * 3 * num_sms;
+        pt = max_ctx >= 32768 ? 4096 : 2048;
         while (pt > 256 && units * ((max_ctx / 2 + pt - 1) / pt) < target) pt >>= 1;
     }
     if (pt % 128 != 0 || pt > 16384) return false;

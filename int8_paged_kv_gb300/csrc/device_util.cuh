@@ -131,36 +131,51 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// (a & b) ^ c in one LOP3
-__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+// prmt with a compile-time selector (an immediate operand)
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt_i(uint32_t a, uint32_t b) {
     uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
+    return d;
+}
+
+// (a & MASK) ^ c in one LOP3, MASK an immediate
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_xor_i(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
     return d;
 }
 
 // Two f16 lanes 0x64XX (= 1024 + XX) minus 1152 -> the signed codes XX - 128.
-__device__ __forceinline__ uint32_t sub_1152_x2(uint32_t v) {
+__device__ __forceinline__ uint32_t sub_1152_x2(uint32_t v, uint32_t bias) {
     uint32_t d;
-    const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(bias));
     return d;
 }
 
+// Constants of the int8 -> f16 conversions, kept in registers by the caller.
+struct F16Consts {
+    uint32_t exp64 = 0x64646464u;     // 0x64 in every byte: f16 exponent of 1024
+    uint32_t bias = 0x64806480u;      // f16x2 (1152, 1152); also 0x64 | 0x80 per half
+};
+
 // Codes in byte lanes 0,1 (lo) and 2,3 (hi) of a word -> two f16x2 values.
 // Exact: every int8 is an f16.
-__device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+__device__ __forceinline__ void codes4_to_f16x2(uint32_t w, uint32_t &lo, uint32_t &hi,
+                                                const F16Consts &k) {
     const uint32_t u = w ^ 0x80808080u;         // two's complement -> offset binary
-    lo = sub_1152_x2(prmt(u, 0x64646464u, 0x4140u));
-    hi = sub_1152_x2(prmt(u, 0x64646464u, 0x4342u));
+    lo = sub_1152_x2(prmt_i<0x4140u>(u, k.exp64), k.bias);
+    hi = sub_1152_x2(prmt_i<0x4342u>(u, k.exp64), k.bias);
 }
 
 // Byte lane e of a and of b -> f16x2 (code_a[e], code_b[e]).
 template <int E>
-__device__ __forceinline__ uint32_t codes_pair_to_f16x2(uint32_t a, uint32_t b) {
-    // d = [a.e, a.e, b.e, b.e]; bytes 1 and 3 are then replaced by 0x64
+__device__ __forceinline__ uint32_t codes_pair_to_f16x2(uint32_t a, uint32_t b, const F16Consts &k) {
+    // d = [a.e, a.e, b.e, b.e]; bytes 1 and 3 then become 0x64, bytes 0 and 2 flip sign
     constexpr uint32_t sel = (uint32_t)E | ((uint32_t)E << 4) | ((uint32_t)(E + 4) << 8) |
                              ((uint32_t)(E + 4) << 12);
-    return sub_1152_x2(and_xor(prmt(a, b, sel), 0x00FF00FFu, 0x64806480u));
+    return sub_1152_x2(and_xor_i<0x00FF00FFu>(prmt_i<sel>(a, b), k.bias), k.bias);
 }
 
 // D = A(16x16, f16, row) * B(16x8, f16, col) + D, f32 accumulate.
