@@ -269,6 +269,25 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------- multi-rank glue
+
+def dist_max(x: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (the bench's timing rule)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(world: int, bytes_per_step: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_step per step, the job
+    takes the slowest rank's time."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args) -> None:
@@ -375,14 +394,10 @@ def run_ours(args) -> None:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dec_ms = [s.elapsed_time(e) for s, e in zip(dstarts, dends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = dist_max(sum(step_ms), dev)
     status = pk.pa_q8_device_status(clear=True)
     ms_per_step = total_ms / args.steps
-    value = world * (bytes_w + bytes_d) / (ms_per_step * 1e-3) / 1e9
+    value = job_gbps(world, bytes_w + bytes_d, ms_per_step)
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_gbs = bytes_d / (dec_avg_ms * 1e-3) / 1e9
 
@@ -423,13 +438,9 @@ def run_ours(args) -> None:
             e2e_step()
             ee[i].record(stream)
         torch.cuda.synchronize()
-        e_total = sum(s.elapsed_time(e) for s, e in zip(es, ee))
-        if world > 1:
-            t = torch.tensor([e_total], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_total = float(t.item())
+        e_total = dist_max(sum(s.elapsed_time(e) for s, e in zip(es, ee)), dev)
         e_ms = e_total / args.steps
-        e2e = {"value": round(world * (bytes_w + bytes_d) / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        e2e = {"value": round(job_gbps(world, bytes_w + bytes_d, e_ms), 2), "unit": UNIT,
                "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
