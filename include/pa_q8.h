@@ -4,7 +4,8 @@
  * C ABI of libpa_q8.so.  Plain pointers and sizes only; every pointer named
  * "device" is a CUDA device address the caller allocated and owns.  The
  * library keeps no per-call state and allocates no device memory: scratch
- * (the split-context partials) lives in a workspace the caller passes in.
+ * (the split-context partials) lives in a workspace the caller passes in
+ * (or, for pa_q8_decode_noalloc, in a fixed buffer compiled into it).
  * All work is queued on the caller's CUDA stream (a cudaStream_t passed as
  * void*; NULL = the legacy default stream) and no function synchronises,
  * except pa_q8_device_status which reads a flag back.
@@ -132,6 +133,36 @@ int pa_q8_decode(float *out, const float *q,
                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
                  int block_size, int max_blocks_per_seq, int64_t num_blocks,
                  float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_q8_decode_noalloc -- pa_q8_decode for callers that cannot allocate.
+ * The pages have no counterpart to this entry point.
+ *
+ * Some callers cannot give the library device memory for scratch: a plugin
+ * hosted by another runtime that owns every device allocation and hands its
+ * plugins no allocator, or a serving loop whose latency budget rules out
+ * allocation calls.  This entry point takes no workspace and allocates
+ * nothing: the split-context partials go to a fixed buffer of
+ * PA_Q8_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU that
+ * loads the library holds it until the process exits).  Arguments, layouts,
+ * kernels and results are those of pa_q8_decode.
+ *   - Sizes whose partials exceed the buffer return PA_Q8_EWORKSPACE
+ *     (pa_q8_decode_workspace_size() gives the bytes a shape needs).
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make it before any
+ *     stream capture.
+ *   - All calls on a device share the buffer: calls whose work overlaps on
+ *     the GPU (different streams, concurrent launches) race on it.  The
+ *     buffer keeps the previous call's contents, none of which is read as
+ *     an initial value.
+ */
+#define PA_Q8_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int pa_q8_decode_noalloc(float *out, const float *q,
+                         const uint32_t *key_cache, const uint32_t *value_cache,
+                         const uint32_t *block_tables, const uint32_t *context_lens,
+                         int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                         int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                         float scale, void *stream);
 
 /* Workspace bytes pa_q8_decode needs for these sizes (0 when no sequence can
  * span more than one partition).  Returns 0 as well for invalid sizes; the

@@ -257,3 +257,66 @@ int pa_q8_selftest_wait_timeout(uint32_t timeout_us, void *stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- decode without allocation
+//
+// Some callers cannot give this library device memory for scratch: a plugin
+// hosted by another runtime that owns every device allocation and hands its
+// plugins no allocator, or a serving loop whose latency budget rules out
+// allocation calls (they can synchronise the device and take unbounded
+// time).  pa_q8_decode_noalloc serves them: it keeps the split-context
+// partials in a buffer compiled into this library, a fixed 64 MiB that every
+// GPU loading the library holds until the process exits.  Host code cannot
+// use the array's name as a device address (it is a host-side stand-in), so
+// the first call on each device looks the address up with
+// cudaGetSymbolAddress while that device is current and caches it; make that
+// first call before any stream capture.  All calls on a device share the
+// buffer, and calls whose kernels overlap on the GPU race on it.  The buffer
+// keeps the previous call's partials; nothing in it needs to start at zero,
+// since every partial the combine step reads is written earlier in the same
+// call.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = PA_Q8_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void *g_noalloc_ptr[kMaxDevices];
+
+int noalloc_scratch(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return PA_Q8_ECUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return PA_Q8_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_q8_decode_noalloc(float *out, const float *q, const uint32_t *key_cache,
+                                    const uint32_t *value_cache, const uint32_t *block_tables,
+                                    const uint32_t *context_lens, int num_seqs, int num_heads,
+                                    int num_kv_heads, int head_size, int block_size,
+                                    int max_blocks_per_seq, int64_t num_blocks, float scale,
+                                    void *stream) {
+    const int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size,
+                                      max_blocks_per_seq);
+    if (rc != PA_Q8_OK) return rc;
+    void *scratch = nullptr;
+    const int src = noalloc_scratch(&scratch);
+    if (src != PA_Q8_OK) return src;
+    // Same launch plan and kernels as pa_q8_decode; partials that would not
+    // fit in the fixed buffer make it return PA_Q8_EWORKSPACE.
+    return pa_q8_decode_ex(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                           num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
+                           num_blocks, scale, scratch, kNoAllocScratchBytes, stream, nullptr);
+}
