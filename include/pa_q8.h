@@ -121,9 +121,9 @@ int pa_q8_reshape_and_cache(const float *key, const float *value,
  *   context_lens    device u32 [num_seqs]; 0 gives a zero output row
  *   num_blocks      physical blocks; table entries >= num_blocks are skipped and flagged
  *   scale           softmax scale (e.g. 1/sqrt(head_size))
- *   workspace       device scratch of >= pa_q8_decode_workspace_size() bytes,
- *                   16-byte aligned (may be NULL when that size is 0); its contents
- *                   need no initialisation and are overwritten
+ *   workspace       device scratch of >= pa_q8_decode_workspace_size() bytes (never 0),
+ *                   16-byte aligned; its contents need no initialisation and are
+ *                   overwritten (sequence order, split-context partials)
  *   stream          cudaStream_t or NULL
  * Concurrent calls on different streams need different workspaces.
  */
@@ -164,8 +164,9 @@ int pa_q8_decode_noalloc(float *out, const float *q,
                          int block_size, int max_blocks_per_seq, int64_t num_blocks,
                          float scale, void *stream);
 
-/* Workspace bytes pa_q8_decode needs for these sizes (0 when no sequence can
- * span more than one partition).  Returns 0 as well for invalid sizes; the
+/* Workspace bytes pa_q8_decode needs for these sizes: the sequence order
+ * (longest context first) and, when a sequence can span more than one
+ * partition, the split-context partials.  Returns 0 for invalid sizes; the
  * decode call reports those. */
 size_t pa_q8_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                    int head_size, int block_size, int max_blocks_per_seq);

@@ -193,10 +193,7 @@ int pa_q8_decode_ex(float *out, const float *q, const uint32_t *key_cache, const
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return PA_Q8_EWORKSPACE;
         if (!aligned16(workspace)) return PA_Q8_EALIGN;
-        const size_t rows = (size_t)num_seqs * num_heads * a.num_partitions;
-        const size_t ml_bytes = ((rows * 2 * sizeof(float) + 255) / 256) * 256;
-        a.partial_ml = static_cast<float *>(workspace);
-        a.partial_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + ml_bytes);
+        pa_q8::plan_workspace_layout(a, workspace);
     }
     a.out = out;
     a.q = q;

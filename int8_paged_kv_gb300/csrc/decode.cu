@@ -75,6 +75,8 @@ struct Params {
     int r;                  // num_heads / num_kv_heads
     int heads_per_cta;
     int head_groups;
+    const uint32_t *order;  // [S]: sequence of grid z (longest context first)
+    uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
     float *pml;             // [S][H][NP][2]
     float *pacc;            // [S][H][NP][D]
     uint32_t *status;
@@ -91,7 +93,7 @@ struct Work {
 
 __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
     w.p = blockIdx.x;
-    w.s = blockIdx.z;
+    w.s = P.order ? (int)__ldg(P.order + blockIdx.z) : (int)blockIdx.z;
     w.g = blockIdx.y / P.head_groups;
     const int hg = blockIdx.y % P.head_groups;
     w.h0 = w.g * P.r + hg * P.heads_per_cta;
@@ -204,11 +206,72 @@ __device__ void drain(const Params &P, uint32_t bars, int ring, int consumed, in
 // Merge the per-warp online-softmax states of the CTA (m in log2 units, l,
 // acc scaled by 2^(E - 139)) and write the output rows, or this
 // partition's partial (M, L, A) for the combine kernel.
+// Log-sum-exp merge of all np partitions of this CTA's heads (run by the
+// last CTA of a (sequence, head group) to finish):
+// out = sum_p A_p 2^(M_p - M*) / sum_p L_p 2^(M_p - M*), M* = max M_p.
+// The partials of other CTAs are read through L2 (__ldcg).  scratch holds
+// (M*, 1/L) per head.
+template <int D>
+__device__ void combine_rows(const Params &P, const Work &w, int np, float *scratch) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    for (int hh = warp; hh < w.nh; hh += nwarps) {
+        const int64_t row0 = ((int64_t)w.s * P.H + w.h0 + hh) * P.NP;
+        float M = -INFINITY;
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float L = 0.0f;
+        for (int p = lane; p < np; p += 32)
+            L += __ldcg(P.pml + (row0 + p) * 2 + 1) * fast_exp2(__ldcg(P.pml + (row0 + p) * 2) - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        if (lane == 0) {
+            scratch[2 * hh] = M;
+            scratch[2 * hh + 1] = 1.0f / L;
+        }
+    }
+    __syncthreads();
+    // four output elements per thread at a time, so their loads overlap
+    constexpr int U = 4;
+    const int n_out = w.nh * D;
+    for (int i0 = threadIdx.x; i0 < n_out; i0 += U * blockDim.x) {
+        float a[U], M[U];
+        int64_t prow[U];
+        int dd[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = min(i0 + u * (int)blockDim.x, n_out - 1);
+            const int hh = i / D;
+            dd[u] = i % D;
+            prow[u] = ((int64_t)w.s * P.H + w.h0 + hh) * P.NP;
+            M[u] = scratch[2 * hh];
+            a[u] = 0.0f;
+        }
+#pragma unroll 2
+        for (int p = 0; p < np; ++p) {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                a[u] = fmaf(__ldcg(P.pacc + (prow[u] + p) * D + dd[u]),
+                            fast_exp2(__ldcg(P.pml + (prow[u] + p) * 2) - M[u]), a[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < n_out) {
+                const int hh = i / D;
+                P.out[((int64_t)w.s * P.H + w.h0 + hh) * D + dd[u]] = a[u] * scratch[2 * hh + 1];
+            }
+        }
+    }
+}
+
 template <int D>
 __device__ void merge_and_store(const Params &P, const Work &w, const float *ml, const float *accs,
                                 int n_slots, int heads_stride, float *fac) {
     // ml: [slot][head][3] = (m, l, E); accs: [slot][head][D]; fac: scratch
-    // [head][n_slots + 2] = per-slot factors, M, L.  Called by every thread.
+    // [head][n_slots + 2] = per-slot factors, M, L, then room for the
+    // combine's weights.  Called by every thread of the CTA.
     for (int hh = threadIdx.x; hh < w.nh; hh += blockDim.x) {
         float M = -INFINITY;
         for (int sl = 0; sl < n_slots; ++sl) M = fmaxf(M, ml[(sl * heads_stride + hh) * 3]);
@@ -245,6 +308,23 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
             }
         }
     }
+    if (w.single) return;
+    // Split context: the last CTA of this (sequence, head group) to arrive
+    // merges every partition (threadfence / counter handshake).
+    __threadfence();
+    __syncthreads();
+    const int np = (w.c + P.PT - 1) / P.PT;
+    int *last = reinterpret_cast<int *>(fac);
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(P.counters + (int64_t)w.s * gridDim.y + blockIdx.y, 1u);
+        *last = (prev == (uint32_t)(np - 1));
+    }
+    __syncthreads();
+    const bool is_last = *last != 0;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    combine_rows<D>(P, w, np, fac);
 }
 
 // ============================================================ tensor cores
@@ -705,51 +785,54 @@ decode_cc_kernel(Params P) {
     merge_and_store<D>(P, w, ml, accs, kCcSlots, NH, accs + kCcSlots * NH * D);
 }
 
-// ================================================================= combine
+// ==================================================================== prep
 //
-// out[s,h] = sum_p A_p 2^(M_p - M*) / sum_p L_p 2^(M_p - M*), M* = max M_p,
-// over the partitions of sequences that have more than one.
-template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(Params P) {
-    const int h = blockIdx.x, s = blockIdx.y;
-    const int64_t cap = (int64_t)P.Nb * P.B;
-    const int64_t craw = __ldg(P.cl + s);
-    const int c = (int)(craw < cap ? craw : cap);
-    const int np = (c + P.PT - 1) / P.PT;
-    if (np <= 1) return;
-    const int64_t row0 = ((int64_t)s * P.H + h) * P.NP;
-    __shared__ float s_w[1024];
-    __shared__ float s_inv;
-    float M = -INFINITY;
-    for (int p = threadIdx.x; p < np; p += blockDim.x) M = fmaxf(M, P.pml[(row0 + p) * 2]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    __shared__ float s_red[4];
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-    float Lp = 0.0f;
-    for (int p = threadIdx.x; p < np; p += blockDim.x) {
-        const float wgt = fast_exp2(P.pml[(row0 + p) * 2] - M);
-        if (p < 1024) s_w[p] = wgt;
-        Lp += P.pml[(row0 + p) * 2 + 1] * wgt;
+// One CTA before the attention grid: zero the split-context arrival
+// counters and order the sequences longest (clamped) context first, so the
+// block scheduler starts the longest-running CTAs first and the grid's tail
+// holds only short ones.  Bitonic sort of (length, index) keys in shared
+// memory for up to kPrepMaxSort sequences; beyond that the order is the
+// identity.
+constexpr int kPrepThreads = 1024;
+constexpr int kPrepMaxSort = 8192;
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *context_lens, int S, int64_t cap,
+                                                            uint32_t *order, uint32_t *counters,
+                                                            int64_t n_counters) {
+    extern __shared__ unsigned long long keys[];
+    for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
+    if (S > kPrepMaxSort) {
+        for (int i = threadIdx.x; i < S; i += blockDim.x) order[i] = (uint32_t)i;
+        return;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xFFFFFFFFu, Lp, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = Lp;
-    __syncthreads();
-    if (threadIdx.x == 0) s_inv = 1.0f / (s_red[0] + s_red[1] + s_red[2] + s_red[3]);
-    __syncthreads();
-    const float inv = s_inv;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float a = 0.0f;
-        for (int p = 0; p < np; ++p) {
-            const float wgt = p < 1024 ? s_w[p] : fast_exp2(P.pml[(row0 + p) * 2] - M);
-            a = fmaf(P.pacc[(row0 + p) * D + d], wgt, a);
+    int n = 1;
+    while (n < S) n <<= 1;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        if (i < S) {
+            const int64_t c = min((int64_t)__ldg(context_lens + i), cap);
+            keys[i] = ((unsigned long long)(cap - c) << 32) | (unsigned)i;   // ascending = longest first
+        } else {
+            keys[i] = ~0ull;
         }
-        P.out[((int64_t)s * P.H + h) * D + d] = a * inv;
     }
+    __syncthreads();
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = keys[i], b = keys[l];
+                    const bool up = (i & k) == 0;
+                    if ((a > b) == up) {
+                        keys[i] = b;
+                        keys[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < S; i += blockDim.x) order[i] = (uint32_t)(keys[i] & 0xFFFFFFFFull);
 }
 
 // ============================================================== selftest
@@ -782,7 +865,7 @@ Params make_params(const DecodeArgs &a) {
     P.PT = a.partition_tokens; P.NP = a.num_partitions;
     P.r = a.num_heads / a.num_kv_heads;
     P.heads_per_cta = a.heads_per_cta; P.head_groups = a.head_groups;
-    P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
+    P.order = a.order; P.counters = a.counters; P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
     return P;
 }
 
@@ -828,10 +911,19 @@ cudaError_t launch_cc(const Params &P, cudaStream_t st) {
 
 template <int D>
 cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
-    cudaError_t e = (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
-    if (e != cudaSuccess || P.NP <= 1) return e;
-    combine_kernel<D><<<dim3(P.H, P.S), 128, 0, st>>>(P);
-    return cudaGetLastError();
+    if (P.order) {
+        const int64_t n_counters = P.NP > 1 ? (int64_t)P.S * P.Hk * P.head_groups : 0;
+        int n = 1;
+        while (n < P.S && n < kPrepMaxSort) n <<= 1;
+        const size_t smem = (size_t)n * sizeof(unsigned long long);
+        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        prep_kernel<<<1, kPrepThreads, smem, st>>>(P.cl, P.S, (int64_t)P.Nb * P.B, const_cast<uint32_t *>(P.order),
+                                                   P.counters, n_counters);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
 }
 
 }  // namespace
@@ -852,12 +944,12 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     if (pt <= 0) {
         // Long partitions amortise each CTA's start-up (table, q, first copies)
         // and epilogue; short ones balance ragged contexts.  Start at 4096
-        // tokens for long-context shapes, 2048 otherwise, and halve while the
-        // expected number of work units (contexts taken at half their maximum)
-        // would leave fewer than two waves of resident CTAs (3 per SM).
+        // tokens and halve while the expected number of work units (contexts
+        // taken at half their maximum) would leave fewer than two waves of
+        // resident CTAs (3 per SM).
         const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
         const int64_t target = 2LL * 3 * num_sms;
-        pt = max_ctx >= 32768 ? 4096 : 2048;
+        pt = 4096;
         while (pt > 256 && units * ((max_ctx / 2 + pt - 1) / pt) < target) pt >>= 1;
     }
     if (pt % 128 != 0 || pt > 16384) return false;
@@ -868,11 +960,31 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     return true;
 }
 
+namespace {
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+}
+
 size_t plan_workspace_bytes(const DecodeArgs &a) {
-    if (a.num_partitions <= 1) return 0;
+    const size_t order = round256((size_t)a.num_seqs * sizeof(uint32_t));
+    if (a.num_partitions <= 1) return order;
+    const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
     const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;
-    const size_t ml = rows * 2 * sizeof(float);
-    return ((ml + 255) / 256) * 256 + rows * a.head_size * sizeof(float);
+    return order + round256(groups * sizeof(uint32_t)) + round256(rows * 2 * sizeof(float)) +
+           rows * a.head_size * sizeof(float);
+}
+
+void plan_workspace_layout(DecodeArgs &a, void *workspace) {
+    char *p = static_cast<char *>(workspace);
+    a.order = reinterpret_cast<uint32_t *>(p);
+    p += round256((size_t)a.num_seqs * sizeof(uint32_t));
+    if (a.num_partitions <= 1) return;
+    const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
+    const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;
+    a.counters = reinterpret_cast<uint32_t *>(p);
+    p += round256(groups * sizeof(uint32_t));
+    a.partial_ml = reinterpret_cast<float *>(p);
+    p += round256(rows * 2 * sizeof(float));
+    a.partial_acc = reinterpret_cast<float *>(p);
 }
 
 int64_t plan_num_ctas(const DecodeArgs &a) {

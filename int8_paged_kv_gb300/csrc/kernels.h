@@ -49,7 +49,11 @@ struct DecodeArgs {
     int num_partitions;    // partitions per sequence (grid x)
     int heads_per_cta;     // query heads one CTA serves (one kv head's group, or part of it)
     int head_groups;       // CTAs per (seq, kv head, partition) along the group
-    // split-context scratch: m,l [S][H][P][2] then acc [S][H][P][D] (f32)
+    // workspace: sequence order [S] (u32, longest context first); when
+    // partitions > 1 also arrival counters [S][Hk * head_groups] (u32),
+    // m,l [S][H][P][2] and acc [S][H][P][D] (f32)
+    uint32_t *order;
+    uint32_t *counters;
     float *partial_ml;
     float *partial_acc;
     uint32_t *status;
@@ -63,8 +67,11 @@ struct DecodePlanLimits {
 // Returns false if no kernel serves these sizes.
 bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int num_sms);
 
-// Workspace bytes for a plan (0 when num_partitions == 1).
+// Workspace bytes for a plan.
 size_t plan_workspace_bytes(const DecodeArgs &a);
+
+// Point the scratch fields of `a` into a workspace of plan_workspace_bytes(a).
+void plan_workspace_layout(DecodeArgs &a, void *workspace);
 
 // Grid size of the attention kernel for a plan.
 int64_t plan_num_ctas(const DecodeArgs &a);

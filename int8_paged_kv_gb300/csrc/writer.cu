@@ -7,9 +7,9 @@
 // bits of amax/127 (1.0 for amax = 0); slot 0xFFFFFFFF skips the row.
 //
 // GB300 mapping: one warp per (token, kv_head).  Each lane loads 16-byte
-// vectors of K and of V (both in flight at once), the amax is a warp
-// shuffle reduction, and lane j stores code word j (consecutive lanes,
-// consecutive words).  Every f32 operation is an explicit round-to-nearest
+// vectors of K and of V (both in flight at once, before the slot read),
+// the amax is a warp (or half-warp) shuffle reduction, and lane j stores
+// code word j (consecutive lanes, consecutive words).  Every f32 operation is an explicit round-to-nearest
 // intrinsic, so nothing is contracted or approximated and the words match
 // an IEEE reference bit for bit.
 #include <cstdint>
@@ -23,23 +23,23 @@ namespace {
 
 constexpr int kWriterWarps = 8;
 
-__device__ __forceinline__ uint32_t quantise_code(float x, float inv) {
-    float t = __fmul_rn(x, inv);
-    if (t != t) return 0u;                    // 0 * inf (127/amax overflowed): code 0
-    t = fminf(fmaxf(roundf(t), -127.0f), 127.0f);
-    return static_cast<uint32_t>(__float2int_rn(t)) & 0xFFu;
+// Code of x: round(x * inv) with halves away from zero, clamped to
+// [-127, 127].  For |t| < 2^23, adding 0.5 to |t| rounded toward zero and
+// truncating gives floor(|t| + 0.5) exactly (every integer below 2^24 is an
+// f32, so rounding down never skips one).  The f32 -> s32 conversion
+// saturates: NaN (0 * inf, when 127/amax overflowed) becomes 0 and +inf
+// becomes INT_MAX, clamped to 127 next.
+__device__ __forceinline__ int quantise_code(float x, float inv) {
+    const float t = __fmul_rn(x, inv);
+    const int a = min(__float2int_rz(__fadd_rz(fabsf(t), 0.5f)), 127);
+    return t < 0.0f ? -a : a;
 }
 
+// Four codes into one word, code l in byte l.
 __device__ __forceinline__ uint32_t pack_word(float4 x, float inv) {
-    return quantise_code(x.x, inv) | (quantise_code(x.y, inv) << 8) |
-           (quantise_code(x.z, inv) << 16) | (quantise_code(x.w, inv) << 24);
-}
-
-template <int G>
-__device__ __forceinline__ float group_max(float v) {
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
+    const uint32_t c0 = (uint32_t)quantise_code(x.x, inv), c1 = (uint32_t)quantise_code(x.y, inv);
+    const uint32_t c2 = (uint32_t)quantise_code(x.z, inv), c3 = (uint32_t)quantise_code(x.w, inv);
+    return prmt_i<0x5410u>(prmt_i<0x0040u>(c0, c1), prmt_i<0x0040u>(c2, c3));
 }
 
 template <bool kVec>
@@ -52,99 +52,102 @@ __device__ __forceinline__ float4 load4(const float *p) {
 }
 
 // D: head_size.  WORDS = D/4 code words per vector; G = lanes per vector
-// (16 for D = 64, else 32); NW = words per lane.  For D = 64 lanes 0-15
-// quantise K and lanes 16-31 quantise V; otherwise every lane does both.
+// (16 for D = 64, else 32); NW = words per lane.  Grid (token groups of
+// kWriterWarps, kv heads): warp w of CTA (x, h) owns token x * 8 + w, head
+// h.  For D = 64 lanes 0-15 quantise K and lanes 16-31 V, otherwise every
+// lane does both.  The K/V loads are issued before the slot is looked at,
+// so the two memory round trips overlap (a PAD row's data is read and
+// dropped).  log2_block < 0 means block_size is not a power of two.
 template <int D, bool kVec>
 __global__ void __launch_bounds__(kWriterWarps * 32)
 quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ value,
                      uint32_t *__restrict__ key_cache, uint32_t *__restrict__ value_cache,
-                     const uint32_t *__restrict__ slot_mapping, int64_t num_tokens,
+                     const uint32_t *__restrict__ slot_mapping, int num_tokens,
                      int64_t key_stride, int64_t value_stride, int num_kv_heads,
-                     int block_size, int64_t num_slots, uint32_t *status) {
+                     int block_size, int log2_block, int64_t num_slots, uint32_t *status) {
     constexpr int WORDS = D / 4;
     constexpr int G = WORDS < 32 ? WORDS : 32;
     constexpr int NW = WORDS / G;
-    constexpr bool kSplit = (G == 16);        // half-warp per vector
+    constexpr int VPL = (G == 16) ? 1 : 2;            // vectors per lane: K and V, or one of them
     const int lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
-    if (item >= num_tokens * num_kv_heads) return;
-    const int64_t tok = item / num_kv_heads;
-    const int h = (int)(item - tok * num_kv_heads);
+    const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
+    if (tok >= num_tokens) return;
+    const int h = blockIdx.y;
+    const int j = lane % G;
+    const float *ksrc = key + (int64_t)tok * key_stride + (int64_t)h * D;
+    const float *vsrc = value + (int64_t)tok * value_stride + (int64_t)h * D;
 
+    float4 x[VPL][NW];
+    if constexpr (VPL == 1) {
+        const float *src = lane >= 16 ? vsrc : ksrc;
+        x[0][0] = load4<kVec>(src + 4 * j);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            x[0][i] = load4<kVec>(ksrc + 4 * (j + 32 * i));
+            x[1][i] = load4<kVec>(vsrc + 4 * (j + 32 * i));
+        }
+    }
     const uint32_t slot = __ldg(slot_mapping + tok);
+
+    float m[VPL];
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+        m[u] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(x[u][i].x), fabsf(x[u][i].y)),
+                                     fmaxf(fabsf(x[u][i].z), fabsf(x[u][i].w))));
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], o));
+    }
     if (slot == kPadSlot) return;
     if ((int64_t)slot >= num_slots) {
         if (lane == 0) flag_error(status, kDevBadSlot);
         return;
     }
-    const int64_t blk = slot / (uint32_t)block_size;
-    const int64_t off = slot - blk * block_size;
-    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * (WORDS + 1);
-
-    if constexpr (kSplit) {
-        const bool is_v = lane >= 16;
-        const int j = lane & 15;
-        const float *src = is_v ? value + tok * value_stride + (int64_t)h * D
-                                : key + tok * key_stride + (int64_t)h * D;
-        const float4 x = load4<kVec>(src + 4 * j);
-        float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-        m = group_max<16>(m);
-        const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
-        uint32_t *cache = is_v ? value_cache : key_cache;
-        cache[dst + j] = pack_word(x, inv);
-        if (j == 0) cache[dst + WORDS] = __float_as_uint(m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f);
+    uint32_t blk, off;
+    if (log2_block >= 0) {
+        blk = slot >> log2_block;
+        off = slot & ((1u << log2_block) - 1u);
     } else {
-        const float *ksrc = key + tok * key_stride + (int64_t)h * D;
-        const float *vsrc = value + tok * value_stride + (int64_t)h * D;
-        float4 xk[NW], xv[NW];
+        blk = slot / (uint32_t)block_size;
+        off = slot - blk * (uint32_t)block_size;
+    }
+    const int64_t dst = (((int64_t)blk * num_kv_heads + h) * block_size + off) * (WORDS + 1);
 #pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            xk[i] = load4<kVec>(ksrc + 4 * (lane + 32 * i));
-            xv[i] = load4<kVec>(vsrc + 4 * (lane + 32 * i));
-        }
-        float mk = 0.0f, mv = 0.0f;
+    for (int u = 0; u < VPL; ++u) {
+        uint32_t *cache = (VPL == 1 ? lane >= 16 : u == 1) ? value_cache : key_cache;
+        const float inv = m[u] > 0.0f ? __fdiv_rn(127.0f, m[u]) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            mk = fmaxf(mk, fmaxf(fmaxf(fabsf(xk[i].x), fabsf(xk[i].y)),
-                                 fmaxf(fabsf(xk[i].z), fabsf(xk[i].w))));
-            mv = fmaxf(mv, fmaxf(fmaxf(fabsf(xv[i].x), fabsf(xv[i].y)),
-                                 fmaxf(fabsf(xv[i].z), fabsf(xv[i].w))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            mk = fmaxf(mk, __shfl_xor_sync(0xFFFFFFFFu, mk, o));
-            mv = fmaxf(mv, __shfl_xor_sync(0xFFFFFFFFu, mv, o));
-        }
-        const float ik = mk > 0.0f ? __fdiv_rn(127.0f, mk) : 0.0f;
-        const float iv = mv > 0.0f ? __fdiv_rn(127.0f, mv) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            key_cache[dst + lane + 32 * i] = pack_word(xk[i], ik);
-            value_cache[dst + lane + 32 * i] = pack_word(xv[i], iv);
-        }
-        if (lane == 0) {
-            key_cache[dst + WORDS] = __float_as_uint(mk > 0.0f ? __fdiv_rn(mk, 127.0f) : 1.0f);
-            value_cache[dst + WORDS] = __float_as_uint(mv > 0.0f ? __fdiv_rn(mv, 127.0f) : 1.0f);
-        }
+        for (int i = 0; i < NW; ++i) cache[dst + j + G * i] = pack_word(x[u][i], inv);
+        if (j == 0) cache[dst + WORDS] = __float_as_uint(m[u] > 0.0f ? __fdiv_rn(m[u], 127.0f) : 1.0f);
     }
 }
 
 template <int D>
 cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
-    const int64_t items = a.num_tokens * a.num_kv_heads;
-    const int64_t grid = (items + kWriterWarps - 1) / kWriterWarps;
-    if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    if (a.num_tokens > 0x7FFFFFFF - kWriterWarps || a.num_kv_heads > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((a.num_tokens + kWriterWarps - 1) / kWriterWarps), (unsigned)a.num_kv_heads);
     const bool vec = ((reinterpret_cast<uintptr_t>(a.key) | reinterpret_cast<uintptr_t>(a.value)) & 15u) == 0 &&
                      (a.key_stride % 4) == 0 && (a.value_stride % 4) == 0;
     const int64_t num_slots = a.num_blocks * a.block_size;
+    int log2_block = -1;
+    if ((a.block_size & (a.block_size - 1)) == 0) {
+        log2_block = 0;
+        while ((1 << log2_block) < a.block_size) ++log2_block;
+    }
     if (vec) {
-        quant_scatter_kernel<D, true><<<(unsigned)grid, kWriterWarps * 32, 0, stream>>>(
-            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, a.num_tokens,
-            a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, num_slots, a.status);
+        quant_scatter_kernel<D, true><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens,
+            a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, log2_block, num_slots, a.status);
     } else {
-        quant_scatter_kernel<D, false><<<(unsigned)grid, kWriterWarps * 32, 0, stream>>>(
-            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, a.num_tokens,
-            a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, num_slots, a.status);
+        quant_scatter_kernel<D, false><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens,
+            a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, log2_block, num_slots, a.status);
     }
     return cudaGetLastError();
 }
