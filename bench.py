@@ -203,7 +203,7 @@ class OracleBench:
         w, cfg, a = self.w, self.w.cfg, self.w.append
         t0 = time.perf_counter()
         rows, wbytes = 0, 0
-        while rows == 0 or (time.perf_counter() - t0 < seconds / 2 and rows < a.num_tokens):
+        while rows == 0 or time.perf_counter() - t0 < seconds / 2:
             i = self.next_row
             sl = slice(i, min(i + rows_per_chunk, a.num_tokens))
             self._write(a.key_view()[sl], a.value_view()[sl], a.slot_mapping[sl])
@@ -213,7 +213,7 @@ class OracleBench:
         tw = time.perf_counter() - t0
         t1 = time.perf_counter()
         nseq, dbytes = 0, 0
-        while nseq == 0 or (time.perf_counter() - t1 < seconds / 2 and nseq < cfg.num_seqs):
+        while nseq == 0 or time.perf_counter() - t1 < seconds / 2:
             s = self.next_seq
             rws = np.array([[s, h] for h in range(cfg.num_heads)], dtype=np.int32)
             self.oracle.decode(w.q, self.kc, self.vc, w.block_tables, w.context_lens,
@@ -234,9 +234,10 @@ def cpu_line_fields(samp: dict, step_bytes_w: int, step_bytes_d: int) -> dict:
     t_step = samp["writer_s_per_byte"] * step_bytes_w + samp["decode_s_per_byte"] * step_bytes_d
     return {"value": round((step_bytes_w + step_bytes_d) / t_step / 1e9, 4), "unit": UNIT,
             "cores": samp["cores"], "kind": "oracle",
-            "sample": (f"fp64 C oracle (OpenMP) on {samp['writer_rows']} of 16384 append rows and "
-                       f"{samp['decode_seqs']} of 256 sequences (all 64 heads), "
-                       f"{samp['seconds']:.1f} s; step time extrapolated by algorithmic bytes")}
+            "sample": (f"fp64 C oracle (OpenMP) on {samp['writer_rows']} append rows (of 16384 per step, "
+                       f"cycling) and {samp['decode_seqs']} sequence decodes (all 64 heads; 256 per "
+                       f"step, cycling), {samp['seconds']:.1f} s; step time extrapolated by "
+                       f"algorithmic bytes")}
 
 
 def run_reference(args) -> None:
@@ -351,7 +352,7 @@ def run_ours(args) -> None:
                                               partition_tokens=args.partition_tokens)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int32, device=dev)
 
     def flush_l2():
         torch.sum(flush, dim=0, out=flush_sink)
@@ -487,7 +488,8 @@ def run_ours(args) -> None:
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
                      "traffic": (round(traffic["bytes_per_launch"]) if traffic else None),
-                     "kernel": "pa_q8_decode call (attention kernel + combine kernel), CUDA events",
+                     "kernel": "pa_q8_decode call (prep kernel + attention kernel with its fused "
+                               "combine), CUDA events on the launching stream",
                      "peak_source": f"{peaks['source']} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)"},
         "clocks": clocks,
         "e2e": e2e,

@@ -790,9 +790,9 @@ decode_cc_kernel(Params P) {
 // One CTA before the attention grid: zero the split-context arrival
 // counters and order the sequences longest (clamped) context first, so the
 // block scheduler starts the longest-running CTAs first and the grid's tail
-// holds only short ones.  Bitonic sort of (length, index) keys in shared
-// memory for up to kPrepMaxSort sequences; beyond that the order is the
-// identity.
+// holds only short ones.  (length, index) keys in shared memory: ranked by
+// counting for up to blockDim sequences, bitonic-sorted up to kPrepMaxSort;
+// beyond that the order is the identity.
 constexpr int kPrepThreads = 1024;
 constexpr int kPrepMaxSort = 8192;
 
@@ -816,21 +816,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
         }
     }
     __syncthreads();
-    for (int k = 2; k <= n; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const unsigned long long a = keys[i], b = keys[l];
-                    const bool up = (i & k) == 0;
-                    if ((a > b) == up) {
-                        keys[i] = b;
-                        keys[l] = a;
-                    }
-                }
-            }
-            __syncthreads();
+    if (S <= (int)blockDim.x) {
+        // one thread per sequence: its rank is the number of smaller keys
+        // (all distinct), read from shared memory as broadcasts
+        if ((int)threadIdx.x < S) {
+            const unsigned long long mine = keys[threadIdx.x];
+            int rank = 0;
+            for (int j = 0; j < S; ++j) rank += keys[j] < mine;
+            order[rank] = threadIdx.x;
         }
+        return;
     }
     for (int i = threadIdx.x; i < S; i += blockDim.x) order[i] = (uint32_t)(keys[i] & 0xFFFFFFFFull);
 }

@@ -210,3 +210,18 @@ def test_plan_is_what_the_benchmark_times():
                                 cfg.block_size, cfg.max_blocks_per_seq)
     assert plan["kernel"] in (TC, CC) and plan["partition_tokens"] % 128 == 0
     assert plan["num_partitions"] * plan["partition_tokens"] >= cfg.max_context
+
+
+@pytest.mark.parametrize("S", [1500, 9000])
+def test_many_sequences_take_every_ordering_path(S):
+    """More sequences than one prep CTA ranks (sorting network) and more than
+    it sorts (identity order): every row still matches the oracle."""
+    from tests.gpu_helpers import assert_close, gpu_decode, oracle_decode
+    rng = np.random.default_rng(S)
+    lens = rng.integers(0, 41, size=S).tolist()
+    w, ok_, ov_, kc, vc = _random_case(S, 4, 2, 64, 16, lens, seed=S)
+    want = oracle_decode(w, ok_, ov_)
+    for kernel in (TC, CC):
+        for pt in (0, 128):
+            assert_close(gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt), want,
+                         f"S {S} kernel {kernel} pt {pt}")
