@@ -502,12 +502,82 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------- per-workload table
+
+def run_configs(args) -> None:
+    """Decode throughput of every workload (both kernel families), one JSON
+    line per (workload, family) -- a report next to the bench line, not a
+    bench line itself."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    from int8_paged_kv_gb300 import build as pkbuild
+
+    pkbuild.build()
+    dev = torch.device("cuda", 0)
+    peaks = measured_peaks()
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+    for name in wl.CONFIGS:
+        w = wl.build(name, with_append=False)
+        cfg = w.cfg
+        S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+
+        def u32(x):
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int32)).to(dev)
+
+        W = D // 4 + 1
+        kc = torch.empty((w.num_blocks, Hk, B, W), dtype=torch.int32, device=dev)
+        vc = torch.empty_like(kc)
+        T = w.key.shape[0]
+        for i in range(0, T, 1 << 18):
+            pk.pa_q8_reshape_and_cache(torch.from_numpy(w.key[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                       torch.from_numpy(w.value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                       kc, vc, u32(w.slot_mapping[i:i + (1 << 18)]), num_kv_heads=Hk,
+                                       head_size=D, block_size=B)
+        w.key = w.value = None
+        q = torch.from_numpy(w.q).to(dev)
+        bt, cl, out = u32(w.block_tables), u32(w.context_lens), torch.empty_like(q)
+        nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens)
+        for kernel in (pk.PA_Q8_KERNEL_TENSOR_CORE, pk.PA_Q8_KERNEL_CUDA_CORE):
+            plan = pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq, kernel=kernel)
+            ws = torch.empty(pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq,
+                                                            kernel=kernel), dtype=torch.uint8, device=dev)
+
+            def run():
+                pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale,
+                                workspace=ws, kernel=kernel)
+            for _ in range(max(3, args.warmup)):
+                torch.sum(flush, dim=0, out=sink)
+                run()
+            ts = []
+            for _ in range(args.steps):
+                torch.sum(flush, dim=0, out=sink)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                run()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            ms = float(np.median(ts))
+            print(json.dumps({"kind": "decode per workload", "workload": name, "description": cfg.description,
+                              "kernel": {1: "cuda-core", 2: "tensor-core"}[kernel],
+                              "partition_tokens": plan["partition_tokens"], "ms": round(ms, 4),
+                              "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
+                              "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                              "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
+        del kc, vc, q, out
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--configs", action="store_true",
+                    help="print decode throughput of every workload instead of the bench line")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--seqs", type=int, default=0,
@@ -521,7 +591,9 @@ def main():
     args.warmup = max(3, args.warmup)          # timing rule: at least 3 warm-up steps
     if args.ref_step_seconds <= 0:
         args.ref_step_seconds = min(4.0, max(0.05, 150.0 / (args.steps + args.warmup)))
-    if args.impl == "reference":
+    if args.configs:
+        run_configs(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

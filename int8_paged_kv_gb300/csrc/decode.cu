@@ -75,7 +75,8 @@ struct Params {
     int r;                  // num_heads / num_kv_heads
     int heads_per_cta;
     int head_groups;
-    const uint32_t *order;  // [S]: sequence of grid z (longest context first)
+    const unsigned long long *order;  // [S]: (clamped length << 32 | sequence) of grid z,
+                                      // longest context first
     uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
     float *pml;             // [S][H][NP][2]
     float *pacc;            // [S][H][NP][D]
@@ -93,14 +94,22 @@ struct Work {
 
 __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
     w.p = blockIdx.x;
-    w.s = P.order ? (int)__ldg(P.order + blockIdx.z) : (int)blockIdx.z;
     w.g = blockIdx.y / P.head_groups;
     const int hg = blockIdx.y % P.head_groups;
     w.h0 = w.g * P.r + hg * P.heads_per_cta;
     w.nh = min(P.heads_per_cta, P.r - hg * P.heads_per_cta);
     const int64_t cap = (int64_t)P.Nb * P.B;
-    const int64_t craw = __ldg(P.cl + w.s);
-    w.c = (int)(craw < cap ? craw : cap);
+    if (P.order) {
+        // written by the prep kernel that precedes this grid on the stream
+        grid_dependency_wait();
+        const unsigned long long e = __ldcg(P.order + blockIdx.z);
+        w.s = (int)(e & 0xFFFFFFFFull);
+        w.c = (int)(e >> 32);
+    } else {
+        w.s = (int)blockIdx.z;
+        const int64_t craw = __ldg(P.cl + w.s);
+        w.c = (int)(craw < cap ? craw : cap);
+    }
     w.t_begin = w.p * P.PT;
     w.len = min(w.c - w.t_begin, P.PT);
     w.single = w.c <= P.PT;
@@ -797,12 +806,17 @@ constexpr int kPrepThreads = 1024;
 constexpr int kPrepMaxSort = 8192;
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *context_lens, int S, int64_t cap,
-                                                            uint32_t *order, uint32_t *counters,
+                                                            unsigned long long *order, uint32_t *counters,
                                                             int64_t n_counters) {
     extern __shared__ unsigned long long keys[];
+    // the attention grid may launch now; it waits for this grid's writes
+    grid_dependents_launch();
     for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
     if (S > kPrepMaxSort) {
-        for (int i = threadIdx.x; i < S; i += blockDim.x) order[i] = (uint32_t)i;
+        for (int i = threadIdx.x; i < S; i += blockDim.x) {
+            const int64_t c = min((int64_t)__ldg(context_lens + i), cap);
+            order[i] = ((unsigned long long)c << 32) | (unsigned)i;
+        }
         return;
     }
     int n = 1;
@@ -823,11 +837,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
             const unsigned long long mine = keys[threadIdx.x];
             int rank = 0;
             for (int j = 0; j < S; ++j) rank += keys[j] < mine;
-            order[rank] = threadIdx.x;
+            order[rank] = ((unsigned long long)(cap - (int64_t)(mine >> 32)) << 32) | threadIdx.x;
         }
         return;
     }
-    for (int i = threadIdx.x; i < S; i += blockDim.x) order[i] = (uint32_t)(keys[i] & 0xFFFFFFFFull);
+    for (int i = threadIdx.x; i < S; i += blockDim.x)
+        order[i] = ((unsigned long long)(cap - (int64_t)(keys[i] >> 32)) << 32) | (keys[i] & 0xFFFFFFFFull);
 }
 
 // ============================================================== selftest
@@ -864,12 +879,25 @@ Params make_params(const DecodeArgs &a) {
     return P;
 }
 
+// The attention grid is launched as a programmatic dependent of the prep
+// kernel before it on the stream: its launch overlaps the prep kernel, and
+// each CTA waits (griddepcontrol.wait) before it reads the prep's output.
 template <typename K>
 cudaError_t launch_attn(K kernel, const Params &P, uint32_t smem_bytes, int threads, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(P.NP, P.Hk * P.head_groups, P.S);
-    kernel<<<grid, threads, smem_bytes, st>>>(P);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.NP, P.Hk * P.head_groups, P.S);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = P.order ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -913,7 +941,8 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
         const size_t smem = (size_t)n * sizeof(unsigned long long);
         cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prep_kernel<<<1, kPrepThreads, smem, st>>>(P.cl, P.S, (int64_t)P.Nb * P.B, const_cast<uint32_t *>(P.order),
+        prep_kernel<<<1, kPrepThreads, smem, st>>>(P.cl, P.S, (int64_t)P.Nb * P.B,
+                                                   const_cast<unsigned long long *>(P.order),
                                                    P.counters, n_counters);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -960,7 +989,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 }
 
 size_t plan_workspace_bytes(const DecodeArgs &a) {
-    const size_t order = round256((size_t)a.num_seqs * sizeof(uint32_t));
+    const size_t order = round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return order;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
     const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;
@@ -970,8 +999,8 @@ size_t plan_workspace_bytes(const DecodeArgs &a) {
 
 void plan_workspace_layout(DecodeArgs &a, void *workspace) {
     char *p = static_cast<char *>(workspace);
-    a.order = reinterpret_cast<uint32_t *>(p);
-    p += round256((size_t)a.num_seqs * sizeof(uint32_t));
+    a.order = reinterpret_cast<unsigned long long *>(p);
+    p += round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
     const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;

@@ -99,6 +99,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+// ----------------------------------------------- programmatic dependent launch
+
+// Block until the grid this one depends on (launched before it on the
+// stream) has finished and its memory is visible.  No-op without a
+// programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the dependent grid to be launched before this one finishes.
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- misc
 
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {

@@ -49,10 +49,11 @@ struct DecodeArgs {
     int num_partitions;    // partitions per sequence (grid x)
     int heads_per_cta;     // query heads one CTA serves (one kv head's group, or part of it)
     int head_groups;       // CTAs per (seq, kv head, partition) along the group
-    // workspace: sequence order [S] (u32, longest context first); when
+    // workspace: sequence order [S] (u64: clamped length << 32 | sequence,
+    // longest context first); when
     // partitions > 1 also arrival counters [S][Hk * head_groups] (u32),
     // m,l [S][H][P][2] and acc [S][H][P][D] (f32)
-    uint32_t *order;
+    unsigned long long *order;
     uint32_t *counters;
     float *partial_ml;
     float *partial_acc;
