@@ -371,7 +371,7 @@ def run_ours(args) -> None:
 
     bytes_w = wl.algorithmic_writer_bytes(Hk, D, a.slot_mapping)
     bytes_d = wl.algorithmic_decode_bytes(cfg, w.context_lens)
-    launches_per_step = 1 + 1 + (1 if plan["num_partitions"] > 1 else 0)
+    launches_per_step = 3          # writer, prep (sequence order), attention (combine fused in)
 
     ev_d0, ev_d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_w0 = torch.cuda.Event(enable_timing=True)

@@ -27,6 +27,7 @@
 //     (lane = 4 head dims).
 // Every wait is bounded; a wait that gives up flags the status word, and a
 // warp leaves only after the copies it issued have landed.
+#include <algorithm>
 #include <cfloat>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -966,15 +967,27 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     const int64_t max_ctx = (int64_t)a.max_blocks_per_seq * a.block_size;
     int pt = requested_partition;
     if (pt <= 0) {
-        // Long partitions amortise each CTA's start-up (table, q, first copies)
-        // and epilogue; short ones balance ragged contexts.  Start at 4096
-        // tokens and halve while the expected number of work units (contexts
-        // taken at half their maximum) would leave fewer than two waves of
-        // resident CTAs (3 per SM).
+        // CTAs resident per SM for this kernel configuration
+        const int hd = a.head_size;
+        const bool big_tile = hd == 256 || a.heads_per_cta > 8;
+        const int per_sm = a.kernel == kCudaCore ? (hd == 256 ? 1 : 2) : (big_tile ? 1 : 3);
+        const int64_t slots = (int64_t)per_sm * num_sms;
         const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-        const int64_t target = 2LL * 3 * num_sms;
-        pt = 4096;
-        while (pt > 256 && units * ((max_ctx / 2 + pt - 1) / pt) < target) pt >>= 1;
+        if (units >= slots) {
+            // Enough (sequence, kv head) work items: one partition per context
+            // (up to 8192 tokens).  The grid runs the longest contexts first,
+            // so the tail holds short ones.
+            pt = (int)std::min<int64_t>((max_ctx + 127) / 128 * 128, 8192);
+        } else {
+            // Few, long contexts: split so that the expected work (contexts
+            // taken at half their maximum) fills about two waves of resident
+            // CTAs (one wave for one-CTA-per-SM kernels), rounded to the
+            // nearest power of two in 256 .. 8192 tokens.
+            const int64_t waves = per_sm > 1 ? 2 : 1;
+            const double want = (double)units * (double)max_ctx / 2.0 / (double)(waves * slots);
+            pt = 256;
+            while (pt < 8192 && (double)pt * 1.4142135 < want) pt <<= 1;
+        }
     }
     if (pt % 128 != 0 || pt > 16384) return false;
     a.partition_tokens = pt;

@@ -4,10 +4,11 @@ Some callers cannot give the library device memory for scratch -- a plugin
 inside another runtime that owns every device allocation, or a serving loop
 that may not call an allocator -- so pa_q8_decode_noalloc keeps the
 split-context partials in a fixed buffer compiled into the library.  This
-test checks, on two calls in a row with different inputs, that its output
-matches the workspace-taking entry point within the decode tolerance
-(|a - b| <= 1e-5 + 1e-4 |b|), that a shape whose partials would not fit the
-buffer is refused, and that nothing was flagged on the device.  The file is
+test checks, on two calls in a row with different inputs (the second one
+split into partitions), that its output matches the workspace-taking entry
+point within the decode tolerance (|a - b| <= 1e-5 + 1e-4 |b|), that a shape
+whose scratch would not fit the buffer is refused, and that nothing was
+flagged on the device.  The file is
 named to be collected last.
 """
 import ctypes
@@ -41,43 +42,82 @@ def _noalloc(L, out, q, kc, vc, bt, cl, w, stream):
                                   ctypes.c_float(w.scale), ctypes.c_void_p(stream))
 
 
+def _cache_from_rows(pk, key, value, slots, nblocks, Hk, D, B, dev):
+    import torch
+    W = D // 4 + 1
+    kc = torch.full((nblocks, Hk, B, W), -1, dtype=torch.int32, device=dev)
+    vc = torch.full_like(kc, -1)
+    T = key.shape[0]
+    pk.pa_q8_reshape_and_cache(key.reshape(T, -1), value.reshape(T, -1), kc, vc, slots,
+                               num_kv_heads=Hk, head_size=D, block_size=B)
+    return kc, vc
+
+
 def test_noalloc_matches_decode_on_two_calls(lib):
+    """Call 1: the 64-sequence workload (one partition per context: the
+    buffer holds the sequence order).  Call 2: three ~20k-token contexts
+    (split into partitions: the buffer also holds their partials, over
+    whatever call 1 left there).  Each output matches pa_q8_decode's on the
+    same inputs."""
     import torch
     import int8_paged_kv_gb300 as pk
     from int8_paged_kv_gb300 import workloads as wl
 
-    w = wl.build("llama8b")
-    cfg = w.cfg
-    S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
     dev = torch.device("cuda")
+    stream = torch.cuda.current_stream().cuda_stream
 
     def u32(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(dev)
 
-    W = D // 4 + 1
-    kc = torch.full((w.num_blocks, Hk, B, W), -1, dtype=torch.int32, device=dev)
-    vc = torch.full_like(kc, -1)
-    T = w.key.shape[0]
-    pk.pa_q8_reshape_and_cache(torch.from_numpy(w.key.reshape(T, -1)).to(dev),
-                               torch.from_numpy(w.value.reshape(T, -1)).to(dev), kc, vc,
-                               u32(w.slot_mapping), num_kv_heads=Hk, head_size=D, block_size=B)
-    need = pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq)
-    assert 0 < need <= 64 << 20            # this shape uses the split-context partials
-    stream = torch.cuda.current_stream().cuda_stream
-    bt = u32(w.block_tables)
-    rng = np.random.default_rng(99)
+    cases = []
+    w = wl.build("llama8b")
+    cfg = w.cfg
+    kc, vc = _cache_from_rows(pk, torch.from_numpy(w.key).to(dev), torch.from_numpy(w.value).to(dev),
+                              u32(w.slot_mapping), w.num_blocks, cfg.num_kv_heads, cfg.head_size,
+                              cfg.block_size, dev)
+    w.key = w.value = None
+    cases.append((w, kc, vc))
 
-    for call in range(2):
-        # second call: other queries and shorter contexts, so stale partials
-        # left in the shared buffer by the first call would show
-        qn = w.q if call == 0 else rng.standard_normal(w.q.shape).astype(np.float32)
-        cln = w.context_lens if call == 0 else (w.context_lens // 3 + 1).astype(np.uint32)
-        q = torch.from_numpy(qn).to(dev)
-        cl = u32(cln)
+    rng = np.random.default_rng(7)
+    S, H, Hk, D, B = 3, 8, 2, 128, 16
+    lens = np.array([20000, 17333, 19001], dtype=np.uint32)
+    Nb = -(-int(lens.max()) // B)
+    nblk = [-(-int(c) // B) for c in lens]
+    perm = rng.permutation(sum(nblk)).astype(np.uint32)
+    bt = np.full((S, Nb), 0xFFFFFFFF, dtype=np.uint32)
+    pos, slots = 0, []
+    for s_, c in enumerate(lens):
+        bt[s_, :nblk[s_]] = perm[pos:pos + nblk[s_]]
+        pos += nblk[s_]
+        t = np.arange(int(c))
+        slots.append(bt[s_, t // B].astype(np.int64) * B + t % B)
+    slots = np.concatenate(slots).astype(np.uint32)
+    T = slots.size
+    gen = torch.Generator(device=dev).manual_seed(7)
+    key = torch.randn(T, Hk, D, device=dev, generator=gen)
+    value = torch.randn(T, Hk, D, device=dev, generator=gen)
+    kc2, vc2 = _cache_from_rows(pk, key, value, u32(slots), sum(nblk), Hk, D, B, dev)
+    cfg2 = wl.Config("three-long", 98, S, H, Hk, D, B, Nb * B)
+    w2 = wl.Workload(cfg=cfg2, context_lens=lens, block_tables=bt, num_blocks=sum(nblk),
+                     q=rng.standard_normal((S, H, D)).astype(np.float32),
+                     scale=float(np.float32(D ** -0.5)), key=None, value=None, slot_mapping=slots,
+                     row_seq=None)
+    cases.append((w2, kc2, vc2))
+
+    needs = [pk.pa_q8_decode_workspace_size(c.cfg.num_seqs, c.cfg.num_heads, c.cfg.num_kv_heads,
+                                            c.cfg.head_size, c.cfg.block_size, c.cfg.max_blocks_per_seq)
+             for c, _, _ in cases]
+    assert 0 < needs[0] < needs[1] <= 64 << 20      # call 2 also stores split-context partials
+
+    for call, (wk, kck, vck) in enumerate(cases):
+        c = wk.cfg
+        q = torch.from_numpy(wk.q).to(dev)
+        bt_d, cl_d = u32(wk.block_tables), u32(wk.context_lens)
         ref = torch.full_like(q, float("nan"))
-        pk.pa_q8_decode(ref, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale)
+        pk.pa_q8_decode(ref, q, kck, vck, bt_d, cl_d, num_kv_heads=c.num_kv_heads,
+                        block_size=c.block_size, scale=wk.scale)
         got = torch.full_like(q, float("nan"))
-        rc = _noalloc(lib, got, q, kc, vc, bt, cl, w, stream)
+        rc = _noalloc(lib, got, q, kck, vck, bt_d, cl_d, wk, stream)
         assert rc == 0, pk.pa_q8_status_string(rc)
         torch.cuda.synchronize()
         a = got.cpu().numpy().astype(np.float64)
@@ -90,9 +130,10 @@ def test_noalloc_matches_decode_on_two_calls(lib):
 def test_noalloc_refuses_shapes_beyond_its_buffer(lib):
     import torch
     import int8_paged_kv_gb300 as pk
-    # 4096 sequences x 64 heads with contexts up to 8192 tokens need more than
-    # the fixed buffer for their partials: refused on the host, nothing launched
-    S, H, Hk, D, B, Nb = 4096, 64, 8, 128, 16, 512
+    # 64 sequences x 64 heads (one kv head) with contexts up to 2^20 tokens
+    # are split into many partitions whose partials need more than the fixed
+    # buffer: refused on the host, nothing launched
+    S, H, Hk, D, B, Nb = 64, 64, 1, 128, 16, 65536
     assert pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, Nb) > 64 << 20
     dummy = torch.empty(64, dtype=torch.float32, device="cuda")
     p = _ptr(dummy)
