@@ -6,12 +6,12 @@
 // halves away from zero; 4 codes per u32 (code l in byte l); then the f32
 // bits of amax/127 (1.0 for amax = 0); slot 0xFFFFFFFF skips the row.
 //
-// GB300 mapping: one warp per (token, kv_head).  Each lane loads 16-byte
-// vectors of K and of V (both in flight at once, before the slot read),
-// the amax is a warp (or half-warp) shuffle reduction, and lane j stores
-// code word j (consecutive lanes, consecutive words).  Every f32 operation is an explicit round-to-nearest
-// intrinsic, so nothing is contracted or approximated and the words match
-// an IEEE reference bit for bit.
+// GB300 mapping: one warp per (token, pair of kv heads), eight lanes per
+// K or V vector, so the per-vector reductions and divisions of four vectors
+// share instructions; loads are 16-byte vectors issued before the slot read.
+// Every f32 operation is an explicit round-to-nearest intrinsic, so nothing
+// is contracted or approximated and the words match an IEEE reference bit
+// for bit.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -51,13 +51,17 @@ __device__ __forceinline__ float4 load4(const float *p) {
     }
 }
 
-// D: head_size.  WORDS = D/4 code words per vector; G = lanes per vector
-// (16 for D = 64, else 32); NW = words per lane.  Grid (token groups of
-// kWriterWarps, kv heads): warp w of CTA (x, h) owns token x * 8 + w, head
-// h.  For D = 64 lanes 0-15 quantise K and lanes 16-31 V, otherwise every
-// lane does both.  The K/V loads are issued before the slot is looked at,
-// so the two memory round trips overlap (a PAD row's data is read and
+// D: head_size.  A warp owns one token and two kv heads (h0, h0 + 1): four
+// vectors K(h0), V(h0), K(h0+1), V(h0+1), eight lanes each (lane group
+// v = lane / 8).  Lane j of a group holds words j, j + 8, ... (NW = D/32 of
+// them), so every load and store instruction covers contiguous 128-byte /
+// 32-byte runs per vector.  Because the four groups run side by side, one
+// instruction sequence computes all four amax reductions (3 shuffle levels)
+// and all four divisions.  The K/V loads are issued before the slot is looked
+// at, so the memory round trips overlap (a PAD row's data is read and
 // dropped).  log2_block < 0 means block_size is not a power of two.
+constexpr int kLanesPerVector = 8;
+
 template <int D, bool kVec>
 __global__ void __launch_bounds__(kWriterWarps * 32)
 quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ value,
@@ -66,45 +70,32 @@ quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ va
                      int64_t key_stride, int64_t value_stride, int num_kv_heads,
                      int block_size, int log2_block, int64_t num_slots, uint32_t *status) {
     constexpr int WORDS = D / 4;
-    constexpr int G = WORDS < 32 ? WORDS : 32;
+    constexpr int G = kLanesPerVector;
     constexpr int NW = WORDS / G;
-    constexpr int VPL = (G == 16) ? 1 : 2;            // vectors per lane: K and V, or one of them
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
     if (tok >= num_tokens) return;
-    const int h = blockIdx.y;
-    const int j = lane % G;
-    const float *ksrc = key + (int64_t)tok * key_stride + (int64_t)h * D;
-    const float *vsrc = value + (int64_t)tok * value_stride + (int64_t)h * D;
-
-    float4 x[VPL][NW];
-    if constexpr (VPL == 1) {
-        const float *src = lane >= 16 ? vsrc : ksrc;
-        x[0][0] = load4<kVec>(src + 4 * j);
-    } else {
+    const int v = lane / G, j = lane % G;
+    const bool is_v = v & 1;
+    const int h = 2 * blockIdx.y + (v >> 1);
+    const bool live = h < num_kv_heads;                 // an odd head count leaves a pair half empty
+    const float *src = is_v ? value + (int64_t)tok * value_stride + (int64_t)h * D
+                            : key + (int64_t)tok * key_stride + (int64_t)h * D;
+    float4 x[NW];
 #pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            x[0][i] = load4<kVec>(ksrc + 4 * (j + 32 * i));
-            x[1][i] = load4<kVec>(vsrc + 4 * (j + 32 * i));
-        }
-    }
+    for (int i = 0; i < NW; ++i)
+        x[i] = live ? load4<kVec>(src + 4 * (j + G * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
     const uint32_t slot = __ldg(slot_mapping + tok);
 
-    float m[VPL];
+    float m = 0.0f;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        m[u] = 0.0f;
+    for (int i = 0; i < NW; ++i)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
 #pragma unroll
-        for (int i = 0; i < NW; ++i)
-            m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(x[u][i].x), fabsf(x[u][i].y)),
-                                     fmaxf(fabsf(x[u][i].z), fabsf(x[u][i].w))));
-    }
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xFFFFFFFFu, m[u], o));
-    }
-    if (slot == kPadSlot) return;
+    for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
+    const float scale = m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f;
+    if (slot == kPadSlot || !live) return;
     if ((int64_t)slot >= num_slots) {
         if (lane == 0) flag_error(status, kDevBadSlot);
         return;
@@ -118,20 +109,17 @@ quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ va
         off = slot - blk * (uint32_t)block_size;
     }
     const int64_t dst = (((int64_t)blk * num_kv_heads + h) * block_size + off) * (WORDS + 1);
+    uint32_t *cache = is_v ? value_cache : key_cache;
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        uint32_t *cache = (VPL == 1 ? lane >= 16 : u == 1) ? value_cache : key_cache;
-        const float inv = m[u] > 0.0f ? __fdiv_rn(127.0f, m[u]) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) cache[dst + j + G * i] = pack_word(x[u][i], inv);
-        if (j == 0) cache[dst + WORDS] = __float_as_uint(m[u] > 0.0f ? __fdiv_rn(m[u], 127.0f) : 1.0f);
-    }
+    for (int i = 0; i < NW; ++i) cache[dst + j + G * i] = pack_word(x[i], inv);
+    if (j == 0) cache[dst + WORDS] = __float_as_uint(scale);
 }
 
 template <int D>
 cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
-    if (a.num_tokens > 0x7FFFFFFF - kWriterWarps || a.num_kv_heads > 65535) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((a.num_tokens + kWriterWarps - 1) / kWriterWarps), (unsigned)a.num_kv_heads);
+    const int64_t head_pairs = (a.num_kv_heads + 1) / 2;
+    if (a.num_tokens > 0x7FFFFFFF - kWriterWarps || head_pairs > 65535) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((a.num_tokens + kWriterWarps - 1) / kWriterWarps), (unsigned)head_pairs);
     const bool vec = ((reinterpret_cast<uintptr_t>(a.key) | reinterpret_cast<uintptr_t>(a.value)) & 15u) == 0 &&
                      (a.key_stride % 4) == 0 && (a.value_stride % 4) == 0;
     const int64_t num_slots = a.num_blocks * a.block_size;
