@@ -55,6 +55,7 @@ def _load():
                                               i32, i32, i64, i64, P, P, P]
         lib.oracle_combine.argtypes = [P, P, P, i32, i32, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i64]
+        lib.oracle_decode_rows.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64]
         _lib = lib
         return lib
 
@@ -136,6 +137,24 @@ def decode(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
     _load().oracle_decode(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
                           _ptr(block_tables), _ptr(context_lens), S, H, num_kv_heads, D,
                           block_size, Nb, float(scale), rp, nr)
+    return out
+
+
+def decode_rows(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+                block_tables: np.ndarray, context_lens: np.ndarray, *, num_kv_heads: int,
+                block_size: int, scale: float) -> np.ndarray:
+    """fp64 multi-row causal decode: q [S, R, H, D]; row b of sequence s
+    attends to the first min(context_len, cap) - (R - 1 - b) tokens.
+    Returns [S, R, H, D]."""
+    _need(q, np.float32, "q")
+    for a, n in ((key_cache, "key_cache"), (value_cache, "value_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens")):
+        _need(a, np.uint32, n)
+    S, R, H, D = q.shape
+    out = np.empty((S, R, H, D), dtype=np.float64)
+    _load().oracle_decode_rows(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
+                               _ptr(block_tables), _ptr(context_lens), S, R, H, num_kv_heads, D,
+                               block_size, block_tables.shape[1], float(scale))
     return out
 
 

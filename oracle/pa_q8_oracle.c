@@ -157,17 +157,15 @@ static int64_t clamped_len(const uint32_t *context_lens, int s, int max_blocks_p
     return c < cap ? c : cap;
 }
 
-/* Partial attention of query row (s, h) over logical tokens [t0, t1):
- * m = max_t z_t, l = sum_t e^(z_t - m), acc[d] = sum_t e^(z_t - m) v_t[d],
- * z_t = scale * q . k_t.  An empty range gives m = -inf, l = 0, acc = 0. */
-void oracle_decode_partial(const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
-                           const uint32_t *block_tables, int num_heads, int num_kv_heads,
-                           int head_size, int block_size, int max_blocks_per_seq, double scale,
-                           int s, int h, int64_t t0, int64_t t1,
-                           double *m_out, double *l_out, double *acc)
+/* Partial attention of the query vector qv (head_size floats) against kv head
+ * g of sequence s over logical tokens [t0, t1): m = max_t z_t,
+ * l = sum_t e^(z_t - m), acc[d] = sum_t e^(z_t - m) v_t[d], z_t = scale * q . k_t.
+ * An empty range gives m = -inf, l = 0, acc = 0. */
+static void attend(const float *qv, const uint32_t *key_cache, const uint32_t *value_cache,
+                   const uint32_t *block_tables, int num_kv_heads, int head_size, int block_size,
+                   int max_blocks_per_seq, double scale, int s, int g, int64_t t0, int64_t t1,
+                   double *m_out, double *l_out, double *acc)
 {
-    const int g = h / (num_heads / num_kv_heads);
-    const float *qv = q + ((int64_t)s * num_heads + h) * head_size;
     for (int d = 0; d < head_size; ++d) acc[d] = 0.0;
     *l_out = 0.0;
     *m_out = -INFINITY;
@@ -196,6 +194,20 @@ void oracle_decode_partial(const float *q, const uint32_t *key_cache, const uint
     *l_out = l;
     free(vec);
     free(z);
+}
+
+/* Partial attention of query row (s, h) over logical tokens [t0, t1), with
+ * kv head g = h / (num_heads / num_kv_heads); q is [num_seqs][num_heads][head_size]. */
+void oracle_decode_partial(const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                           const uint32_t *block_tables, int num_heads, int num_kv_heads,
+                           int head_size, int block_size, int max_blocks_per_seq, double scale,
+                           int s, int h, int64_t t0, int64_t t1,
+                           double *m_out, double *l_out, double *acc)
+{
+    const int g = h / (num_heads / num_kv_heads);
+    const float *qv = q + ((int64_t)s * num_heads + h) * head_size;
+    attend(qv, key_cache, value_cache, block_tables, num_kv_heads, head_size, block_size,
+           max_blocks_per_seq, scale, s, g, t0, t1, m_out, l_out, acc);
 }
 
 /* Merge n partials (m_i, l_i, acc_i[D]) of one query row by their
@@ -239,6 +251,37 @@ void oracle_decode(double *out, const float *q, const uint32_t *key_cache,
                               head_size, block_size, max_blocks_per_seq, scale, s, h, 0, c,
                               &m, &l, o);
         if (c == 0) continue;           /* all zeros */
+        for (int d = 0; d < head_size; ++d) o[d] /= l;
+    }
+}
+
+/* Multi-row causal decode ("attention.rs", attention_b: the per-row loop
+ * over b with t_len = base_pos + b + 1).  Sequence s holds
+ * c = min(context_len, max_blocks_per_seq * block_size) tokens, the last
+ * num_rows of which are the rows being decoded; query row b attends to the
+ * first c - (num_rows - 1 - b) tokens (none -> a zero row).
+ * q and out are [num_seqs][num_rows][num_heads][head_size]. */
+void oracle_decode_rows(double *out, const float *q, const uint32_t *key_cache,
+                        const uint32_t *value_cache, const uint32_t *block_tables,
+                        const uint32_t *context_lens, int num_seqs, int num_rows, int num_heads,
+                        int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                        double scale)
+{
+    const int64_t n = (int64_t)num_seqs * num_rows * num_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        const int s = (int)(i / ((int64_t)num_rows * num_heads));
+        const int b = (int)((i / num_heads) % num_rows);
+        const int h = (int)(i % num_heads);
+        double *o = out + i * head_size;
+        const int64_t c = clamped_len(context_lens, s, max_blocks_per_seq, block_size);
+        const int64_t t1 = c - (num_rows - 1 - b);
+        double m, l;
+        const int g = h / (num_heads / num_kv_heads);
+        const float *qv = q + (((int64_t)s * num_rows + b) * num_heads + h) * head_size;
+        attend(qv, key_cache, value_cache, block_tables, num_kv_heads, head_size, block_size,
+               max_blocks_per_seq, scale, s, g, 0, t1 > 0 ? t1 : 0, &m, &l, o);
+        if (t1 <= 0) continue;          /* zeros */
         for (int d = 0; d < head_size; ++d) o[d] /= l;
     }
 }

@@ -392,3 +392,65 @@ def test_dequant_view_roundtrip(oracle_lib):
     x = case["key"].astype(np.float64)
     amax = np.abs(x).max(axis=-1, keepdims=True)
     assert np.all(np.abs(K - x) <= amax / 254 * (1 + 2.0**-14))
+
+
+# ---------------------------------------------------- multi-row causal decode
+
+
+def _rows_case(rng, S, R, H, Hk, D, B, lens):
+    case = random_paged_case(rng, S=S, H=H, Hk=Hk, D=D, B=B, lens=lens)
+    case["qr"] = rng.standard_normal((S, R, H, D)).astype(np.float32)
+    case["R"] = R
+    return case
+
+
+def _rows(case, cl=None, scale=0.125):
+    return oracle.decode_rows(case["qr"], case["kc"], case["vc"], case["bt"],
+                              case["cl"] if cl is None else cl, num_kv_heads=case["Hk"],
+                              block_size=case["B"], scale=scale)
+
+
+@pytest.mark.parametrize("R", [1, 2, 5])
+def test_rows_vs_causal_brute_force(oracle_lib, R):
+    """Row b of sequence s attends to its first c_s - (R - 1 - b) tokens
+    ("attention.rs", attention_b: t_len = base_pos + b + 1): a dense
+    numpy/scipy softmax over that prefix, kv heads repeated over their group."""
+    rng = np.random.default_rng(40 + R)
+    S, H, Hk, D, B = 3, 8, 2, 64, 16
+    lens = [37, 3, 100]
+    case = _rows_case(rng, S, R, H, Hk, D, B, lens)
+    got = _rows(case, scale=0.125)
+    r = H // Hk
+    for s in range(S):
+        c = lens[s]
+        K = np.repeat(dense_context(case["kc"], case["bt"], s, c, D), r, axis=1)
+        V = np.repeat(dense_context(case["vc"], case["bt"], s, c, D), r, axis=1)
+        for b in range(R):
+            n = c - (R - 1 - b)
+            if n <= 0:
+                assert np.all(got[s, b] == 0.0)
+                continue
+            z = 0.125 * np.einsum("hd,chd->hc", case["qr"][s, b].astype(np.float64), K[:n])
+            want = np.einsum("hc,chd->hd", softmax(z, axis=1), V[:n])
+            np.testing.assert_allclose(got[s, b], want, rtol=1e-12, atol=1e-13)
+
+
+def test_rows_reduce_to_single_query_decode(oracle_lib):
+    """R = 1 is the single-query decode; row b equals the single-query decode
+    of the context cut to c - (R - 1 - b) tokens (clamp first, then cut)."""
+    rng = np.random.default_rng(44)
+    S, R, H, Hk, D, B = 2, 4, 4, 2, 64, 16
+    case = _rows_case(rng, S, R, H, Hk, D, B, [50, 20])
+    cap = case["Nb"] * B
+    cl = np.array([10_000, 20], dtype=np.uint32)           # sequence 0 clamps to cap first
+    got = _rows(case, cl=cl)
+    for b in range(R):
+        cut = np.array([min(int(c), cap) - (R - 1 - b) for c in cl], dtype=np.uint32)
+        want = oracle.decode(np.ascontiguousarray(case["qr"][:, b]), case["kc"], case["vc"], case["bt"],
+                             cut, num_kv_heads=Hk, block_size=B, scale=0.125)
+        np.testing.assert_array_equal(got[:, b], want)
+    one = dict(case, qr=np.ascontiguousarray(case["qr"][:, :1]))
+    np.testing.assert_array_equal(
+        _rows(one, cl=cl)[:, 0],
+        oracle.decode(np.ascontiguousarray(case["qr"][:, 0]), case["kc"], case["vc"], case["bt"], cl,
+                      num_kv_heads=Hk, block_size=B, scale=0.125))
