@@ -505,8 +505,9 @@ def run_ours(args) -> None:
 # ------------------------------------------------------- per-workload table
 
 def run_configs(args) -> None:
-    """Decode throughput of every workload (both kernel families), one JSON
-    line per (workload, family) -- a report next to the bench line, not a
+    """Decode throughput of every workload (both kernel families; 1 and 4
+    query rows per sequence on the batches that fill the GPU), one JSON line
+    per (workload, rows, family) -- a report next to the bench line, not a
     bench line itself."""
     import torch
 
@@ -538,15 +539,31 @@ def run_configs(args) -> None:
         w.key = w.value = None
         q = torch.from_numpy(w.q).to(dev)
         bt, cl, out = u32(w.block_tables), u32(w.context_lens), torch.empty_like(q)
-        nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens)
-        for kernel in (pk.PA_Q8_KERNEL_TENSOR_CORE, pk.PA_Q8_KERNEL_CUDA_CORE):
-            plan = pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq, kernel=kernel)
-            ws = torch.empty(pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq,
-                                                            kernel=kernel), dtype=torch.uint8, device=dev)
+        # R > 1: causal decode of R query rows per sequence (pa_q8_decode_rows),
+        # on the workloads whose batches fill the GPU
+        row_counts = (1, 4) if name in ("llama8b", "long", "large") else (1,)
+        for R, kernel in [(R, k) for R in row_counts
+                          for k in (pk.PA_Q8_KERNEL_TENSOR_CORE, pk.PA_Q8_KERNEL_CUDA_CORE)]:
+            nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, R)
+            if R == 1:
+                plan = pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq, kernel=kernel)
+                ws = torch.empty(pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq,
+                                                                kernel=kernel), dtype=torch.uint8, device=dev)
 
-            def run():
-                pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale,
-                                workspace=ws, kernel=kernel)
+                def run():
+                    pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale,
+                                    workspace=ws, kernel=kernel)
+            else:
+                plan = {"partition_tokens": None}
+                qr = torch.from_numpy(wl.query_rows(w, R)).to(dev)
+                outr = torch.empty_like(qr)
+                ws = torch.empty(pk.pa_q8_decode_rows_workspace_size(S, R, H, Hk, D, B, cfg.max_blocks_per_seq,
+                                                                     kernel=kernel),
+                                 dtype=torch.uint8, device=dev)
+
+                def run():
+                    pk.pa_q8_decode_rows(outr, qr, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B,
+                                         scale=w.scale, workspace=ws, kernel=kernel)
             for _ in range(max(3, args.warmup)):
                 torch.sum(flush, dim=0, out=sink)
                 run()
@@ -561,7 +578,7 @@ def run_configs(args) -> None:
                 ts.append(a.elapsed_time(b))
             ms = float(np.median(ts))
             print(json.dumps({"kind": "decode per workload", "workload": name, "description": cfg.description,
-                              "kernel": {1: "cuda-core", 2: "tensor-core"}[kernel],
+                              "query_rows": R, "kernel": {1: "cuda-core", 2: "tensor-core"}[kernel],
                               "partition_tokens": plan["partition_tokens"], "ms": round(ms, 4),
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),

@@ -186,6 +186,35 @@ size_t pa_q8_decode_workspace_size_ex(int num_seqs, int num_heads, int num_kv_he
                                       int head_size, int block_size, int max_blocks_per_seq,
                                       const pa_q8_decode_options *opts);
 
+/*
+ * pa_q8_decode_rows -- causal decode of several query rows per sequence
+ * ("attention.rs", attention_b: the loop over rows b whose visible length is
+ * the base position + b + 1).  Sequence s holds c = min(context_lens[s],
+ * max_blocks_per_seq * block_size) tokens in the caches, the last num_rows of
+ * which belong to the rows being decoded: query row b (0 <= b < num_rows)
+ * attends to the first c - (num_rows - 1 - b) tokens; a row that sees none is
+ * written as zeros.  num_rows = 1 is pa_q8_decode_ex.
+ *
+ *   out, q          device f32 [num_seqs][num_rows][num_heads][head_size], 16-byte aligned
+ *   num_rows        query rows per sequence, >= 1; num_kv_heads * num_rows *
+ *                   (num_heads / num_kv_heads) <= 65535
+ *   workspace       >= pa_q8_decode_rows_workspace_size() bytes (never 0)
+ * Every other argument, the status codes and the kernel families are those
+ * of pa_q8_decode_ex.  The rows of a kv head share each K/V tile the kernel
+ * copies, so the cache is read once per call whatever num_rows is.
+ */
+int pa_q8_decode_rows(float *out, const float *q,
+                      const uint32_t *key_cache, const uint32_t *value_cache,
+                      const uint32_t *block_tables, const uint32_t *context_lens,
+                      int num_seqs, int num_rows, int num_heads, int num_kv_heads,
+                      int head_size, int block_size, int max_blocks_per_seq,
+                      int64_t num_blocks, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream, const pa_q8_decode_options *opts);
+
+size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads,
+                                        int num_kv_heads, int head_size, int block_size,
+                                        int max_blocks_per_seq, const pa_q8_decode_options *opts);
+
 /* The launch plan pa_q8_decode_ex would use (no launch): kernel family,
  * tokens per partition, partitions per sequence (grid x), CTAs launched for
  * the attention kernel.  Any output pointer may be NULL.  Needs a current

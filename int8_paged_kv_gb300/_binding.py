@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
         L.pa_q8_decode.argtypes = dec
         L.pa_q8_decode_ex.restype = i32
         L.pa_q8_decode_ex.argtypes = dec + [ctypes.POINTER(DecodeOptions)]
+        L.pa_q8_decode_rows.restype = i32
+        L.pa_q8_decode_rows.argtypes = ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32,
+                                         P, sz, P, ctypes.POINTER(DecodeOptions)])
+        L.pa_q8_decode_rows_workspace_size.restype = sz
+        L.pa_q8_decode_rows_workspace_size.argtypes = [i32] * 7 + [ctypes.POINTER(DecodeOptions)]
         L.pa_q8_decode_workspace_size.restype = sz
         L.pa_q8_decode_workspace_size.argtypes = [i32] * 6
         L.pa_q8_decode_workspace_size_ex.restype = sz
@@ -192,6 +197,46 @@ def pa_q8_decode(out, q, key_cache, value_cache, block_tables, context_lens, *, 
         int(block_size), Nb, nb, float(scale), ws_ptr, ws_bytes, _stream(stream),
         _opts(kernel, partition_tokens))
     _check("pa_q8_decode", rc)
+    return out
+
+
+def pa_q8_decode_rows_workspace_size(num_seqs, num_rows, num_heads, num_kv_heads, head_size,
+                                     block_size, max_blocks_per_seq, *, kernel: int = 0,
+                                     partition_tokens: int = 0) -> int:
+    return int(lib().pa_q8_decode_rows_workspace_size(
+        int(num_seqs), int(num_rows), int(num_heads), int(num_kv_heads), int(head_size),
+        int(block_size), int(max_blocks_per_seq), _opts(kernel, partition_tokens)))
+
+
+def pa_q8_decode_rows(out, q, key_cache, value_cache, block_tables, context_lens, *,
+                      num_kv_heads: int, block_size: int, scale: float,
+                      num_blocks: int | None = None, workspace=None, kernel: int = 0,
+                      partition_tokens: int = 0, stream=None):
+    """out[S, R, H, D] = causal multi-row decode: row b of sequence s attends
+    to the first c - (R - 1 - b) cached tokens (see include/pa_q8.h).
+    Returns `out`."""
+    import torch
+    S, R, H, D = q.shape
+    if out.shape != q.shape or not out.is_contiguous() or not q.is_contiguous():
+        raise ValueError("q and out must be contiguous [num_seqs, num_rows, num_heads, head_size]")
+    Nb = int(block_tables.shape[1])
+    if block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("block_tables / context_lens do not match num_seqs")
+    nb = int(key_cache.shape[0]) if num_blocks is None else int(num_blocks)
+    need = pa_q8_decode_rows_workspace_size(S, R, H, num_kv_heads, D, block_size, Nb, kernel=kernel,
+                                            partition_tokens=partition_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_q8_decode_rows(
+        _cuda(out, torch.float32, "out"), _cuda(q, torch.float32, "q"),
+        _cuda(key_cache, torch.uint32, "key_cache"), _cuda(value_cache, torch.uint32, "value_cache"),
+        _cuda(block_tables, torch.uint32, "block_tables"),
+        _cuda(context_lens, torch.uint32, "context_lens"), S, R, H, int(num_kv_heads), D,
+        int(block_size), Nb, nb, float(scale), ws_ptr, ws_bytes, _stream(stream),
+        _opts(kernel, partition_tokens))
+    _check("pa_q8_decode_rows", rc)
     return out
 
 

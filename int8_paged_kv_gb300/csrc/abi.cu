@@ -51,15 +51,15 @@ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 bool head_size_ok(int d) { return d == 64 || d == 128 || d == 256; }
 
 int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int block_size,
-                       int max_blocks_per_seq) {
+                       int max_blocks_per_seq, int num_rows = 1) {
     if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 ||
-        max_blocks_per_seq <= 0)
+        max_blocks_per_seq <= 0 || num_rows <= 0)
         return PA_Q8_EINVAL;
     if (num_heads % num_kv_heads != 0 || head_size % 4 != 0 || block_size % 4 != 0) return PA_Q8_EINVAL;
     if (!head_size_ok(head_size) || !pow2(block_size) || block_size > 1024) return PA_Q8_EUNSUPPORTED;
     if (num_seqs > 65535) return PA_Q8_EUNSUPPORTED;            // grid z
-    if ((int64_t)num_kv_heads * ((num_heads / num_kv_heads + 15) / 16 + 1) > 65535)
-        return PA_Q8_EUNSUPPORTED;                              // grid y
+    // grid y = kv heads x groups of (row, head) pairs; at worst one pair per group
+    if ((int64_t)num_kv_heads * num_rows * (num_heads / num_kv_heads) > 65535) return PA_Q8_EUNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30) return PA_Q8_EUNSUPPORTED;
     return PA_Q8_OK;
 }
@@ -74,14 +74,71 @@ int plan_for(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int num_sms
 }
 
 void fill_shape(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_heads, int head_size,
-                int block_size, int max_blocks_per_seq) {
+                int block_size, int max_blocks_per_seq, int num_rows = 1) {
     std::memset(&a, 0, sizeof a);
     a.num_seqs = num_seqs;
+    a.num_rows = num_rows;
     a.num_heads = num_heads;
     a.num_kv_heads = num_kv_heads;
     a.head_size = head_size;
     a.block_size = block_size;
     a.max_blocks_per_seq = max_blocks_per_seq;
+}
+
+size_t workspace_impl(int num_seqs, int num_rows, int num_heads, int num_kv_heads, int head_size,
+                      int block_size, int max_blocks_per_seq, const pa_q8_decode_options *opts) {
+    if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
+                           num_rows) != PA_Q8_OK)
+        return 0;
+    pa_q8::DecodeArgs a;
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_rows);
+    int sms = 0;
+    if (device_info(nullptr, &sms) != PA_Q8_OK) sms = 152;     // size query without a device
+    if (plan_for(a, opts, sms) != PA_Q8_OK) return 0;
+    return pa_q8::plan_workspace_bytes(a);
+}
+
+int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_rows,
+                int num_heads, int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
+                const pa_q8_decode_options *opts) {
+    int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
+                                num_rows);
+    if (rc != PA_Q8_OK) return rc;
+    if (num_blocks <= 0) return PA_Q8_EINVAL;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens) return PA_Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        !aligned4(block_tables) || !aligned4(context_lens))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int sms = 0;
+    rc = device_info(&status, &sms);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::DecodeArgs a;
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_rows);
+    rc = plan_for(a, opts, sms);
+    if (rc != PA_Q8_OK) return rc;
+    const size_t need = pa_q8::plan_workspace_bytes(a);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return PA_Q8_EWORKSPACE;
+        if (!aligned16(workspace)) return PA_Q8_EALIGN;
+        pa_q8::plan_workspace_layout(a, workspace);
+    }
+    a.out = out;
+    a.q = q;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.status = status;
+    if (pa_q8::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
 }
 
 }  // namespace
@@ -133,15 +190,14 @@ int pa_q8_reshape_and_cache(const float *key, const float *value, uint32_t *key_
 size_t pa_q8_decode_workspace_size_ex(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                                       int block_size, int max_blocks_per_seq,
                                       const pa_q8_decode_options *opts) {
-    if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq) !=
-        PA_Q8_OK)
-        return 0;
-    pa_q8::DecodeArgs a;
-    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
-    int sms = 0;
-    if (device_info(nullptr, &sms) != PA_Q8_OK) sms = 152;     // size query without a device
-    if (plan_for(a, opts, sms) != PA_Q8_OK) return 0;
-    return pa_q8::plan_workspace_bytes(a);
+    return workspace_impl(num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, opts);
+}
+
+size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads, int num_kv_heads,
+                                        int head_size, int block_size, int max_blocks_per_seq,
+                                        const pa_q8_decode_options *opts) {
+    return workspace_impl(num_seqs, num_rows, num_heads, num_kv_heads, head_size, block_size,
+                          max_blocks_per_seq, opts);
 }
 
 size_t pa_q8_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
@@ -174,41 +230,19 @@ int pa_q8_decode_ex(float *out, const float *q, const uint32_t *key_cache, const
                     int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
                     int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
                     const pa_q8_decode_options *opts) {
-    int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
-    if (rc != PA_Q8_OK) return rc;
-    if (num_blocks <= 0) return PA_Q8_EINVAL;
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens) return PA_Q8_EINVAL;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
-        !aligned4(block_tables) || !aligned4(context_lens))
-        return PA_Q8_EALIGN;
-    uint32_t *status = nullptr;
-    int sms = 0;
-    rc = device_info(&status, &sms);
-    if (rc != PA_Q8_OK) return rc;
-    pa_q8::DecodeArgs a;
-    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq);
-    rc = plan_for(a, opts, sms);
-    if (rc != PA_Q8_OK) return rc;
-    const size_t need = pa_q8::plan_workspace_bytes(a);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return PA_Q8_EWORKSPACE;
-        if (!aligned16(workspace)) return PA_Q8_EALIGN;
-        pa_q8::plan_workspace_layout(a, workspace);
-    }
-    a.out = out;
-    a.q = q;
-    a.key_cache = key_cache;
-    a.value_cache = value_cache;
-    a.block_tables = block_tables;
-    a.context_lens = context_lens;
-    a.num_blocks = num_blocks;
-    a.scale = scale;
-    a.status = status;
-    if (pa_q8::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-        cudaGetLastError();
-        return PA_Q8_ECUDA;
-    }
-    return PA_Q8_OK;
+    return decode_impl(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs, 1, num_heads,
+                       num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale, workspace,
+                       workspace_bytes, stream, opts);
+}
+
+int pa_q8_decode_rows(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                      const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_rows,
+                      int num_heads, int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
+                      int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
+                      const pa_q8_decode_options *opts) {
+    return decode_impl(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs, num_rows,
+                       num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale,
+                       workspace, workspace_bytes, stream, opts);
 }
 
 int pa_q8_decode(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,

@@ -29,6 +29,7 @@
 // warp leaves only after the copies it issued have landed.
 #include <algorithm>
 #include <cfloat>
+#include <climits>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -74,17 +75,21 @@ struct Params {
     int PT;                 // tokens per partition
     int NP;                 // partitions per sequence (grid x)
     int r;                  // num_heads / num_kv_heads
+    int R;                  // query rows per sequence (1 = single-query decode)
+    int rv;                 // R * r: (row, head) "virtual heads" per kv head
     int heads_per_cta;
     int head_groups;
     const unsigned long long *order;  // [S]: (clamped length << 32 | sequence) of grid z,
                                       // longest context first
     uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
-    float *pml;             // [S][H][NP][2]
-    float *pacc;            // [S][H][NP][D]
+    float *pml;             // [S][R][H][NP][2]
+    float *pacc;            // [S][R][H][NP][D]
     uint32_t *status;
 };
 
-// Which CTA this is and the token range it owns.
+// Which CTA this is and the token range it owns.  The CTA serves virtual
+// heads h0 .. h0 + nh - 1 of kv head g: virtual head vh is query row
+// b = vh / r, head g * r + vh % r of that row.
 struct Work {
     int s, g, h0, nh, p;
     int c;          // clamped context length
@@ -97,8 +102,8 @@ __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
     w.p = blockIdx.x;
     w.g = blockIdx.y / P.head_groups;
     const int hg = blockIdx.y % P.head_groups;
-    w.h0 = w.g * P.r + hg * P.heads_per_cta;
-    w.nh = min(P.heads_per_cta, P.r - hg * P.heads_per_cta);
+    w.h0 = hg * P.heads_per_cta;
+    w.nh = min(P.heads_per_cta, P.rv - w.h0);
     const int64_t cap = (int64_t)P.Nb * P.B;
     if (P.order) {
         // written by the prep kernel that precedes this grid on the stream
@@ -117,13 +122,28 @@ __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
     return w.len > 0;
 }
 
+// Row of q / out (in units of head_size) of virtual head vh of the CTA's
+// group: sequence s, query row vh / r, head g * r + vh % r.
+__device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) {
+    const int b = vh / P.r;
+    return ((int64_t)w.s * P.R + b) * P.H + (int64_t)w.g * P.r + (vh - b * P.r);
+}
+
+// Tokens of this partition virtual head vh attends to: query row b sees the
+// first c - (R - 1 - b) tokens of the context ("attention.rs", attention_b:
+// t_len = base_pos + b + 1).
+__device__ __forceinline__ int row_len(const Params &P, const Work &w, int vh) {
+    const int cb = w.c - (P.R - 1 - vh / P.r);
+    return max(0, min(cb - w.t_begin, P.PT));
+}
+
 // Zero output rows of a sequence whose context is empty (partition 0 only).
 template <int D>
 __device__ void write_zero_rows(const Params &P, const Work &w) {
     if (w.p != 0 || w.c != 0) return;
     for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
         const int hh = i / D, d = i % D;
-        P.out[((int64_t)w.s * P.H + w.h0 + hh) * D + d] = 0.0f;
+        P.out[qrow(P, w, w.h0 + hh) * D + d] = 0.0f;
     }
 }
 
@@ -226,11 +246,12 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     for (int hh = warp; hh < w.nh; hh += nwarps) {
-        const int64_t row0 = ((int64_t)w.s * P.H + w.h0 + hh) * P.NP;
+        const int64_t row0 = qrow(P, w, w.h0 + hh) * P.NP;
         float M = -INFINITY;
         for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        if (M == -INFINITY) M = 0.0f;       // a query row that sees no token: weights 0, row 0
         float L = 0.0f;
         for (int p = lane; p < np; p += 32)
             L += __ldcg(P.pml + (row0 + p) * 2 + 1) * fast_exp2(__ldcg(P.pml + (row0 + p) * 2) - M);
@@ -238,7 +259,7 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
         if (lane == 0) {
             scratch[2 * hh] = M;
-            scratch[2 * hh + 1] = 1.0f / L;
+            scratch[2 * hh + 1] = L > 0.0f ? 1.0f / L : 0.0f;
         }
     }
     __syncthreads();
@@ -254,7 +275,7 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
             const int i = min(i0 + u * (int)blockDim.x, n_out - 1);
             const int hh = i / D;
             dd[u] = i % D;
-            prow[u] = ((int64_t)w.s * P.H + w.h0 + hh) * P.NP;
+            prow[u] = qrow(P, w, w.h0 + hh) * P.NP;
             M[u] = scratch[2 * hh];
             a[u] = 0.0f;
         }
@@ -270,7 +291,7 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
             const int i = i0 + u * (int)blockDim.x;
             if (i < n_out) {
                 const int hh = i / D;
-                P.out[((int64_t)w.s * P.H + w.h0 + hh) * D + dd[u]] = a[u] * scratch[2 * hh + 1];
+                P.out[qrow(P, w, w.h0 + hh) * D + dd[u]] = a[u] * scratch[2 * hh + 1];
             }
         }
     }
@@ -306,11 +327,12 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
         const float *f = fac + hh * (n_slots + 2);
         float A = 0.0f;
         for (int sl = 0; sl < n_slots; ++sl) A = fmaf(accs[(sl * heads_stride + hh) * D + d], f[sl], A);
-        const int h = w.h0 + hh;
+        const int64_t qr = qrow(P, w, w.h0 + hh);
         if (w.single) {
-            P.out[((int64_t)w.s * P.H + h) * D + d] = A / f[n_slots + 1];
+            // a query row that sees no token (L = 0) gets a zero row
+            P.out[qr * D + d] = f[n_slots + 1] > 0.0f ? A / f[n_slots + 1] : 0.0f;
         } else {
-            const int64_t row = ((int64_t)w.s * P.H + h) * P.NP + w.p;
+            const int64_t row = qr * P.NP + w.p;
             P.pacc[row * D + d] = A;
             if (d == 0) {
                 P.pml[row * 2] = f[n_slots];
@@ -422,7 +444,11 @@ decode_tc_kernel(Params P) {
 
     const int nh_tile = max(0, min(8, w.nh - 8 * ht));
     const bool row_ok = gq < nh_tile;
-    const int h = w.h0 + 8 * ht + gq;
+    const int vh = w.h0 + 8 * ht + gq;                      // this thread's virtual head
+    // tokens this row sees in the partition (query row b sees c - (R-1-b));
+    // chunks below the warp's smallest length need no masking
+    const int len_row = row_ok ? row_len(P, w, vh) : w.len;
+    const int len_min = __reduce_min_sync(0xFFFFFFFFu, (unsigned)len_row);
 
     // q of head gq scaled by 2^-eq into [1, 2) in magnitude, as hi/lo f16
     // pairs.  Head size 256 keeps these fragments in shared memory.
@@ -430,12 +456,12 @@ decode_tc_kernel(Params P) {
     uint4 *qf = reinterpret_cast<uint4 *>(smem + L.extra);           // [HT][NKS][32]
     float qk2;
     {
-        const float4 *qrow = reinterpret_cast<const float4 *>(
-            P.q + ((int64_t)w.s * P.H + (row_ok ? h : w.h0)) * D);
+        const float4 *qv = reinterpret_cast<const float4 *>(
+            P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
         float mx = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
-            const float4 v = row_ok ? __ldg(qrow + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
             mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -445,7 +471,7 @@ decode_tc_kernel(Params P) {
         qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
-            const float4 v = row_ok ? __ldg(qrow + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
             uint32_t f0, f1, f2, f3;
             split_f16x2(v.x * down, v.y * down, f0, f1);
             split_f16x2(v.z * down, v.w * down, f2, f3);
@@ -481,7 +507,7 @@ decode_tc_kernel(Params P) {
                              (RING * ts + k) * (L.slot_bytes / 4);
         const uint32_t *sV = sK + kChunk * W;
         const int t0 = (ts + SLOTS * i) * kChunk;              // partition-relative
-        const bool full = t0 + kChunk <= w.len;
+        const bool full = t0 + kChunk <= len_min;
 
         // ---- S = Q K^T for the 32 tokens (n-tile j holds tokens 8j .. 8j+7)
         float s[4][4];
@@ -516,7 +542,7 @@ decode_tc_kernel(Params P) {
                 float zz = (s[j][e] + s[j][e + 2]) * kscale * qk2;
                 float vv = __uint_as_float(sV[t * W + D / 4]);
                 if (!full) {
-                    const bool valid = t0 + t < w.len;
+                    const bool valid = t0 + t < len_row;
                     zz = valid ? zz : -INFINITY;
                     vv = valid ? vv : 0.0f;
                 }
@@ -549,10 +575,12 @@ decode_tc_kernel(Params P) {
             E = E_new;
             wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
         }
+        // a row that has seen no token yet keeps m = -inf; its z are all -inf
+        const float m_ref = m == -INFINITY ? 0.0f : m;
         float pw[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const float p = fast_exp2(z[u] - m);        // <= 2^kLazy; masked tokens: 2^-inf = 0
+            const float p = fast_exp2(z[u] - m_ref);    // <= 2^kLazy; masked tokens: 2^-inf = 0
             lsum += p;
             pw[u] = p * vs[u] * wscale;
         }
@@ -626,6 +654,10 @@ __device__ __forceinline__ void codes4_to_f32(uint32_t x, float &a, float &b, fl
     d = __uint_as_float(prmt_i<0x7653u>(u, hi)) - 8388736.0f;
 }
 
+// shared memory beside the ring: q rows [NH][D], weights [slot][NH][32], row lags [NH]
+template <int D, int NH>
+__host__ __device__ constexpr uint32_t cc_extra() { return NH * D * 4 + kCcSlots * 32 * NH * 4 + NH * 4; }
+
 template <int D, int NH>
 __global__ void __launch_bounds__(kCcSlots * 32, (D == 256 ? 1 : 2))
 decode_cc_kernel(Params P) {
@@ -642,14 +674,14 @@ decode_cc_kernel(Params P) {
         write_zero_rows<D>(P, w);
         return;
     }
-    const uint32_t extra = NH * D * 4 + kCcSlots * 32 * NH * 4;
-    const Layout L = make_layout(D, kCcSlots, RING, P.PT, P.B, extra);
+    const Layout L = make_layout(D, kCcSlots, RING, P.PT, P.B, cc_extra<D, NH>());
     const int ts = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bars = smem_addr(smem + L.bars) + 8 * RING * ts;
     const uint32_t ring = smem_addr(smem + L.ring) + RING * L.slot_bytes * ts;
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
     float *sq = reinterpret_cast<float *>(smem + L.extra);             // [NH][D]
     float *myw = sq + NH * D + ts * 32 * NH;                           // [NH][32]
+    int *slag = reinterpret_cast<int *>(sq + NH * D + kCcSlots * 32 * NH);   // [NH]
     const int nchunks = (w.len + kChunk - 1) / kChunk;
     const int my_n = ts < nchunks ? (nchunks - ts + kCcSlots - 1) / kCcSlots : 0;
     const uint64_t policy = l2_policy_evict_first();
@@ -661,8 +693,11 @@ decode_cc_kernel(Params P) {
     load_table(P, w, const_cast<uint32_t *>(table));
     for (int i = threadIdx.x; i < NH * D; i += blockDim.x) {
         const int hh = i / D;
-        sq[i] = hh < w.nh ? __ldg(P.q + ((int64_t)w.s * P.H + w.h0 + hh) * D + (i % D)) : 0.0f;
+        sq[i] = hh < w.nh ? __ldg(P.q + qrow(P, w, w.h0 + hh) * D + (i % D)) : 0.0f;
     }
+    // query row b of R sees the first c - (R-1-b) tokens: its lag behind the context
+    if (threadIdx.x < NH)
+        slag[threadIdx.x] = (int)threadIdx.x < w.nh ? P.R - 1 - (w.h0 + (int)threadIdx.x) / P.r : INT_MAX;
     __syncthreads();
     int issued = 0;
     for (; issued < RING && issued < my_n; ++issued)
@@ -694,6 +729,7 @@ decode_cc_kernel(Params P) {
         const int t0 = (ts + kCcSlots * i) * kChunk;
         // ---- logits, lane = token
         const bool valid = t0 + lane < w.len;
+        const int ahead = w.c - w.t_begin - t0 - lane;        // tokens from this one to the context end
         float dot[NH];
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh) dot[hh] = 0.0f;
@@ -712,7 +748,8 @@ decode_cc_kernel(Params P) {
         const float vscale = valid ? __uint_as_float(sV[lane * W + WORDS]) : 0.0f;
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh) {
-            const float z = valid ? dot[hh] * kscale : -INFINITY;
+            const bool seen = valid && slag[hh] < ahead;      // causal limit of this query row
+            const float z = seen ? dot[hh] * kscale : -INFINITY;
             float cm = z;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
@@ -727,7 +764,7 @@ decode_cc_kernel(Params P) {
                 }
                 m[hh] = m_new;
             }
-            const float p = valid ? fast_exp2(z - m[hh]) : 0.0f;
+            const float p = seen ? fast_exp2(z - m[hh]) : 0.0f;
             lsum[hh] += p;
             myw[hh * 32 + lane] = p * vscale;
         }
@@ -875,6 +912,8 @@ Params make_params(const DecodeArgs &a) {
     P.scale_log2 = a.scale * kLog2e;
     P.PT = a.partition_tokens; P.NP = a.num_partitions;
     P.r = a.num_heads / a.num_kv_heads;
+    P.R = a.num_rows;
+    P.rv = P.R * P.r;
     P.heads_per_cta = a.heads_per_cta; P.head_groups = a.head_groups;
     P.order = a.order; P.counters = a.counters; P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
     return P;
@@ -916,8 +955,7 @@ cudaError_t launch_tc(const Params &P, cudaStream_t st) {
 
 template <int D, int NH>
 cudaError_t launch_cc_nh(const Params &P, cudaStream_t st) {
-    const uint32_t extra = NH * D * 4 + kCcSlots * 32 * NH * 4;
-    const Layout L = make_layout(D, kCcSlots, cc_ring<D>(), P.PT, P.B, extra);
+    const Layout L = make_layout(D, kCcSlots, cc_ring<D>(), P.PT, P.B, cc_extra<D, NH>());
     return launch_attn(decode_cc_kernel<D, NH>, P, L.total, kCcSlots * 32, st);
 }
 
@@ -954,7 +992,10 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
 }  // namespace
 
 bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int num_sms) {
-    const int r = a.num_heads / a.num_kv_heads;
+    if (a.num_rows < 1) a.num_rows = 1;
+    // (query row, head) pairs served per kv head: the rows of one sequence
+    // share their kv group's K/V read like the heads of a GQA group
+    const int r = a.num_rows * (a.num_heads / a.num_kv_heads);
     a.kernel = requested_kernel == kAuto ? kTensorCore : requested_kernel;
     if (a.kernel == kTensorCore) {
         a.heads_per_cta = r < 16 ? r : 16;
@@ -1005,7 +1046,7 @@ size_t plan_workspace_bytes(const DecodeArgs &a) {
     const size_t order = round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return order;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-    const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;
+    const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions;
     return order + round256(groups * sizeof(uint32_t)) + round256(rows * 2 * sizeof(float)) +
            rows * a.head_size * sizeof(float);
 }
@@ -1016,7 +1057,7 @@ void plan_workspace_layout(DecodeArgs &a, void *workspace) {
     p += round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-    const size_t rows = (size_t)a.num_seqs * a.num_heads * a.num_partitions;
+    const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions;
     a.counters = reinterpret_cast<uint32_t *>(p);
     p += round256(groups * sizeof(uint32_t));
     a.partial_ml = reinterpret_cast<float *>(p);

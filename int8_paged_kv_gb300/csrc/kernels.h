@@ -36,6 +36,7 @@ struct DecodeArgs {
     const uint32_t *block_tables;
     const uint32_t *context_lens;
     int num_seqs;
+    int num_rows;          // query rows per sequence (causal: row b sees c - (rows - 1 - b) tokens)
     int num_heads;
     int num_kv_heads;
     int head_size;

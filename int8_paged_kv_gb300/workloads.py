@@ -32,7 +32,7 @@ UNUSED_BLOCK = 0xFFFFFFFF   # block_tables entry past the end of a sequence
 BASE_SEED = 20261202
 
 # generator streams (second element of the child seed)
-_S_Q, _S_K, _S_V, _S_APPEND, _S_KZERO, _S_VZERO = 1, 2, 3, 4, 5, 6
+_S_Q, _S_K, _S_V, _S_APPEND, _S_KZERO, _S_VZERO, _S_QROWS = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclass(frozen=True)
@@ -324,14 +324,25 @@ def empty_cache(w: Workload, fill: int = 0) -> np.ndarray:
     return np.full((w.num_blocks, cfg.num_kv_heads, cfg.block_size, W), fill, dtype=np.uint32)
 
 
-def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray) -> int:
+def query_rows(w: Workload, num_rows: int) -> np.ndarray:
+    """Seeded queries for a multi-row causal decode: f32 [S, num_rows, H, D]
+    ~ N(0, 1), the rows of the last num_rows positions of each sequence (as
+    when a batch of draft tokens is verified in one pass)."""
+    cfg = w.cfg
+    q = np.empty((cfg.num_seqs, int(num_rows), cfg.num_heads, cfg.head_size), dtype=np.float32)
+    _fill_normal(q, (cfg.seed, _S_QROWS, int(num_rows)), 1.0)
+    return q
+
+
+def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray, num_rows: int = 1) -> int:
     """Bytes a decode must move: every context token's K and V vector once
-    (head_size code bytes + a 4-byte scale word each), q in, out back, the
-    block-table entries walked and the context lengths."""
+    (head_size code bytes + a 4-byte scale word each), q in, out back (one
+    vector per query row and head), the block-table entries walked and the
+    context lengths."""
     c = np.minimum(context_lens.astype(np.int64), cfg.max_blocks_per_seq * cfg.block_size)
     S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
     kv = int(c.sum()) * Hk * 2 * (D + 4)
-    qo = 2 * S * H * D * 4
+    qo = 2 * S * int(num_rows) * H * D * 4
     bt = int((-(-c // B)).sum()) * 4
     return kv + qo + bt + S * 4
 

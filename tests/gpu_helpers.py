@@ -62,6 +62,62 @@ def oracle_decode(w, kc, vc, rows=None, q=None, bt=None, cl=None):
                          scale=w.scale, rows=rows)
 
 
+def random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0):
+    """A poisoned paged cache written by both writers (checked equal)."""
+    rng = np.random.default_rng(seed)
+    nblk = [-(-int(c) // B) for c in lens]
+    Nb = Nb or max(1, max(nblk))
+    pool = sum(nblk) + 3
+    perm = rng.permutation(pool).astype(np.uint32)
+    bt = np.full((S, Nb), 0xFFFFFFFF, dtype=np.uint32)
+    pos = 0
+    for s in range(S):
+        bt[s, :nblk[s]] = perm[pos:pos + nblk[s]]
+        pos += nblk[s]
+    T = int(sum(lens))
+    key = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
+    val = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
+    slots = np.concatenate([(bt[s, np.arange(c) // B].astype(np.int64) * B + np.arange(c) % B)
+                            for s, c in enumerate(lens) if c > 0] or [np.zeros(0, np.int64)]).astype(np.uint32)
+    W = D // 4 + 1
+    ok_ = np.full((pool, Hk, B, W), 0xFFFFFFFF, dtype=np.uint32)
+    ov_ = ok_.copy()
+    oracle.reshape_and_cache(key, val, ok_, ov_, slots, num_kv_heads=Hk, head_size=D, block_size=B)
+    kc, vc = dev_u32(ok_.copy()), dev_u32(ov_.copy())
+    kc.fill_(-1)
+    vc.fill_(-1)
+    if T:
+        pk.pa_q8_reshape_and_cache(torch.from_numpy(key.reshape(T, -1)).cuda(),
+                                   torch.from_numpy(val.reshape(T, -1)).cuda(), kc, vc,
+                                   dev_u32(slots), num_kv_heads=Hk, head_size=D, block_size=B)
+    assert np.array_equal(host_u32(kc), ok_) and np.array_equal(host_u32(vc), ov_)
+    q = rng.standard_normal((S, H, D)).astype(np.float32)
+    cfg = wl.Config("case", 99, S, H, Hk, D, B, Nb * B)
+    w = wl.Workload(cfg=cfg, context_lens=np.asarray(lens, dtype=np.uint32), block_tables=bt,
+                    num_blocks=pool, q=q, scale=float(np.float32(scale_mult / np.sqrt(D))),
+                    key=None, value=None, slot_mapping=slots, row_seq=None)
+    return w, ok_, ov_, kc, vc
+
+
+def gpu_decode_rows(w, kc, vc, q, *, kernel=0, partition_tokens=0, cl=None):
+    """pa_q8_decode_rows on device copies; q: f32 [S, R, H, D] numpy."""
+    qd = torch.from_numpy(q).cuda()
+    out = torch.full_like(qd, float("nan"))
+    pk.pa_q8_decode_rows(out, qd, kc, vc, dev_u32(w.block_tables),
+                         dev_u32(w.context_lens if cl is None else cl),
+                         num_kv_heads=w.cfg.num_kv_heads, block_size=w.cfg.block_size,
+                         scale=w.scale, num_blocks=w.num_blocks, kernel=kernel,
+                         partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def oracle_decode_rows(w, kc, vc, q, cl=None):
+    return oracle.decode_rows(q, kc, vc, w.block_tables, w.context_lens if cl is None else cl,
+                              num_kv_heads=w.cfg.num_kv_heads, block_size=w.cfg.block_size,
+                              scale=w.scale)
+
+
 def assert_close(got, want, what=""):
     """|got - want| <= 1e-5 + 1e-4 |want| elementwise (want from the oracle)."""
     got = np.asarray(got, dtype=np.float64)

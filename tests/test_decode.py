@@ -89,45 +89,9 @@ def test_partition_invariance(kernel, pt):
     assert_close(got, want, f"pt {pt}")
 
 
-def _random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0):
-    """A poisoned paged cache written by both writers (checked equal)."""
-    import torch
-    import int8_paged_kv_gb300 as pk
-    from tests.gpu_helpers import dev_u32, host_u32
-    import oracle
-    rng = np.random.default_rng(seed)
-    nblk = [-(-int(c) // B) for c in lens]
-    Nb = Nb or max(1, max(nblk))
-    pool = sum(nblk) + 3
-    perm = rng.permutation(pool).astype(np.uint32)
-    bt = np.full((S, Nb), 0xFFFFFFFF, dtype=np.uint32)
-    pos = 0
-    for s in range(S):
-        bt[s, :nblk[s]] = perm[pos:pos + nblk[s]]
-        pos += nblk[s]
-    T = int(sum(lens))
-    key = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
-    val = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
-    slots = np.concatenate([(bt[s, np.arange(c) // B].astype(np.int64) * B + np.arange(c) % B)
-                            for s, c in enumerate(lens) if c > 0] or [np.zeros(0, np.int64)]).astype(np.uint32)
-    W = D // 4 + 1
-    ok_ = np.full((pool, Hk, B, W), 0xFFFFFFFF, dtype=np.uint32)
-    ov_ = ok_.copy()
-    oracle.reshape_and_cache(key, val, ok_, ov_, slots, num_kv_heads=Hk, head_size=D, block_size=B)
-    kc, vc = dev_u32(ok_.copy()), dev_u32(ov_.copy())
-    kc.fill_(-1)
-    vc.fill_(-1)
-    if T:
-        pk.pa_q8_reshape_and_cache(torch.from_numpy(key.reshape(T, -1)).cuda(),
-                                   torch.from_numpy(val.reshape(T, -1)).cuda(), kc, vc,
-                                   dev_u32(slots), num_kv_heads=Hk, head_size=D, block_size=B)
-    assert np.array_equal(host_u32(kc), ok_) and np.array_equal(host_u32(vc), ov_)
-    q = rng.standard_normal((S, H, D)).astype(np.float32)
-    cfg = wl.Config("case", 99, S, H, Hk, D, B, Nb * B)
-    w = wl.Workload(cfg=cfg, context_lens=np.asarray(lens, dtype=np.uint32), block_tables=bt,
-                    num_blocks=pool, q=q, scale=float(np.float32(scale_mult / np.sqrt(D))),
-                    key=None, value=None, slot_mapping=slots, row_seq=None)
-    return w, ok_, ov_, kc, vc
+def _random_case(*args, **kw):
+    from tests.gpu_helpers import random_case
+    return random_case(*args, **kw)
 
 
 @pytest.mark.parametrize("kernel", [TC, CC])

@@ -1,0 +1,157 @@
+"""GPU multi-row causal decode (pa_q8_decode_rows) against the fp64 oracle
+(oracle.decode_rows: row b of R attends to the first c - (R-1-b) tokens,
+"attention.rs", attention_b), |gpu - oracle| <= 1e-5 + 1e-4 |oracle|
+elementwise, for both kernel families: row counts 1..16 (several head groups
+per kv head), GQA ratios and head sizes, forced partitions whose last one
+some rows see none of, contexts shorter than R (zero rows), clamped
+contexts, and the full-size large-batch workload on sampled rows.  R = 1 is
+pa_q8_decode bit for bit."""
+import numpy as np
+import pytest
+
+from int8_paged_kv_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TC, CC = 2, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int8_paged_kv_gb300 import build
+    build.build()
+    import oracle
+    oracle.build()
+
+
+_CACHE = {}
+
+
+def _setup(name):
+    if name in _CACHE:
+        return _CACHE[name]
+    from tests.gpu_helpers import dev_u32, oracle_write, poisoned_cache
+    w = wl.build(name, with_append=False)
+    ok_, ov_ = poisoned_cache(w), poisoned_cache(w)
+    oracle_write(w.key, w.value, w.slot_mapping, ok_, ov_, w.cfg)
+    w.key = w.value = None
+    _CACHE.clear()
+    _CACHE[name] = (w, ok_, ov_, dev_u32(ok_), dev_u32(ov_))
+    return _CACHE[name]
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+def test_one_row_is_single_query_decode_bitwise(kernel):
+    """R = 1 runs the single-query launch: identical bits."""
+    from tests.gpu_helpers import gpu_decode, gpu_decode_rows
+    w, ok_, ov_, kc, vc = _setup("llama8b")
+    for pt in (0, 512):
+        a = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+        b = gpu_decode_rows(w, kc, vc, w.q[:, None].copy(), kernel=kernel, partition_tokens=pt)
+        assert np.array_equal(a, b[:, 0]), f"pt {pt}"
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("name,R", [("tiny", 1), ("tiny", 3), ("tiny", 8), ("llama8b", 2),
+                                    ("llama8b", 5), ("edge", 3)])
+def test_workloads_all_rows(name, R, kernel):
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows, oracle_decode_rows
+    w, ok_, ov_, kc, vc = _setup(name)
+    q = wl.query_rows(w, R)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    got = gpu_decode_rows(w, kc, vc, q, kernel=kernel)
+    assert_close(got, want, f"{name} R {R} kernel {kernel}")
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+def test_forced_partitions_with_rows_that_see_none_of_the_last(kernel):
+    """Contexts 1 .. 3 tokens past a partition boundary: the lower rows see
+    nothing of the last partition, the combine must give those partials no
+    weight; contexts shorter than R give zero rows."""
+    from tests.gpu_helpers import assert_close, gpu_decode_rows, oracle_decode_rows
+    R, pt = 4, 256
+    lens = [257, 258, 259, 513, 512, 1, 2, 3, 4, 0, 1000, 777]
+    w, ok_, ov_, kc, vc = _random_case(len(lens), 8, 2, 128, 16, lens, seed=41)
+    q = np.random.default_rng(41).standard_normal((len(lens), R, 8, 128)).astype(np.float32)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    for p in (0, pt, 128):
+        got = gpu_decode_rows(w, kc, vc, q, kernel=kernel, partition_tokens=p)
+        assert_close(got, want, f"pt {p}")
+        # row b of a context c sees c - (3 - b) tokens: none -> exact zeros
+        for s, c in enumerate(lens):
+            for b in range(R):
+                if c - (R - 1 - b) <= 0:
+                    assert np.all(got[s, b] == 0.0), (s, b)
+
+
+def _random_case(*args, **kw):
+    from tests.gpu_helpers import random_case
+    return random_case(*args, **kw)
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("H,Hk,D,R", [(4, 4, 64, 16), (8, 4, 64, 7), (32, 1, 128, 2), (16, 2, 128, 4),
+                                      (16, 1, 256, 3), (8, 8, 256, 2), (24, 2, 64, 5)])
+def test_gqa_ratios_head_sizes_and_row_counts(kernel, H, Hk, D, R):
+    from tests.gpu_helpers import assert_close, gpu_decode_rows, oracle_decode_rows
+    lens = [1, 17, 300, 1000]
+    w, ok_, ov_, kc, vc = _random_case(4, H, Hk, D, 16, lens, seed=H * 7 + Hk + D + R)
+    q = np.random.default_rng(R).standard_normal((4, R, H, D)).astype(np.float32)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    for pt in (0, 256):
+        assert_close(gpu_decode_rows(w, kc, vc, q, kernel=kernel, partition_tokens=pt), want,
+                     f"H {H} Hk {Hk} D {D} R {R} pt {pt}")
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+def test_clamped_context(kernel):
+    from tests.gpu_helpers import assert_close, gpu_decode_rows, oracle_decode_rows
+    lens = [64, 208, 50]                                   # 208 = max_blocks_per_seq * 16
+    w, ok_, ov_, kc, vc = _random_case(3, 8, 2, 128, 16, lens, seed=6)
+    cl = np.array([64, 10_000, 50], dtype=np.uint32)       # seq 1 clamps to 208
+    q = np.random.default_rng(6).standard_normal((3, 6, 8, 128)).astype(np.float32)
+    want = oracle_decode_rows(w, ok_, ov_, q, cl=cl)
+    assert_close(gpu_decode_rows(w, kc, vc, q, kernel=kernel, cl=cl), want, "clamped")
+
+
+def _sampled_rows_oracle(w, ok_, ov_, q, picks):
+    """fp64 rows (s, b, h) one by one: the oracle's partial over the first
+    c - (R-1-b) tokens, normalised."""
+    import oracle
+    R = q.shape[1]
+    cap = w.cfg.max_blocks_per_seq * w.cfg.block_size
+    out = []
+    for s, b, h in picks:
+        t1 = max(0, min(int(w.context_lens[s]), cap) - (R - 1 - b))
+        if t1 == 0:
+            out.append(np.zeros(w.cfg.head_size))
+            continue
+        _, l, acc = oracle.decode_partial(np.ascontiguousarray(q[:, b]), ok_, ov_, w.block_tables,
+                                          num_kv_heads=w.cfg.num_kv_heads,
+                                          block_size=w.cfg.block_size, scale=w.scale, s=int(s),
+                                          h=int(h), t0=0, t1=t1)
+        out.append(acc / l)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("kernel", [0, TC, CC])
+def test_large_batch_four_rows_sampled(kernel):
+    """The large-batch workload with 4 query rows per sequence, in the
+    automatic launch plan; sampled (s, b, h) rows against the oracle."""
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows
+    w, ok_, ov_, kc, vc = _setup("large")
+    R = 4
+    q = wl.query_rows(w, R)
+    got = gpu_decode_rows(w, kc, vc, q, kernel=kernel)
+    rng = np.random.default_rng(kernel)
+    S, H = w.cfg.num_seqs, w.cfg.num_heads
+    picks = {(int(np.argmax(w.context_lens)), R - 1, 0), (int(np.argmin(w.context_lens)), 0, H - 1)}
+    while len(picks) < 96:
+        picks.add((int(rng.integers(S)), int(rng.integers(R)), int(rng.integers(H))))
+    picks = sorted(picks)
+    want = _sampled_rows_oracle(w, ok_, ov_, q, picks)
+    sel = np.array([got[s, b, h] for s, b, h in picks])
+    assert_close(sel, want, f"large R 4 kernel {kernel}")
+    assert np.all(np.isfinite(got))
+    assert device_status() == 0
