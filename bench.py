@@ -504,6 +504,57 @@ def run_ours(args) -> None:
 
 # ------------------------------------------------------- per-workload table
 
+def run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks) -> None:
+    """One decode step with one new token per sequence: the fused
+    pa_q8_decode_append against pa_q8_reshape_and_cache followed by
+    pa_q8_decode (same new tokens, same positions)."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    cfg = w.cfg
+    S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    dev = q.device
+    key, value = wl.new_token_rows(w, 1)
+    kd = torch.from_numpy(key.reshape(S, Hk * D)).to(dev)
+    vd = torch.from_numpy(value.reshape(S, Hk * D)).to(dev)
+    pos = np.minimum(w.context_lens.astype(np.int64), cfg.max_blocks_per_seq * B) - 1
+    slots = (w.block_tables[np.arange(S), pos // B].astype(np.int64) * B + pos % B).astype(np.uint32)
+    sm = torch.from_numpy(slots.view(np.int32)).to(dev)
+    q4 = q.reshape(S, 1, H, D)
+    out4 = torch.empty_like(q4)
+    ws = torch.empty(pk.pa_q8_decode_rows_workspace_size(S, 1, H, Hk, D, B, cfg.max_blocks_per_seq),
+                     dtype=torch.uint8, device=dev)
+    nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens) + wl.algorithmic_writer_bytes(Hk, D, slots)
+
+    def fused():
+        pk.pa_q8_decode_append(out4, q4, kd, vd, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B,
+                               scale=w.scale, workspace=ws)
+
+    def unfused():
+        pk.pa_q8_reshape_and_cache(kd, vd, kc, vc, sm, num_kv_heads=Hk, head_size=D, block_size=B)
+        pk.pa_q8_decode(out4.view(S, H, D), q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B,
+                        scale=w.scale, workspace=ws)
+    for label, run in (("fused append+decode", fused), ("writer then decode", unfused)):
+        for _ in range(max(3, args.warmup)):
+            torch.sum(flush, dim=0, out=sink)
+            run()
+        ts = []
+        for _ in range(args.steps):
+            torch.sum(flush, dim=0, out=sink)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = float(np.median(ts))
+        print(json.dumps({"kind": "decode step with append", "workload": name, "step": label,
+                          "new_tokens": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                          "gbps": round(nbytes / ms / 1e6, 1),
+                          "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1)}),
+              flush=True)
+
+
 def run_configs(args) -> None:
     """Decode throughput of every workload (both kernel families; 1 and 4
     query rows per sequence on the batches that fill the GPU), one JSON line
@@ -583,6 +634,8 @@ def run_configs(args) -> None:
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
                               "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
+        if name in ("llama8b", "large"):
+            run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks)
         del kc, vc, q, out
         torch.cuda.empty_cache()
 

@@ -211,6 +211,39 @@ int pa_q8_decode_rows(float *out, const float *q,
                       int64_t num_blocks, float scale, void *workspace,
                       size_t workspace_bytes, void *stream, const pa_q8_decode_options *opts);
 
+/*
+ * pa_q8_decode_append -- one decode step with the newest tokens' K/V
+ * appended inside the attention launch: reshape_and_cache_q8 of those rows
+ * followed by pa_q8_decode_rows, in that order (append, then attend), as one
+ * kernel launch after the ordering prep.
+ *
+ * context_lens[s] counts the new tokens: row b (0 <= b < num_rows) of the
+ * new K/V rows is position c - num_rows + b of sequence s, c = min(
+ * context_lens[s], max_blocks_per_seq * block_size); it is quantised exactly
+ * as pa_q8_reshape_and_cache does (same words, bit for bit) and stored at
+ * slot block_tables[s][p / block_size] * block_size + p % block_size.  Rows
+ * whose position is negative (c < num_rows) are not stored.  Query row b then
+ * attends to the first c - (num_rows - 1 - b) tokens, its own among them.
+ *
+ *   key, value      device f32 rows, row (s, b) at key + (s * num_rows + b) *
+ *                   key_stride holding num_kv_heads * head_size floats (kv head
+ *                   major); 16-byte aligned, strides multiples of 4 floats
+ *   key_cache,
+ *   value_cache     written (the new tokens' slots) and read
+ * Every other argument, the workspace (pa_q8_decode_rows_workspace_size) and
+ * the status codes are those of pa_q8_decode_rows.  A slot whose block id is
+ * >= num_blocks is neither written nor read, and flagged
+ * PA_Q8_DEV_BAD_BLOCK.
+ */
+int pa_q8_decode_append(float *out, const float *q, const float *key, const float *value,
+                        int64_t key_stride, int64_t value_stride,
+                        uint32_t *key_cache, uint32_t *value_cache,
+                        const uint32_t *block_tables, const uint32_t *context_lens,
+                        int num_seqs, int num_rows, int num_heads, int num_kv_heads,
+                        int head_size, int block_size, int max_blocks_per_seq,
+                        int64_t num_blocks, float scale, void *workspace,
+                        size_t workspace_bytes, void *stream, const pa_q8_decode_options *opts);
+
 size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads,
                                         int num_kv_heads, int head_size, int block_size,
                                         int max_blocks_per_seq, const pa_q8_decode_options *opts);

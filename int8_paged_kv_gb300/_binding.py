@@ -63,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.pa_q8_decode_rows.restype = i32
         L.pa_q8_decode_rows.argtypes = ([P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, f32,
                                          P, sz, P, ctypes.POINTER(DecodeOptions)])
+        L.pa_q8_decode_append.restype = i32
+        L.pa_q8_decode_append.argtypes = ([P, P, P, P, i64, i64, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           i32, i64, f32, P, sz, P, ctypes.POINTER(DecodeOptions)])
         L.pa_q8_decode_rows_workspace_size.restype = sz
         L.pa_q8_decode_rows_workspace_size.argtypes = [i32] * 7 + [ctypes.POINTER(DecodeOptions)]
         L.pa_q8_decode_workspace_size.restype = sz
@@ -237,6 +240,53 @@ def pa_q8_decode_rows(out, q, key_cache, value_cache, block_tables, context_lens
         int(block_size), Nb, nb, float(scale), ws_ptr, ws_bytes, _stream(stream),
         _opts(kernel, partition_tokens))
     _check("pa_q8_decode_rows", rc)
+    return out
+
+
+def _rows2d(t, n_rows, name):
+    """(tensor, row stride in floats) of new K/V rows given as [S, R, Hk, D]
+    / [S, R, Hk * D] (contiguous) or [S * R, Hk * D] (rows may be strided)."""
+    if t.dim() == 2:
+        if t.shape[0] != n_rows or t.stride(1) != 1:
+            raise ValueError(f"{name}: expected [num_seqs * num_rows, num_kv_heads * head_size] rows")
+        return t, int(t.stride(0))
+    if not t.is_contiguous() or t.shape[0] * t.shape[1] != n_rows:
+        raise ValueError(f"{name}: expected contiguous [num_seqs, num_rows, ...] rows")
+    return t, int(t[0].numel() // t.shape[1])
+
+
+def pa_q8_decode_append(out, q, key, value, key_cache, value_cache, block_tables, context_lens, *,
+                        num_kv_heads: int, block_size: int, scale: float,
+                        num_blocks: int | None = None, workspace=None, kernel: int = 0,
+                        partition_tokens: int = 0, stream=None):
+    """Append the newest num_rows tokens' K/V (rows of key / value) to the
+    caches and decode q [S, R, H, D] over them, in one attention launch (see
+    include/pa_q8.h).  Returns `out`."""
+    import torch
+    S, R, H, D = q.shape
+    if out.shape != q.shape or not out.is_contiguous() or not q.is_contiguous():
+        raise ValueError("q and out must be contiguous [num_seqs, num_rows, num_heads, head_size]")
+    Nb = int(block_tables.shape[1])
+    if block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("block_tables / context_lens do not match num_seqs")
+    k2, ks = _rows2d(key, S * R, "key")
+    v2, vs = _rows2d(value, S * R, "value")
+    nb = int(key_cache.shape[0]) if num_blocks is None else int(num_blocks)
+    need = pa_q8_decode_rows_workspace_size(S, R, H, num_kv_heads, D, block_size, Nb, kernel=kernel,
+                                            partition_tokens=partition_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_q8_decode_append(
+        _cuda(out, torch.float32, "out"), _cuda(q, torch.float32, "q"),
+        _cuda(k2, torch.float32, "key"), _cuda(v2, torch.float32, "value"), ks, vs,
+        _cuda(key_cache, torch.uint32, "key_cache"), _cuda(value_cache, torch.uint32, "value_cache"),
+        _cuda(block_tables, torch.uint32, "block_tables"),
+        _cuda(context_lens, torch.uint32, "context_lens"), S, R, H, int(num_kv_heads), D,
+        int(block_size), Nb, nb, float(scale), ws_ptr, ws_bytes, _stream(stream),
+        _opts(kernel, partition_tokens))
+    _check("pa_q8_decode_append", rc)
     return out
 
 

@@ -98,11 +98,19 @@ size_t workspace_impl(int num_seqs, int num_rows, int num_heads, int num_kv_head
     return pa_q8::plan_workspace_bytes(a);
 }
 
+// New K/V rows of the fused append (key == nullptr: plain decode).
+struct AppendRows {
+    const float *key = nullptr;
+    const float *value = nullptr;
+    int64_t key_stride = 0;
+    int64_t value_stride = 0;
+};
+
 int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
                 const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_rows,
                 int num_heads, int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
                 int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
-                const pa_q8_decode_options *opts) {
+                const pa_q8_decode_options *opts, const AppendRows &app = AppendRows{}) {
     int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
                                 num_rows);
     if (rc != PA_Q8_OK) return rc;
@@ -111,6 +119,12 @@ int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uin
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
         !aligned4(block_tables) || !aligned4(context_lens))
         return PA_Q8_EALIGN;
+    if (app.key) {
+        const int64_t row = (int64_t)num_kv_heads * head_size;
+        if (!app.value || app.key_stride < row || app.value_stride < row) return PA_Q8_EINVAL;
+        if (!aligned16(app.key) || !aligned16(app.value) || app.key_stride % 4 || app.value_stride % 4)
+            return PA_Q8_EALIGN;
+    }
     uint32_t *status = nullptr;
     int sms = 0;
     rc = device_info(&status, &sms);
@@ -134,6 +148,10 @@ int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uin
     a.num_blocks = num_blocks;
     a.scale = scale;
     a.status = status;
+    a.new_key = app.key;
+    a.new_value = app.value;
+    a.new_key_stride = app.key_stride;
+    a.new_value_stride = app.value_stride;
     if (pa_q8::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PA_Q8_ECUDA;
@@ -191,6 +209,24 @@ size_t pa_q8_decode_workspace_size_ex(int num_seqs, int num_heads, int num_kv_he
                                       int block_size, int max_blocks_per_seq,
                                       const pa_q8_decode_options *opts) {
     return workspace_impl(num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, opts);
+}
+
+int pa_q8_decode_append(float *out, const float *q, const float *key, const float *value,
+                        int64_t key_stride, int64_t value_stride, uint32_t *key_cache,
+                        uint32_t *value_cache, const uint32_t *block_tables, const uint32_t *context_lens,
+                        int num_seqs, int num_rows, int num_heads, int num_kv_heads, int head_size,
+                        int block_size, int max_blocks_per_seq, int64_t num_blocks, float scale,
+                        void *workspace, size_t workspace_bytes, void *stream,
+                        const pa_q8_decode_options *opts) {
+    AppendRows app;
+    app.key = key;
+    app.value = value;
+    app.key_stride = key_stride;
+    app.value_stride = value_stride;
+    if (!key) return PA_Q8_EINVAL;
+    return decode_impl(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs, num_rows,
+                       num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale,
+                       workspace, workspace_bytes, stream, opts, app);
 }
 
 size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads, int num_kv_heads,

@@ -56,6 +56,13 @@ constexpr int kVScaleBias = 131;           // weights carry 2^(131 - E): p * vs 
 #ifndef PA_Q8_TC_RING_256
 #define PA_Q8_TC_RING_256 2
 #endif
+// Virtual heads per tensor-core CTA for head sizes 64 / 128.  Each head tile
+// converts the chunk's codes itself, so a 16-head CTA does twice the work of
+// an 8-head one on one CTA per SM; two 8-head CTAs (three per SM) finish
+// sooner, their second K/V read mostly served by L2.
+#ifndef PA_Q8_TC_MAX_HEADS
+#define PA_Q8_TC_MAX_HEADS 8
+#endif
 #ifndef PA_Q8_TC_MINB_128
 #define PA_Q8_TC_MINB_128 3                // CTAs per SM the register budget targets
 #endif
@@ -85,6 +92,12 @@ struct Params {
     float *pml;             // [S][R][H][NP][2]
     float *pacc;            // [S][R][H][NP][D]
     uint32_t *status;
+    // fused append of the newest R tokens (nk == nullptr: none)
+    const float *nk;
+    const float *nv;
+    int64_t nk_stride, nv_stride;
+    uint32_t *kc_w;         // the caches, written by the append
+    uint32_t *vc_w;
 };
 
 // Which CTA this is and the token range it owns.  The CTA serves virtual
@@ -135,6 +148,56 @@ __device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) 
 __device__ __forceinline__ int row_len(const Params &P, const Work &w, int vh) {
     const int cb = w.c - (P.R - 1 - vh / P.r);
     return max(0, min(cb - w.t_begin, P.PT));
+}
+
+// Fused append: quantise the sequence's newest R tokens (positions c-R ..
+// c-1 of the clamped context; row b of the new K/V rows is position c-R+b)
+// that fall in this CTA's partition, for its kv head, and store their K and V
+// token vectors in the cache -- the writer's arithmetic, one warp per vector.
+// Every CTA whose tiles hold such a token stores it, all with the same bits,
+// so a tile copy observes the token's words whichever store it sees; the
+// caller's CTA barrier (after the proxy fence here) orders the stores before
+// this CTA's bulk copies.
+template <int D>
+__device__ void append_tokens(const Params &P, const Work &w) {
+    constexpr int WORDS = D / 4;
+    constexpr int NW = (WORDS + 31) / 32;          // words per lane (head size 64: lanes 0..15)
+    const int first = w.c - P.R;                    // position of new row 0 (may be < 0)
+    const int t_lo = max(first, w.t_begin), t_hi = min(w.c, w.t_begin + P.PT);
+    const int nvec = 2 * max(0, t_hi - t_lo);       // (token, K or V) vectors
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int v = warp; v < nvec; v += (int)(blockDim.x >> 5)) {
+        const int t = t_lo + (v >> 1);
+        const bool is_v = v & 1;
+        const int64_t row = (int64_t)w.s * P.R + (t - first);
+        const float4 *src = reinterpret_cast<const float4 *>(
+            (is_v ? P.nv + row * P.nv_stride : P.nk + row * P.nk_stride) + (int64_t)w.g * D);
+        float4 x[NW];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const int wd = lane + 32 * i;
+            x[i] = wd < WORDS ? __ldg(src + wd) : make_float4(0.f, 0.f, 0.f, 0.f);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
+        const float scale = m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f;
+        const uint32_t pb = __ldg(P.bt + (int64_t)w.s * P.Nb + (t >> P.log2B));
+        if ((int64_t)pb >= P.num_blocks) {         // warp-uniform; the table walk flags it
+            continue;
+        }
+        uint32_t *dst = (is_v ? P.vc_w : P.kc_w) +
+                        (((int64_t)pb * P.Hk + w.g) * P.B + (t & (P.B - 1))) * (WORDS + 1);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const int wd = lane + 32 * i;
+            if (wd < WORDS) dst[wd] = pack_word(x[i], inv);
+        }
+        if (lane == 0) dst[WORDS] = __float_as_uint(scale);
+    }
+    fence_proxy_async_global();
 }
 
 // Zero output rows of a sequence whose context is empty (partition 0 only).
@@ -432,6 +495,7 @@ decode_tc_kernel(Params P) {
         for (int k = 0; k < RING; ++k) mbar_init(bars + 8 * k, 1);
         fence_mbar_init();
     }
+    if (P.nk) append_tokens<D>(P, w);
     load_table(P, w, const_cast<uint32_t *>(table));
     __syncthreads();
 
@@ -690,6 +754,7 @@ decode_cc_kernel(Params P) {
         for (int k = 0; k < RING; ++k) mbar_init(bars + 8 * k, 1);
         fence_mbar_init();
     }
+    if (P.nk) append_tokens<D>(P, w);
     load_table(P, w, const_cast<uint32_t *>(table));
     for (int i = threadIdx.x; i < NH * D; i += blockDim.x) {
         const int hh = i / D;
@@ -916,6 +981,10 @@ Params make_params(const DecodeArgs &a) {
     P.rv = P.R * P.r;
     P.heads_per_cta = a.heads_per_cta; P.head_groups = a.head_groups;
     P.order = a.order; P.counters = a.counters; P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
+    P.nk = a.new_key; P.nv = a.new_value;
+    P.nk_stride = a.new_key_stride; P.nv_stride = a.new_value_stride;
+    P.kc_w = const_cast<uint32_t *>(a.key_cache);      // written only by the fused append
+    P.vc_w = const_cast<uint32_t *>(a.value_cache);
     return P;
 }
 
@@ -945,9 +1014,11 @@ template <int D>
 cudaError_t launch_tc(const Params &P, cudaStream_t st) {
     constexpr int SLOTS = PA_Q8_TC_SLOTS;
     constexpr int RING = tc_ring<D>();
-    if (P.heads_per_cta > 8) {
-        const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc_extra_bytes<D, 2>());
-        return launch_attn(decode_tc_kernel<D, 2>, P, L.total, 2 * SLOTS * 32, st);
+    if constexpr (D == 256) {       // 16-head CTAs: head size 256 only (make_plan)
+        if (P.heads_per_cta > 8) {
+            const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc_extra_bytes<D, 2>());
+            return launch_attn(decode_tc_kernel<D, 2>, P, L.total, 2 * SLOTS * 32, st);
+        }
     }
     const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc_extra_bytes<D, 1>());
     return launch_attn(decode_tc_kernel<D, 1>, P, L.total, SLOTS * 32, st);
@@ -998,7 +1069,8 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     const int r = a.num_rows * (a.num_heads / a.num_kv_heads);
     a.kernel = requested_kernel == kAuto ? kTensorCore : requested_kernel;
     if (a.kernel == kTensorCore) {
-        a.heads_per_cta = r < 16 ? r : 16;
+        const int cap = a.head_size == 256 ? 16 : PA_Q8_TC_MAX_HEADS;
+        a.heads_per_cta = r < cap ? r : cap;
     } else {
         int hp = 16;
         while (hp > 1 && (r % hp) != 0) hp >>= 1;

@@ -93,6 +93,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic stores to global memory before bulk copies
+// (async proxy) that a CTA barrier later lets another thread issue.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -152,6 +158,28 @@ __device__ __forceinline__ uint32_t prmt_i(uint32_t a, uint32_t b) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
     return d;
 }
+
+// ----------------------------------------------- int8 token-vector encoding
+
+// Code of x: round(x * inv) with halves away from zero, clamped to
+// [-127, 127].  For |t| < 2^23, adding 0.5 to |t| rounded toward zero and
+// truncating gives floor(|t| + 0.5) exactly (every integer below 2^24 is an
+// f32, so rounding down never skips one).  The f32 -> s32 conversion
+// saturates: NaN (0 * inf, when 127/amax overflowed) becomes 0 and +inf
+// becomes INT_MAX, clamped to 127 next.
+__device__ __forceinline__ int quantise_code(float x, float inv) {
+    const float t = __fmul_rn(x, inv);
+    const int a = min(__float2int_rz(__fadd_rz(fabsf(t), 0.5f)), 127);
+    return t < 0.0f ? -a : a;
+}
+
+// Four codes into one word, code l in byte l.
+__device__ __forceinline__ uint32_t pack_word(float4 x, float inv) {
+    const uint32_t c0 = (uint32_t)quantise_code(x.x, inv), c1 = (uint32_t)quantise_code(x.y, inv);
+    const uint32_t c2 = (uint32_t)quantise_code(x.z, inv), c3 = (uint32_t)quantise_code(x.w, inv);
+    return prmt_i<0x5410u>(prmt_i<0x0040u>(c0, c1), prmt_i<0x0040u>(c2, c3));
+}
+
 
 // (a & MASK) ^ c in one LOP3, MASK an immediate
 template <uint32_t MASK>

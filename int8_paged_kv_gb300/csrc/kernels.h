@@ -59,6 +59,13 @@ struct DecodeArgs {
     float *partial_ml;
     float *partial_acc;
     uint32_t *status;
+    // fused append (new_key == nullptr: none): rows [num_seqs][num_rows] of
+    // num_kv_heads * head_size floats, row (s, b) at new_key + (s * num_rows +
+    // b) * new_key_stride; the token of row b is position c - num_rows + b
+    const float *new_key;
+    const float *new_value;
+    int64_t new_key_stride;
+    int64_t new_value_stride;
 };
 
 struct DecodePlanLimits {

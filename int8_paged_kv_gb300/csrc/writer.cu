@@ -23,25 +23,6 @@ namespace {
 
 constexpr int kWriterWarps = 8;
 
-// Code of x: round(x * inv) with halves away from zero, clamped to
-// [-127, 127].  For |t| < 2^23, adding 0.5 to |t| rounded toward zero and
-// truncating gives floor(|t| + 0.5) exactly (every integer below 2^24 is an
-// f32, so rounding down never skips one).  The f32 -> s32 conversion
-// saturates: NaN (0 * inf, when 127/amax overflowed) becomes 0 and +inf
-// becomes INT_MAX, clamped to 127 next.
-__device__ __forceinline__ int quantise_code(float x, float inv) {
-    const float t = __fmul_rn(x, inv);
-    const int a = min(__float2int_rz(__fadd_rz(fabsf(t), 0.5f)), 127);
-    return t < 0.0f ? -a : a;
-}
-
-// Four codes into one word, code l in byte l.
-__device__ __forceinline__ uint32_t pack_word(float4 x, float inv) {
-    const uint32_t c0 = (uint32_t)quantise_code(x.x, inv), c1 = (uint32_t)quantise_code(x.y, inv);
-    const uint32_t c2 = (uint32_t)quantise_code(x.z, inv), c3 = (uint32_t)quantise_code(x.w, inv);
-    return prmt_i<0x5410u>(prmt_i<0x0040u>(c0, c1), prmt_i<0x0040u>(c2, c3));
-}
-
 template <bool kVec>
 __device__ __forceinline__ float4 load4(const float *p) {
     if constexpr (kVec) {

@@ -32,7 +32,7 @@ UNUSED_BLOCK = 0xFFFFFFFF   # block_tables entry past the end of a sequence
 BASE_SEED = 20261202
 
 # generator streams (second element of the child seed)
-_S_Q, _S_K, _S_V, _S_APPEND, _S_KZERO, _S_VZERO, _S_QROWS = 1, 2, 3, 4, 5, 6, 7
+_S_Q, _S_K, _S_V, _S_APPEND, _S_KZERO, _S_VZERO, _S_QROWS, _S_NEWKV = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @dataclass(frozen=True)
@@ -332,6 +332,18 @@ def query_rows(w: Workload, num_rows: int) -> np.ndarray:
     q = np.empty((cfg.num_seqs, int(num_rows), cfg.num_heads, cfg.head_size), dtype=np.float32)
     _fill_normal(q, (cfg.seed, _S_QROWS, int(num_rows)), 1.0)
     return q
+
+
+def new_token_rows(w: Workload, num_rows: int) -> tuple[np.ndarray, np.ndarray]:
+    """Seeded K and V rows of the newest num_rows tokens of each sequence, as
+    a decode step appends them: f32 [S, num_rows, Hk, D] each, ~N(0, 1)."""
+    cfg = w.cfg
+    shape = (cfg.num_seqs, int(num_rows), cfg.num_kv_heads, cfg.head_size)
+    key = np.empty(shape, dtype=np.float32)
+    value = np.empty(shape, dtype=np.float32)
+    _fill_normal(key, (cfg.seed, _S_NEWKV, int(num_rows), 0), 1.0)
+    _fill_normal(value, (cfg.seed, _S_NEWKV, int(num_rows), 1), 1.0)
+    return key, value
 
 
 def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray, num_rows: int = 1) -> int:
