@@ -56,6 +56,8 @@ def _load():
         lib.oracle_combine.argtypes = [P, P, P, i32, i32, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i64]
         lib.oracle_decode_rows.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64]
+        lib.oracle_reshape_and_cache_f32.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32]
+        lib.oracle_decode_f32.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i64]
         _lib = lib
         return lib
 
@@ -180,4 +182,61 @@ def combine(m: np.ndarray, l: np.ndarray, acc: np.ndarray) -> np.ndarray:
     n, D = acc.shape
     out = np.empty(D, dtype=np.float64)
     _load().oracle_combine(_ptr(m), _ptr(l), _ptr(acc), n, D, _ptr(out))
+    return out
+
+
+# ----------------------------------------------------------------- f32 cache
+# The f32 variant of the cache: [num_blocks, num_kv_heads, block_size,
+# head_size] f32 (the q8 layout with f32 elements and no scale word).
+
+
+def reshape_and_cache_f32(key: np.ndarray, value: np.ndarray, key_cache: np.ndarray,
+                          value_cache: np.ndarray, slot_mapping: np.ndarray, *,
+                          num_kv_heads: int, head_size: int, block_size: int) -> None:
+    """Copy rows into the f32 caches in place (PAD slots skipped).  key/value:
+    f32 [T, Hk, D] or a 2-D view of rows with contiguous elements."""
+    T = int(slot_mapping.shape[0])
+    _need(slot_mapping, np.uint32, "slot_mapping")
+    _need(key_cache, np.float32, "key_cache")
+    _need(value_cache, np.float32, "value_cache")
+
+    def base_and_stride(a):
+        if a.dtype != np.float32:
+            raise TypeError("key/value must be float32")
+        if a.flags.c_contiguous:
+            return a, num_kv_heads * head_size
+        if a.ndim != 2 or a.strides[1] != 4:
+            raise ValueError("strided key/value must be 2-D views with contiguous rows")
+        return a, a.strides[0] // 4
+
+    k, ks = base_and_stride(key)
+    v, vs = base_and_stride(value)
+    _load().oracle_reshape_and_cache_f32(
+        ctypes.c_void_p(k.ctypes.data), ctypes.c_void_p(v.ctypes.data),
+        _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), T, ks, vs,
+        num_kv_heads, head_size, block_size)
+
+
+def decode_f32(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+               block_tables: np.ndarray, context_lens: np.ndarray, *, num_kv_heads: int,
+               block_size: int, scale: float, rows: np.ndarray | None = None) -> np.ndarray:
+    """fp64 decode over the f32 caches.  Returns [S, H, D] (rows=None) or
+    [n_rows, D] for the given int32 (s, h) pairs."""
+    _need(q, np.float32, "q")
+    _need(key_cache, np.float32, "key_cache")
+    _need(value_cache, np.float32, "value_cache")
+    _need(block_tables, np.uint32, "block_tables")
+    _need(context_lens, np.uint32, "context_lens")
+    S, H, D = q.shape
+    Nb = block_tables.shape[1]
+    if rows is None:
+        out = np.empty((S, H, D), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((rows.shape[0], D), dtype=np.float64)
+        rp, nr = _ptr(rows), rows.shape[0]
+    _load().oracle_decode_f32(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
+                              _ptr(block_tables), _ptr(context_lens), S, H, num_kv_heads, D,
+                              block_size, Nb, float(scale), rp, nr)
     return out

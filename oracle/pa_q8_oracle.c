@@ -27,6 +27,10 @@
  *    merge of (max, sum, weighted sum) partials by their log-sum-exp is
  *    written out in oracle_combine below.
  *
+ *  - the f32 cache variant (paged_attn.comp, named by paged_attn_q8.comp's
+ *    header comment as the same math over an f32 cache): a copy writer and
+ *    the same fp64 decode over f32 values (end of this file).
+ *
  * Arithmetic.  The writer is bit-exact by construction: every f32 operation
  * of the shader (one division, one product, one division for the scale) is
  * done in double and rounded once to float.  For +, -, *, / of two floats
@@ -283,5 +287,90 @@ void oracle_decode_rows(double *out, const float *q, const uint32_t *key_cache,
                max_blocks_per_seq, scale, s, g, 0, t1 > 0 ? t1 : 0, &m, &l, o);
         if (t1 <= 0) continue;          /* zeros */
         for (int d = 0; d < head_size; ++d) o[d] /= l;
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * The f32 cache variant.  paged_attn_q8.comp's header comment describes the
+ * q8 shader as the same math and workgroup structure as paged_attn.comp,
+ * which reads an f32 cache ("1 byte/elem vs the f32 cache's 4"), and
+ * reshape_and_cache_q8.comp says its slot rule mirrors the f32 writer.
+ * Neither f32 shader is on the pages; the reading taken here is the q8
+ * layout with f32 elements and no scale word:
+ * [num_blocks, num_kv_heads, block_size, head_size] f32.  The writer copies
+ * each (token, kv head) vector to its slot (PAD slots skipped); the decode
+ * is the same fp64 softmax as oracle_decode over those values.
+ * ------------------------------------------------------------------------ */
+
+void oracle_reshape_and_cache_f32(const float *key, const float *value,
+                                  float *key_cache, float *value_cache,
+                                  const uint32_t *slot_mapping, int64_t num_tokens,
+                                  int64_t key_stride, int64_t value_stride,
+                                  int num_kv_heads, int head_size, int block_size)
+{
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        uint32_t slot = slot_mapping[i];
+        if (slot == PAD_SLOT) continue;
+        int64_t block = (int64_t)(slot / (uint32_t)block_size);
+        int64_t off = (int64_t)(slot % (uint32_t)block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_size;
+            memcpy(key_cache + dst, key + i * key_stride + (int64_t)h * head_size,
+                   sizeof(float) * (size_t)head_size);
+            memcpy(value_cache + dst, value + i * value_stride + (int64_t)h * head_size,
+                   sizeof(float) * (size_t)head_size);
+        }
+    }
+}
+
+/* The f32 vector of logical token t of sequence s, kv head g. */
+static const float *f32_token(const float *cache, const uint32_t *block_tables,
+                              int max_blocks_per_seq, int num_kv_heads, int head_size,
+                              int block_size, int s, int g, int64_t t)
+{
+    uint32_t block = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+    int64_t off = t % block_size;
+    return cache + (((int64_t)block * num_kv_heads + g) * block_size + off) * head_size;
+}
+
+/* out[s, h, :] = softmax(scale * q[s,h] . K^T) V over the clamped context of
+ * sequence s, K and V read from the f32 caches; rows as in oracle_decode. */
+void oracle_decode_f32(double *out, const float *q, const float *key_cache,
+                       const float *value_cache, const uint32_t *block_tables,
+                       const uint32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                       int head_size, int block_size, int max_blocks_per_seq, double scale,
+                       const int32_t *rows, int64_t n_rows)
+{
+    int64_t n = rows ? n_rows : (int64_t)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        int s = rows ? rows[2 * i] : (int)(i / num_heads);
+        int h = rows ? rows[2 * i + 1] : (int)(i % num_heads);
+        int g = h / (num_heads / num_kv_heads);
+        const float *qv = q + ((int64_t)s * num_heads + h) * head_size;
+        double *o = out + i * head_size;
+        for (int d = 0; d < head_size; ++d) o[d] = 0.0;
+        int64_t c = clamped_len(context_lens, s, max_blocks_per_seq, block_size);
+        if (c == 0) continue;           /* all zeros */
+        double *z = (double *)malloc(sizeof(double) * (size_t)c);
+        double m = -INFINITY;
+        for (int64_t t = 0; t < c; ++t) {
+            const float *k = f32_token(key_cache, block_tables, max_blocks_per_seq, num_kv_heads,
+                                       head_size, block_size, s, g, t);
+            double dot = 0.0;
+            for (int d = 0; d < head_size; ++d) dot += (double)qv[d] * (double)k[d];
+            z[t] = scale * dot;
+            if (z[t] > m) m = z[t];
+        }
+        double l = 0.0;
+        for (int64_t t = 0; t < c; ++t) {
+            double p = exp(z[t] - m);
+            l += p;
+            const float *v = f32_token(value_cache, block_tables, max_blocks_per_seq, num_kv_heads,
+                                       head_size, block_size, s, g, t);
+            for (int d = 0; d < head_size; ++d) o[d] += p * (double)v[d];
+        }
+        for (int d = 0; d < head_size; ++d) o[d] /= l;
+        free(z);
     }
 }
