@@ -555,6 +555,51 @@ def run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks) -> No
               flush=True)
 
 
+def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
+    """The same decode over an f32 cache (pa_f32_decode): 4 * head_size bytes
+    per token vector instead of head_size + 4."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    cfg = w.cfg
+    S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    dev = q.device
+    kc = torch.empty((w.num_blocks, Hk, B, D), dtype=torch.float32, device=dev)
+    vc = torch.empty_like(kc)
+    T = w.key.shape[0]
+    for i in range(0, T, 1 << 18):
+        sm = torch.from_numpy(np.ascontiguousarray(w.slot_mapping[i:i + (1 << 18)]).view(np.int32)).to(dev)
+        pk.pa_f32_reshape_and_cache(torch.from_numpy(w.key[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                    torch.from_numpy(w.value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                    kc, vc, sm, num_kv_heads=Hk, head_size=D, block_size=B)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(1, pk.pa_f32_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq)),
+                     dtype=torch.uint8, device=dev)
+
+    def run():
+        pk.pa_f32_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale, workspace=ws)
+    for _ in range(max(3, args.warmup)):
+        torch.sum(flush, dim=0, out=sink)
+        run()
+    ts = []
+    for _ in range(args.steps):
+        torch.sum(flush, dim=0, out=sink)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = float(np.median(ts))
+    nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="f32")
+    print(json.dumps({"kind": "decode per workload, f32 cache", "workload": name, "kernel": "f32 cuda-core",
+                      "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
+                      "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                      "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
+    del kc, vc
+    torch.cuda.empty_cache()
+
+
 def run_configs(args) -> None:
     """Decode throughput of every workload (both kernel families; 1 and 4
     query rows per sequence on the batches that fill the GPU), one JSON line
@@ -587,9 +632,11 @@ def run_configs(args) -> None:
                                        torch.from_numpy(w.value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
                                        kc, vc, u32(w.slot_mapping[i:i + (1 << 18)]), num_kv_heads=Hk,
                                        head_size=D, block_size=B)
-        w.key = w.value = None
         q = torch.from_numpy(w.q).to(dev)
         bt, cl, out = u32(w.block_tables), u32(w.context_lens), torch.empty_like(q)
+        if name in ("llama8b", "long", "large"):
+            run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks)
+        w.key = w.value = None
         # R > 1: causal decode of R query rows per sequence (pa_q8_decode_rows),
         # on the workloads whose batches fill the GPU
         row_counts = (1, 4) if name in ("llama8b", "long", "large") else (1,)

@@ -248,6 +248,46 @@ size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_head
                                         int num_kv_heads, int head_size, int block_size,
                                         int max_blocks_per_seq, const pa_q8_decode_options *opts);
 
+/*
+ * ---- The f32 cache variant ------------------------------------------------
+ * "paged_attn_q8.comp" (header comment) describes itself as the math of
+ * "paged_attn.comp" over an int8 cache instead of an f32 one ("1 byte/elem
+ * vs the f32 cache's 4"), and "reshape_and_cache_q8.comp" says its slot rule
+ * mirrors the f32 writer.  Neither f32 shader is on the pages; the layout
+ * read here is the q8 one with f32 elements and no scale word:
+ *   f32 [num_blocks][num_kv_heads][block_size][head_size].
+ * Same arguments, statuses, device flags and result semantics as the q8
+ * calls; block_size a power of two (>= 8 for the decode, whose tiles move as
+ * 2-D tensor copies), num_blocks * num_kv_heads * block_size < 2^31.
+ */
+
+/* Copy each (token, kv head) K and V vector to its slot of the f32 caches;
+ * slot 0xFFFFFFFF skips the row, slots >= num_blocks * block_size are skipped
+ * and flagged PA_Q8_DEV_BAD_SLOT.  Rows as in pa_q8_reshape_and_cache (any
+ * 4-byte alignment; 16-byte aligned rows and caches take 16-byte moves). */
+int pa_f32_reshape_and_cache(const float *key, const float *value,
+                             float *key_cache, float *value_cache,
+                             const uint32_t *slot_mapping, int64_t num_tokens,
+                             int64_t key_stride, int64_t value_stride,
+                             int num_kv_heads, int head_size, int block_size,
+                             int64_t num_blocks, void *stream);
+
+/* pa_q8_decode over the f32 caches (16-byte aligned), output = softmax(scale
+ * * q . K^T) . V per (seq, head) with the same GQA map, clamp, empty-context
+ * rule and split-context combine.  opts may set partition_tokens; its kernel
+ * must be PA_Q8_KERNEL_AUTO (the f32 cache has one kernel family). */
+int pa_f32_decode(float *out, const float *q,
+                  const float *key_cache, const float *value_cache,
+                  const uint32_t *block_tables, const uint32_t *context_lens,
+                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                  int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                  float scale, void *workspace, size_t workspace_bytes, void *stream,
+                  const pa_q8_decode_options *opts);
+
+size_t pa_f32_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                    int head_size, int block_size, int max_blocks_per_seq,
+                                    const pa_q8_decode_options *opts);
+
 /* The launch plan pa_q8_decode_ex would use (no launch): kernel family,
  * tokens per partition, partitions per sequence (grid x), CTAs launched for
  * the attention kernel.  Any output pointer may be NULL.  Needs a current

@@ -64,12 +64,26 @@ int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_s
     return PA_Q8_OK;
 }
 
-int plan_for(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int num_sms) {
-    const int kernel = opts ? opts->kernel : PA_Q8_KERNEL_AUTO;
+// f32: the f32-cache decode, whose only kernel family is its own (opts->kernel
+// must be automatic).
+int plan_for(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int num_sms, bool f32 = false) {
+    int kernel = opts ? opts->kernel : PA_Q8_KERNEL_AUTO;
     const int pt = opts ? opts->partition_tokens : 0;
     if (kernel < PA_Q8_KERNEL_AUTO || kernel > PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
+    if (f32) {
+        if (kernel != PA_Q8_KERNEL_AUTO) return PA_Q8_EINVAL;
+        kernel = pa_q8::kF32;
+    }
     if (pt < 0 || (pt > 0 && pt % 128 != 0)) return PA_Q8_EINVAL;
     if (!pa_q8::make_plan(a, kernel, pt, num_sms)) return PA_Q8_EUNSUPPORTED;
+    return PA_Q8_OK;
+}
+
+// Extra limits of the f32-cache decode: tensor copies of min(B, 32)-row
+// boxes 1024-byte aligned in shared memory (B >= 8), row coordinates in s32.
+int check_f32_shape(int num_kv_heads, int block_size, int64_t num_blocks) {
+    if (block_size < 8) return PA_Q8_EUNSUPPORTED;
+    if (num_blocks > 0 && num_blocks * num_kv_heads * block_size > (int64_t)0x7FFFFFFF) return PA_Q8_EUNSUPPORTED;
     return PA_Q8_OK;
 }
 
@@ -86,15 +100,17 @@ void fill_shape(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_he
 }
 
 size_t workspace_impl(int num_seqs, int num_rows, int num_heads, int num_kv_heads, int head_size,
-                      int block_size, int max_blocks_per_seq, const pa_q8_decode_options *opts) {
+                      int block_size, int max_blocks_per_seq, const pa_q8_decode_options *opts,
+                      bool f32 = false) {
     if (check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
                            num_rows) != PA_Q8_OK)
         return 0;
+    if (f32 && check_f32_shape(num_kv_heads, block_size, 0) != PA_Q8_OK) return 0;
     pa_q8::DecodeArgs a;
     fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_rows);
     int sms = 0;
     if (device_info(nullptr, &sms) != PA_Q8_OK) sms = 152;     // size query without a device
-    if (plan_for(a, opts, sms) != PA_Q8_OK) return 0;
+    if (plan_for(a, opts, sms, f32) != PA_Q8_OK) return 0;
     return pa_q8::plan_workspace_bytes(a);
 }
 
@@ -110,11 +126,13 @@ int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uin
                 const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_rows,
                 int num_heads, int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq,
                 int64_t num_blocks, float scale, void *workspace, size_t workspace_bytes, void *stream,
-                const pa_q8_decode_options *opts, const AppendRows &app = AppendRows{}) {
+                const pa_q8_decode_options *opts, const AppendRows &app = AppendRows{},
+                bool f32 = false) {
     int rc = check_decode_shape(num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq,
                                 num_rows);
     if (rc != PA_Q8_OK) return rc;
     if (num_blocks <= 0) return PA_Q8_EINVAL;
+    if (f32 && (rc = check_f32_shape(num_kv_heads, block_size, num_blocks)) != PA_Q8_OK) return rc;
     if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens) return PA_Q8_EINVAL;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) ||
         !aligned4(block_tables) || !aligned4(context_lens))
@@ -131,7 +149,7 @@ int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uin
     if (rc != PA_Q8_OK) return rc;
     pa_q8::DecodeArgs a;
     fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_rows);
-    rc = plan_for(a, opts, sms);
+    rc = plan_for(a, opts, sms, f32);
     if (rc != PA_Q8_OK) return rc;
     const size_t need = pa_q8::plan_workspace_bytes(a);
     if (need > 0) {
@@ -227,6 +245,52 @@ int pa_q8_decode_append(float *out, const float *q, const float *key, const floa
     return decode_impl(out, q, key_cache, value_cache, block_tables, context_lens, num_seqs, num_rows,
                        num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale,
                        workspace, workspace_bytes, stream, opts, app);
+}
+
+int pa_f32_reshape_and_cache(const float *key, const float *value, float *key_cache, float *value_cache,
+                             const uint32_t *slot_mapping, int64_t num_tokens, int64_t key_stride,
+                             int64_t value_stride, int num_kv_heads, int head_size, int block_size,
+                             int64_t num_blocks, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_Q8_EINVAL;
+    if (head_size % 4 != 0) return PA_Q8_EINVAL;
+    if (!head_size_ok(head_size) || !pow2(block_size) || block_size > 1024) return PA_Q8_EUNSUPPORTED;
+    if (key_stride < (int64_t)num_kv_heads * head_size || value_stride < (int64_t)num_kv_heads * head_size)
+        return PA_Q8_EINVAL;
+    if (num_blocks * block_size > (int64_t)0xFFFFFFFFu || num_kv_heads > 65535) return PA_Q8_EUNSUPPORTED;
+    if (num_tokens == 0) return PA_Q8_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_Q8_EINVAL;
+    if (!aligned4(key) || !aligned4(value) || !aligned4(key_cache) || !aligned4(value_cache) ||
+        !aligned4(slot_mapping))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int rc = device_info(&status, nullptr);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::WriterArgs a{key, value, reinterpret_cast<uint32_t *>(key_cache),
+                        reinterpret_cast<uint32_t *>(value_cache), slot_mapping, num_tokens, key_stride,
+                        value_stride, num_kv_heads, head_size, block_size, num_blocks, status};
+    if (pa_q8::launch_writer_f32(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
+int pa_f32_decode(float *out, const float *q, const float *key_cache, const float *value_cache,
+                  const uint32_t *block_tables, const uint32_t *context_lens, int num_seqs, int num_heads,
+                  int num_kv_heads, int head_size, int block_size, int max_blocks_per_seq, int64_t num_blocks,
+                  float scale, void *workspace, size_t workspace_bytes, void *stream,
+                  const pa_q8_decode_options *opts) {
+    return decode_impl(out, q, reinterpret_cast<const uint32_t *>(key_cache),
+                       reinterpret_cast<const uint32_t *>(value_cache), block_tables, context_lens, num_seqs, 1,
+                       num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, num_blocks, scale,
+                       workspace, workspace_bytes, stream, opts, AppendRows{}, true);
+}
+
+size_t pa_f32_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                    int block_size, int max_blocks_per_seq, const pa_q8_decode_options *opts) {
+    return workspace_impl(num_seqs, 1, num_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq, opts,
+                          true);
 }
 
 size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads, int num_kv_heads,

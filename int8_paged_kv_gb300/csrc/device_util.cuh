@@ -93,6 +93,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 2-D tensor copy (TMA) of one box of the tensor map `tmap` (a
+// __grid_constant__ kernel parameter) at element coordinates (x, y) into
+// shared memory at `dst`, completing `bar`'s transaction count.  x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Order this thread's generic stores to global memory before bulk copies
 // (async proxy) that a CTA barrier later lets another thread issue.
 __device__ __forceinline__ void fence_proxy_async_global() {

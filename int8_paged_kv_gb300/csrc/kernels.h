@@ -25,8 +25,11 @@ struct WriterArgs {
 };
 
 cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream);
+// The f32 cache's writer: key_cache / value_cache hold f32 [blocks][Hk][B][D].
+cudaError_t launch_writer_f32(const WriterArgs &a, cudaStream_t stream);
 
-enum KernelFamily { kAuto = 0, kCudaCore = 1, kTensorCore = 2 };
+// kF32: the f32-cache decode (pa_f32_decode only)
+enum KernelFamily { kAuto = 0, kCudaCore = 1, kTensorCore = 2, kF32 = 3 };
 
 struct DecodeArgs {
     float *out;

@@ -121,6 +121,76 @@ cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ f32 cache
+//
+// The f32 cache's writer: each (token, kv head) K and V vector is copied to
+// its slot of the f32 cache [num_blocks][Hk][B][D] (slot 0xFFFFFFFF skips the
+// row, as in the q8 writer).  One warp per (token, kv head); lanes move 16-byte
+// groups when the rows allow it, single floats otherwise.
+template <int D, bool kVec>
+__global__ void __launch_bounds__(kWriterWarps * 32)
+f32_scatter_kernel(const float *__restrict__ key, const float *__restrict__ value,
+                   float *__restrict__ key_cache, float *__restrict__ value_cache,
+                   const uint32_t *__restrict__ slot_mapping, int num_tokens, int64_t key_stride,
+                   int64_t value_stride, int num_kv_heads, int log2_block, int64_t num_slots,
+                   uint32_t *status) {
+    const int lane = threadIdx.x & 31;
+    const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
+    const int h = blockIdx.y;
+    if (tok >= num_tokens) return;
+    const uint32_t slot = __ldg(slot_mapping + tok);
+    if (slot == kPadSlot) return;
+    if ((int64_t)slot >= num_slots) {
+        if (lane == 0) flag_error(status, kDevBadSlot);
+        return;
+    }
+    const uint32_t blk = slot >> log2_block, off = slot & ((1u << log2_block) - 1u);
+    const int64_t dst = (((int64_t)blk * num_kv_heads + h) << log2_block | off) * D;
+    const float *ks = key + (int64_t)tok * key_stride + (int64_t)h * D;
+    const float *vs = value + (int64_t)tok * value_stride + (int64_t)h * D;
+    if constexpr (kVec) {
+#pragma unroll
+        for (int i = lane; i < D / 4; i += 32) {
+            const float4 a = __ldcs(reinterpret_cast<const float4 *>(ks) + i);
+            const float4 b = __ldcs(reinterpret_cast<const float4 *>(vs) + i);
+            reinterpret_cast<float4 *>(key_cache + dst)[i] = a;
+            reinterpret_cast<float4 *>(value_cache + dst)[i] = b;
+        }
+    } else {
+#pragma unroll 4
+        for (int i = lane; i < D; i += 32) {
+            key_cache[dst + i] = __ldcs(ks + i);
+            value_cache[dst + i] = __ldcs(vs + i);
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_f32_d(const WriterArgs &a, cudaStream_t stream) {
+    if (a.num_tokens > 0x7FFFFFFF - kWriterWarps || a.num_kv_heads > 65535) return cudaErrorInvalidValue;
+    if ((a.block_size & (a.block_size - 1)) != 0) return cudaErrorInvalidValue;
+    int log2_block = 0;
+    while ((1 << log2_block) < a.block_size) ++log2_block;
+    const dim3 grid((unsigned)((a.num_tokens + kWriterWarps - 1) / kWriterWarps), (unsigned)a.num_kv_heads);
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.key) | reinterpret_cast<uintptr_t>(a.value) |
+                       reinterpret_cast<uintptr_t>(a.key_cache) | reinterpret_cast<uintptr_t>(a.value_cache)) &
+                      15u) == 0 &&
+                     (a.key_stride % 4) == 0 && (a.value_stride % 4) == 0;
+    float *kc = reinterpret_cast<float *>(a.key_cache);
+    float *vc = reinterpret_cast<float *>(a.value_cache);
+    const int64_t num_slots = a.num_blocks * a.block_size;
+    if (vec) {
+        f32_scatter_kernel<D, true><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, kc, vc, a.slot_mapping, (int)a.num_tokens, a.key_stride, a.value_stride,
+            a.num_kv_heads, log2_block, num_slots, a.status);
+    } else {
+        f32_scatter_kernel<D, false><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, kc, vc, a.slot_mapping, (int)a.num_tokens, a.key_stride, a.value_stride,
+            a.num_kv_heads, log2_block, num_slots, a.status);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream) {
@@ -128,6 +198,15 @@ cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream) {
         case 64: return launch_d<64>(a, stream);
         case 128: return launch_d<128>(a, stream);
         case 256: return launch_d<256>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_writer_f32(const WriterArgs &a, cudaStream_t stream) {
+    switch (a.head_size) {
+        case 64: return launch_f32_d<64>(a, stream);
+        case 128: return launch_f32_d<128>(a, stream);
+        case 256: return launch_f32_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -346,14 +346,16 @@ def new_token_rows(w: Workload, num_rows: int) -> tuple[np.ndarray, np.ndarray]:
     return key, value
 
 
-def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray, num_rows: int = 1) -> int:
+def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray, num_rows: int = 1,
+                             cache: str = "q8") -> int:
     """Bytes a decode must move: every context token's K and V vector once
-    (head_size code bytes + a 4-byte scale word each), q in, out back (one
-    vector per query row and head), the block-table entries walked and the
-    context lengths."""
+    (q8: head_size code bytes + a 4-byte scale word each; f32: 4 * head_size
+    bytes), q in, out back (one vector per query row and head), the
+    block-table entries walked and the context lengths."""
     c = np.minimum(context_lens.astype(np.int64), cfg.max_blocks_per_seq * cfg.block_size)
     S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
-    kv = int(c.sum()) * Hk * 2 * (D + 4)
+    vec = {"q8": D + 4, "f32": 4 * D}[cache]
+    kv = int(c.sum()) * Hk * 2 * vec
     qo = 2 * S * int(num_rows) * H * D * 4
     bt = int((-(-c // B)).sum()) * 4
     return kv + qo + bt + S * 4
