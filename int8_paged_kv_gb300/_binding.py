@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "pa_q8.h")
 PA_Q8_KERNEL_AUTO = 0
 PA_Q8_KERNEL_CUDA_CORE = 1
 PA_Q8_KERNEL_TENSOR_CORE = 2
+PA_Q8_KERNEL_TCGEN05 = 3
 PA_Q8_DEV_BAD_BLOCK = 0x1
 PA_Q8_DEV_BAD_SLOT = 0x2
 PA_Q8_DEV_WAIT_TIMEOUT = 0x4

@@ -69,7 +69,7 @@ int check_decode_shape(int num_seqs, int num_heads, int num_kv_heads, int head_s
 int plan_for(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int num_sms, bool f32 = false) {
     int kernel = opts ? opts->kernel : PA_Q8_KERNEL_AUTO;
     const int pt = opts ? opts->partition_tokens : 0;
-    if (kernel < PA_Q8_KERNEL_AUTO || kernel > PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
+    if (kernel < PA_Q8_KERNEL_AUTO || kernel > PA_Q8_KERNEL_TCGEN05) return PA_Q8_EINVAL;
     if (f32) {
         if (kernel != PA_Q8_KERNEL_AUTO) return PA_Q8_EINVAL;
         kernel = pa_q8::kF32;

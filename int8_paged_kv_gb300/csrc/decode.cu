@@ -900,6 +900,381 @@ decode_cc_kernel(Params P) {
     merge_and_store<D>(P, w, ml, accs, kCcSlots, NH, accs + kCcSlots * NH * D);
 }
 
+// ======================================================== tcgen05 (multi-row)
+//
+// Many virtual heads per kv head (multi-row decode: R query rows x r heads)
+// make the contraction GEMM-shaped, so it runs on the 5th-generation tensor
+// cores: one CTA of 4 warps serves up to 64 virtual heads of one kv head for
+// one partition.  Warp q owns TMEM lanes 32q .. 32q+31 = M rows: rows 32q + j
+// (j < 16) hold the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq
+// like the mma.sync kernel), rows 32q + 16 + j its lo part, so the two halves
+// of a logit are one shuffle apart and every thread owns one whole row of S.
+// Per 32-token chunk: the raw tile arrives by bulk copy (same ring as the
+// other families); the codes are converted once to f16 K [32 x D] and V^T
+// [D x 32] operand tiles; one thread issues S = Q.K^T (M 128, N 32, K = D)
+// into TMEM; each thread turns its S row into weights w = p * v_scale *
+// 2^(131 - E) (the mma.sync kernel's online softmax, lazy rescale of its O
+// row in TMEM), split hi/lo into the P tile [128 x 32]; one thread issues
+// O += P.V (M 128, N = D, K 32).  QK of a chunk overlaps the V conversion,
+// PV overlaps the next chunk's K conversion.  TMEM holds S (32 columns) and
+// O (D columns).
+
+constexpr int kUmmaHeads = 64;
+
+template <int D>
+__host__ __device__ constexpr int umma_ring() { return 3; }
+template <int D>
+__host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 64 ? 128u : (D == 128 ? 256u : 512u); }
+template <int D>
+__host__ __device__ constexpr int umma_ctas_per_sm() { return (int)(512u / umma_tmem_cols<D>()); }
+
+// Byte offset of element (r, k) of an f16 operand tile with kdim columns in
+// the K-major core-matrix layout (LBO = 128, SBO = kdim / 8 * 128).
+__device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
+    return (uint32_t)(((r >> 3) * (kdim >> 3) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+struct UmmaLayout {
+    uint32_t table, ops, ring, slot_bytes, total;
+};
+
+// [ring barriers, 2 QK / 2 PV barriers, TMEM address] [table] [operand
+// tiles Q, K x2, V^T x2, P x2] [raw chunk ring].  Total at least a 1/(n+1) share of the
+// shared memory, so no more CTAs share an SM than its TMEM serves.
+template <int D>
+__host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
+    constexpr int RING = umma_ring<D>();
+    UmmaLayout L{};
+    const int ptok = B < kChunk ? B : kChunk;
+    const int pieces = (PT + ptok - 1) / ptok + 1;
+    L.table = align_up((RING + 5) * 8, 16);
+    L.ops = align_up(L.table + pieces * 4, 128);
+    const uint32_t ops_bytes = 128u * D * 2 + 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * 32 * 2);
+    L.ring = align_up(L.ops + ops_bytes, 128);
+    L.slot_bytes = align_up(2u * kChunk * (D / 4 + 1) * 4, 128);
+    L.total = L.ring + RING * L.slot_bytes;
+    const uint32_t floor_bytes = 232448u / (umma_ctas_per_sm<D>() + 1) + 128u;
+    if (L.total < floor_bytes) L.total = floor_bytes;
+    return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128, umma_ctas_per_sm<D>())
+decode_umma_kernel(Params P) {
+    constexpr int RING = umma_ring<D>();
+    constexpr int W = D / 4 + 1;
+    constexpr uint32_t TCOLS = umma_tmem_cols<D>();
+    constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
+    constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D);
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    Work w;
+    if (!setup_work(P, w)) {
+        write_zero_rows<D>(P, w);
+        return;
+    }
+    const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t s0 = smem_addr(smem);
+    // chunk j's QK and PV arrive on barrier j & 1: one phase in flight per barrier
+    const uint32_t ring_bars = s0, bar_qk0 = s0 + 8 * RING, bar_pv0 = bar_qk0 + 16;
+    const uint32_t tmem_slot = bar_pv0 + 16;
+    const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
+    constexpr uint32_t P_BYTES = 128u * kChunk * 2;
+    uint8_t *sQ = smem + L.ops, *sK0 = sQ + Q_BYTES, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
+    const uint32_t aQ = s0 + L.ops, aK0 = aQ + Q_BYTES, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
+    const uint32_t ring = s0 + L.ring;
+    const uint64_t policy = l2_policy_evict_first();
+    const F16Consts fk;
+
+    // This thread's M row: virtual head hl (CTA-local), hi (lanes 0-15) or lo
+    // part; in the softmax it handles tokens 16 * lo_part .. +15 of the chunk
+    // for both rows of its head.
+    const int hl = 16 * warp + (lane & 15);
+    const bool row_ok = hl < w.nh;
+    const int vh = w.h0 + hl;
+    const bool lo_part = lane >= 16;
+    const int half = lo_part ? 16 : 0;
+    const int len_row = row_ok ? row_len(P, w, vh) : 0;
+    const int row = 32 * warp + lane, row_hi = 32 * warp + (lane & 15), row_lo = row_hi + 16;
+    const bool warp_active = 16 * warp < w.nh;          // warp-uniform: its quadrant holds a real head
+
+    if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
+    if (tid == 0) {
+        for (int k = 0; k < RING; ++k) mbar_init(ring_bars + 8 * k, 1);
+        mbar_init(bar_qk0, 1);
+        mbar_init(bar_qk0 + 8, 1);
+        mbar_init(bar_pv0, 1);
+        mbar_init(bar_pv0 + 8, 1);
+        fence_mbar_init();
+    }
+    load_table(P, w, const_cast<uint32_t *>(table));
+    for (int i = tid; i < 2 * 128 * kChunk / 8; i += 128)   // P rows of heads that do not exist stay 0
+        reinterpret_cast<uint4 *>(sP0)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // Q row: q * 2^-eq as hi (or lo) f16, K-major
+    float qk2;
+    {
+        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
+        float mx = 0.0f;
+        for (int c = 0; c < D / 4; ++c) {
+            const float4 v = row_ok ? __ldg(qv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
+        qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
+        for (int c = 0; c < D / 8; ++c) {
+            const float4 a = row_ok ? __ldg(qv + 2 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = row_ok ? __ldg(qv + 2 * c + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            uint32_t h[4], l[4];
+            split_f16x2(a.x * down, a.y * down, h[0], l[0]);
+            split_f16x2(a.z * down, a.w * down, h[1], l[1]);
+            split_f16x2(b.x * down, b.y * down, h[2], l[2]);
+            split_f16x2(b.z * down, b.w * down, h[3], l[3]);
+            *reinterpret_cast<uint4 *>(sQ + kmaj_off(row, 8 * c, D)) =
+                lo_part ? make_uint4(l[0], l[1], l[2], l[3]) : make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + (tmem_slot - s0));
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t tO = tmem + 64;                        // S double buffer: columns 0-31, 32-63
+
+    const int nch = (w.len + kChunk - 1) / kChunk;
+    int issued = 0;
+    if (warp == 0)
+        for (; issued < RING && issued < nch; ++issued)
+            issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
+
+    // K codes of chunk c (resident in its ring slot) -> f16 K tile c & 1 [32 tokens][D]
+    auto convert_k = [&](int c) {
+        const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + (c % RING) * L.slot_bytes);
+        uint8_t *dst = sK0 + (c & 1) * K_BYTES;
+        // lane = token: the 8 lanes of a store phase write 8 rows of one core
+        // matrix (8 bank groups); the reads stride 33 words (all banks)
+        for (int u = tid; u < kChunk * D / 8; u += 128) {
+            const int t = u % kChunk, c8 = u / kChunk;
+            uint32_t a0, a1, a2, a3;
+            codes4_to_f16x2(rawK[t * W + 2 * c8], a0, a1, fk);
+            codes4_to_f16x2(rawK[t * W + 2 * c8 + 1], a2, a3, fk);
+            *reinterpret_cast<uint4 *>(dst + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
+        }
+    };
+    auto issue_qk = [&](int c) {
+        tc_fence_after();
+        const uint32_t aK = aK0 + (c & 1) * K_BYTES, tS = tmem + 32 * (c & 1);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+            umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16), umma_smem_desc(aK + ks * 256, 128, D * 16),
+                     IDESC_QK, ks > 0);
+        umma_commit(bar_qk0 + 8 * (c & 1));
+    };
+
+    float m = -INFINITY, lsum = 0.0f;                     // lsum over this thread's token halves
+    int E = 12;
+    float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+    bool ok = true;
+    int ring_done = 0, qk_issued = 0, qk_done = 0, pv_issued = 0, pv_done = 0;
+    {   // prologue: chunk 0's keys and QK
+        const bool got = mbar_wait(ring_bars, 0);
+        if (got) convert_k(0);
+        fence_proxy_async_smem();
+        if (__syncthreads_or(!got)) {
+            ok = false;
+        } else {
+            ring_done = 1;
+            if (tid == 0) issue_qk(0);
+            qk_issued = 1;
+        }
+    }
+    for (int i = 0; ok && i < nch; ++i) {
+        const int k = i % RING;
+        const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
+        const uint32_t *rawV = rawK + kChunk * W;
+        uint8_t *sV = sV0 + (i & 1) * V_BYTES, *sP = sP0 + (i & 1) * P_BYTES;
+        bool good = true;
+        // (A) the next chunk's keys (its K tile was last read by QK of chunk i - 1, done)
+        if (i + 1 < nch) {
+            good = mbar_wait(ring_bars + 8 * ((i + 1) % RING), ((i + 1) / RING) & 1);
+            if (good) convert_k(i + 1);
+        }
+        // (B) this chunk's values -> f16 V^T tile i & 1 [D][32 tokens]; its last
+        // reader, PV of chunk i - 2, must be done (so must PV i - 1's predecessors)
+        while (good && pv_done < pv_issued - 1) {
+            good = mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1);
+            if (good) ++pv_done;
+        }
+        if (good) {
+            // lane = head dim d: row d of V^T, 8 tokens per 16-byte store; the 8
+            // lanes of a store phase write 8 rows (8 bank groups), four lanes
+            // read the same code word
+            for (int u = tid; u < D * (kChunk / 8); u += 128) {
+                const int d = u % D, tg = u / D;
+                const uint32_t *src = rawV + (8 * tg) * W + (d >> 2);
+                const uint32_t e = (uint32_t)(d & 3);
+                const uint32_t sel = e | (e << 4) | ((e + 4) << 8) | ((e + 4) << 12);
+                uint32_t h[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    h[j] = sub_1152_x2(and_xor_i<0x00FF00FFu>(prmt_r(src[2 * j * W], src[(2 * j + 1) * W], sel),
+                                                            fk.bias),
+                                       fk.bias);
+                *reinterpret_cast<uint4 *>(sV + kmaj_off(d, 8 * tg, kChunk)) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        if (__syncthreads_or(!good)) {
+            ok = false;
+            break;
+        }
+        if (i + 1 < nch) {
+            ++ring_done;
+            if (tid == 0) issue_qk(i + 1);       // overlaps this chunk's softmax
+            ++qk_issued;
+        }
+        // (C) S of chunk i: this thread's 16 tokens of its head (hi + lo rows)
+        good = mbar_wait(bar_qk0 + 8 * (qk_done & 1), (qk_done >> 1) & 1);
+        if (good) ++qk_done;
+        good = __all_sync(0xFFFFFFFFu, good);     // TMEM accesses below are warp-collective
+        if (good && warp_active) {
+            tc_fence_after();
+            float sv[32];
+            tmem_ld32(tmem + 32 * (i & 1) + lane_off, sv);
+            float z[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float other = __shfl_xor_sync(0xFFFFFFFFu, lo_part ? sv[j] : sv[16 + j], 16);
+                z[j] = sv[half + j] + other;
+            }
+            const int t0 = i * kChunk + half;
+            float cmax = -INFINITY, vmax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const bool valid = t0 + j < len_row;
+                z[j] = valid ? z[j] * __uint_as_float(rawK[(half + j) * W + D / 4]) * qk2 : -INFINITY;
+                cmax = fmaxf(cmax, z[j]);
+                vmax = fmaxf(vmax, valid ? __uint_as_float(rawV[(half + j) * W + D / 4]) : 0.0f);
+            }
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 16));
+            const int Ec = (int)(__float_as_uint(vmax) >> 23);
+            const bool need = cmax > m + (float)kLazy || Ec > E;
+            float fa = 1.0f;
+            if (need) {
+                const float m_new = fmaxf(m, cmax);
+                const int E_new = max(E, Ec);
+                const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+                const float ea = (E - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - E_new) << 23);
+                fa = alpha * ea;
+                lsum *= alpha;
+                m = m_new;
+                E = E_new;
+                wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+            }
+            // rescale this warp's O rows once PV of chunk i - 1 is done; rows
+            // that need none take factor 1
+            const bool rescale = pv_issued > 0 && __any_sync(0xFFFFFFFFu, need);
+            bool o_ready = true;
+            if (rescale && pv_done < pv_issued) {
+                o_ready = mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1);
+                if (o_ready) ++pv_done;
+                o_ready = __all_sync(0xFFFFFFFFu, o_ready);
+                if (o_ready) tc_fence_after();
+                else good = false;
+            }
+            if (rescale && o_ready) {
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tO + lane_off + 32 * c, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= fa;
+                    tmem_st32(tO + lane_off + 32 * c, o);
+                }
+            }
+            const float m_ref = m == -INFINITY ? 0.0f : m;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {                 // tokens half + 8c .. +7, both rows of the head
+                uint32_t ph[4], pl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 8 * c + 2 * e;
+                    const float p0 = fast_exp2(z[j] - m_ref), p1 = fast_exp2(z[j + 1] - m_ref);
+                    lsum += p0 + p1;
+                    const float vs0 = t0 + j < len_row ? __uint_as_float(rawV[(half + j) * W + D / 4]) : 0.0f;
+                    const float vs1 = t0 + j + 1 < len_row ? __uint_as_float(rawV[(half + j + 1) * W + D / 4]) : 0.0f;
+                    split_f16x2(p0 * vs0 * wscale, p1 * vs1 * wscale, ph[e], pl[e]);
+                }
+                *reinterpret_cast<uint4 *>(sP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
+                    make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4 *>(sP + kmaj_off(row_lo, half + 8 * c, kChunk)) =
+                    make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(!good)) {
+            ok = false;
+            break;
+        }
+        // raw buffer k is consumed: refill it; then O += P . V
+        if (warp == 0 && issued < nch) {
+            issue_chunk<D>(P, w, table, issued, ring + k * L.slot_bytes, ring_bars + 8 * k, policy);
+            ++issued;
+        }
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t aP = aP0 + (i & 1) * P_BYTES, aV = aV0 + (i & 1) * V_BYTES;
+            umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, i > 0);
+            umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512), IDESC_PV, true);
+            umma_commit(bar_pv0 + 8 * (i & 1));
+        }
+        ++pv_issued;
+    }
+    // every MMA and copy this CTA started has finished before TMEM is freed (bounded)
+    for (; qk_done < qk_issued; ++qk_done)
+        if (!mbar_wait(bar_qk0 + 8 * (qk_done & 1), (qk_done >> 1) & 1)) { ok = false; break; }
+    for (; pv_done < pv_issued; ++pv_done)
+        if (!mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1)) { ok = false; break; }
+    if (warp == 0) drain(P, ring_bars, RING, ring_done, issued);
+    ok = !__syncthreads_or(!ok);                 // CTA-uniform: the TMEM loads below are warp-collective
+    tc_fence_after();
+    float *ml = reinterpret_cast<float *>(sQ);                    // [64][3]   (operand tiles are free)
+    float *accs = ml + kUmmaHeads * 3;                            // [64][D]
+    if (ok && warp_active) {
+        for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + lane_off + 32 * c, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] += __shfl_xor_sync(0xFFFFFFFFu, o[j], 16);
+            if (!lo_part) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) accs[hl * D + 32 * c + j] = o[j];
+            }
+        }
+        const float l_row = lsum + __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+        if (!lo_part) {
+            ml[hl * 3] = m;
+            ml[hl * 3 + 1] = l_row;
+            ml[hl * 3 + 2] = (float)E;
+        }
+    }
+    tc_fence_before();
+    const bool failed = __syncthreads_or(!ok);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+    }
+    if (failed) {
+        if (tid == 0) flag_error(P.status, kDevWaitTimeout);
+        return;
+    }
+    merge_and_store<D>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
+}
+
 // ============================================================== f32 cache
 //
 // The f32 variant of the cache, token vectors of head_size f32 values and no
@@ -1406,6 +1781,10 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     if (kernel == kF32) return launch_f32<D>(P, st);
+    if (kernel == kTcgen05) {
+        const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
+        return launch_attn(decode_umma_kernel<D>, P, L.total, 128, st);
+    }
     return (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
 }
 
@@ -1416,8 +1795,12 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     // (query row, head) pairs served per kv head: the rows of one sequence
     // share their kv group's K/V read like the heads of a GQA group
     const int r = a.num_rows * (a.num_heads / a.num_kv_heads);
+    // automatic: the mma.sync tensor-core family (the tcgen05 family is
+    // selectable; it does not yet beat it on any measured shape)
     a.kernel = requested_kernel == kAuto ? kTensorCore : requested_kernel;
-    if (a.kernel == kTensorCore) {
+    if (a.kernel == kTcgen05) {
+        a.heads_per_cta = r < kUmmaHeads ? r : kUmmaHeads;
+    } else if (a.kernel == kTensorCore) {
         const int cap = a.head_size == 256 ? 16 : PA_Q8_TC_MAX_HEADS;
         a.heads_per_cta = r < cap ? r : cap;
     } else {
@@ -1432,7 +1815,10 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
         // CTAs resident per SM for this kernel configuration
         const int hd = a.head_size;
         const bool big_tile = hd == 256 || a.heads_per_cta > 8;
-        const int per_sm = a.kernel == kF32 ? 1 : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2) : (big_tile ? 1 : 3);
+        const int per_sm = a.kernel == kF32       ? 1
+                           : a.kernel == kTcgen05 ? (hd == 64 ? 4 : hd == 128 ? 2 : 1)
+                           : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
+                                                   : (big_tile ? 1 : 3);
         const int64_t slots = (int64_t)per_sm * num_sms;
         const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
         if (units >= slots) {

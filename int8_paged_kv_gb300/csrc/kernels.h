@@ -28,8 +28,9 @@ cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream);
 // The f32 cache's writer: key_cache / value_cache hold f32 [blocks][Hk][B][D].
 cudaError_t launch_writer_f32(const WriterArgs &a, cudaStream_t stream);
 
+// kTcgen05: 5th-generation tensor cores (many virtual heads per kv head);
 // kF32: the f32-cache decode (pa_f32_decode only)
-enum KernelFamily { kAuto = 0, kCudaCore = 1, kTensorCore = 2, kF32 = 3 };
+enum KernelFamily { kAuto = 0, kCudaCore = 1, kTensorCore = 2, kTcgen05 = 3, kF32 = 8 };
 
 struct DecodeArgs {
     float *out;
@@ -48,7 +49,7 @@ struct DecodeArgs {
     int64_t num_blocks;
     float scale;
     // plan (filled by make_plan)
-    int kernel;            // kCudaCore or kTensorCore
+    int kernel;            // kCudaCore, kTensorCore, kTcgen05 or kF32
     int partition_tokens;  // tokens per partition
     int num_partitions;    // partitions per sequence (grid x)
     int heads_per_cta;     // query heads one CTA serves (one kv head's group, or part of it)

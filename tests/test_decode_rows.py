@@ -13,7 +13,7 @@ from int8_paged_kv_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-TC, CC = 2, 1
+TC, CC, T5 = 2, 1, 3          # T5: tcgen05 (5th-generation tensor cores, TMEM accumulators)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -51,7 +51,7 @@ def test_one_row_is_single_query_decode_bitwise(kernel):
         assert np.array_equal(a, b[:, 0]), f"pt {pt}"
 
 
-@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("kernel", [TC, CC, T5])
 @pytest.mark.parametrize("name,R", [("tiny", 1), ("tiny", 3), ("tiny", 8), ("llama8b", 2),
                                     ("llama8b", 5), ("edge", 3)])
 def test_workloads_all_rows(name, R, kernel):
@@ -64,7 +64,7 @@ def test_workloads_all_rows(name, R, kernel):
     assert device_status() == 0
 
 
-@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("kernel", [TC, CC, T5])
 def test_forced_partitions_with_rows_that_see_none_of_the_last(kernel):
     """Contexts 1 .. 3 tokens past a partition boundary: the lower rows see
     nothing of the last partition, the combine must give those partials no
@@ -90,7 +90,7 @@ def _random_case(*args, **kw):
     return random_case(*args, **kw)
 
 
-@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("kernel", [TC, CC, T5])
 @pytest.mark.parametrize("H,Hk,D,R", [(4, 4, 64, 16), (8, 4, 64, 7), (32, 1, 128, 2), (16, 2, 128, 4),
                                       (16, 1, 256, 3), (8, 8, 256, 2), (24, 2, 64, 5)])
 def test_gqa_ratios_head_sizes_and_row_counts(kernel, H, Hk, D, R):
@@ -104,7 +104,7 @@ def test_gqa_ratios_head_sizes_and_row_counts(kernel, H, Hk, D, R):
                      f"H {H} Hk {Hk} D {D} R {R} pt {pt}")
 
 
-@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("kernel", [TC, CC, T5])
 def test_clamped_context(kernel):
     from tests.gpu_helpers import assert_close, gpu_decode_rows, oracle_decode_rows
     lens = [64, 208, 50]                                   # 208 = max_blocks_per_seq * 16
@@ -135,7 +135,7 @@ def _sampled_rows_oracle(w, ok_, ov_, q, picks):
     return np.array(out)
 
 
-@pytest.mark.parametrize("kernel", [0, TC, CC])
+@pytest.mark.parametrize("kernel", [0, TC, CC, T5])
 def test_large_batch_four_rows_sampled(kernel):
     """The large-batch workload with 4 query rows per sequence, in the
     automatic launch plan; sampled (s, b, h) rows against the oracle."""
@@ -155,3 +155,18 @@ def test_large_batch_four_rows_sampled(kernel):
     assert_close(sel, want, f"large R 4 kernel {kernel}")
     assert np.all(np.isfinite(got))
     assert device_status() == 0
+
+
+@pytest.mark.parametrize("H,Hk,D", [(8, 2, 64), (32, 8, 128), (16, 1, 256), (64, 1, 128)])
+def test_tcgen05_single_row_and_wide_groups(H, Hk, D):
+    """The tcgen05 family asked for explicitly at R = 1, and a 64-head group
+    (one full CTA of virtual heads), against the oracle."""
+    from tests.gpu_helpers import assert_close, gpu_decode_rows, oracle_decode_rows
+    lens = [1, 40, 333, 1500]
+    w, ok_, ov_, kc, vc = _random_case(4, H, Hk, D, 16, lens, seed=H + D)
+    for R in (1, 2):
+        q = np.random.default_rng(R + H).standard_normal((4, R, H, D)).astype(np.float32)
+        want = oracle_decode_rows(w, ok_, ov_, q)
+        for pt in (0, 256):
+            assert_close(gpu_decode_rows(w, kc, vc, q, kernel=T5, partition_tokens=pt), want,
+                         f"H {H} Hk {Hk} D {D} R {R} pt {pt}")
