@@ -904,29 +904,40 @@ decode_cc_kernel(Params P) {
 //
 // Many virtual heads per kv head (multi-row decode: R query rows x r heads)
 // make the contraction GEMM-shaped, so it runs on the 5th-generation tensor
-// cores: one CTA of 4 warps serves up to 64 virtual heads of one kv head for
-// one partition.  Warp q owns TMEM lanes 32q .. 32q+31 = M rows: rows 32q + j
-// (j < 16) hold the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq
-// like the mma.sync kernel), rows 32q + 16 + j its lo part, so the two halves
-// of a logit are one shuffle apart and every thread owns one whole row of S.
-// Per 32-token chunk: the raw tile arrives by bulk copy (same ring as the
-// other families); the codes are converted once to f16 K [32 x D] and V^T
-// [D x 32] operand tiles; one thread issues S = Q.K^T (M 128, N 32, K = D)
-// into TMEM; each thread turns its S row into weights w = p * v_scale *
-// 2^(131 - E) (the mma.sync kernel's online softmax, lazy rescale of its O
-// row in TMEM), split hi/lo into the P tile [128 x 32]; one thread issues
-// O += P.V (M 128, N = D, K 32).  QK of a chunk overlaps the V conversion,
-// PV overlaps the next chunk's K conversion.  TMEM holds S (32 columns) and
+// cores: one CTA serves up to 64 virtual heads of one kv head for one
+// partition.  TMEM lane quadrant q holds M rows 32q .. 32q+31: rows 32q + j
+// (j < 16) the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq like
+// the mma.sync kernel), rows 32q + 16 + j its lo part, so a logit's two
+// halves are one shuffle apart.  TMEM holds S twice (columns 0-31, 32-63) and
 // O (D columns).
+//
+// Warp roles, linked only by mbarriers (every wait bounded and abortable):
+//  - warps 0-3, softmax: warp q owns quadrant q (idle when it holds no head).
+//    Per chunk: S row -> online softmax (hi/lo partner threads take 16 tokens
+//    each; lazy rescale of O rows in TMEM) -> P tile rows (w = p * v_scale *
+//    2^(131 - E), split hi/lo like the mma.sync kernel).
+//  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
+//    the other families) become f16 K [32][D] and V^T [D][32] tiles (K-major
+//    core matrices) and the token scales a small table.
+//  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
+//    and, one chunk behind, O += P.V (M 128, N D, K 32).
+// K, V^T, P and S are double buffered by chunk parity.  Signals per buffer
+// b = chunk & 1: conv[b] (96 conversion threads), s_free[b] / p_ready[b]
+// (the active softmax threads), qk[b] / pv[b] (tcgen05.commit).  A waiter
+// never falls two phases behind: the next phase of each barrier needs a step
+// that follows the wait.
 
 constexpr int kUmmaHeads = 64;
+constexpr int kUmmaThreads = 256;
+constexpr int kUmmaConvThreads = 96;
 
 template <int D>
 __host__ __device__ constexpr int umma_ring() { return 3; }
 template <int D>
 __host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 64 ? 128u : (D == 128 ? 256u : 512u); }
+// resident CTAs per SM: TMEM (512 columns) and registers (2 x 256 threads x 128)
 template <int D>
-__host__ __device__ constexpr int umma_ctas_per_sm() { return (int)(512u / umma_tmem_cols<D>()); }
+__host__ __device__ constexpr int umma_ctas_per_sm() { return D == 256 ? 1 : 2; }
 
 // Byte offset of element (r, k) of an f16 operand tile with kdim columns in
 // the K-major core-matrix layout (LBO = 128, SBO = kdim / 8 * 128).
@@ -934,20 +945,26 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
     return (uint32_t)(((r >> 3) * (kdim >> 3) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
 
+// barrier slots (8 bytes each) after the ring's
+enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarConv = 4, kBarSFree = 6, kBarPReady = 8, kUmmaBars = 10 };
+
 struct UmmaLayout {
-    uint32_t table, ops, ring, slot_bytes, total;
+    uint32_t misc, scales, table, ops, ring, slot_bytes, total;
 };
 
-// [ring barriers, 2 QK / 2 PV barriers, TMEM address] [table] [operand
-// tiles Q, K x2, V^T x2, P x2] [raw chunk ring].  Total at least a 1/(n+1) share of the
-// shared memory, so no more CTAs share an SM than its TMEM serves.
+// [barriers: ring, kUmmaBars] [TMEM address, abort flag] [token scales 2 x
+// (K, V) x 32] [table] [operand tiles Q, K x2, V^T x2, P x2] [raw chunk ring].
+// Total at least a 1/(n+1) share of the shared memory, so no more CTAs share
+// an SM than its TMEM serves.
 template <int D>
 __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
     constexpr int RING = umma_ring<D>();
     UmmaLayout L{};
     const int ptok = B < kChunk ? B : kChunk;
     const int pieces = (PT + ptok - 1) / ptok + 1;
-    L.table = align_up((RING + 5) * 8, 16);
+    L.misc = (RING + kUmmaBars) * 8;
+    L.scales = align_up(L.misc + 8, 16);
+    L.table = L.scales + 2 * 2 * kChunk * 4;
     L.ops = align_up(L.table + pieces * 4, 128);
     const uint32_t ops_bytes = 128u * D * 2 + 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * 32 * 2);
     L.ring = align_up(L.ops + ops_bytes, 128);
@@ -959,12 +976,13 @@ __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(128, umma_ctas_per_sm<D>())
+__global__ void __launch_bounds__(kUmmaThreads, umma_ctas_per_sm<D>())
 decode_umma_kernel(Params P) {
     constexpr int RING = umma_ring<D>();
     constexpr int W = D / 4 + 1;
     constexpr uint32_t TCOLS = umma_tmem_cols<D>();
     constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
+    constexpr uint32_t P_BYTES = 128u * kChunk * 2;
     constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D);
 
     extern __shared__ __align__(128) uint8_t smem[];
@@ -976,44 +994,47 @@ decode_umma_kernel(Params P) {
     const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t s0 = smem_addr(smem);
-    // chunk j's QK and PV arrive on barrier j & 1: one phase in flight per barrier
-    const uint32_t ring_bars = s0, bar_qk0 = s0 + 8 * RING, bar_pv0 = bar_qk0 + 16;
-    const uint32_t tmem_slot = bar_pv0 + 16;
+    const uint32_t ring_bars = s0, bars = s0 + 8 * RING;
+    auto bar = [&](int kind, int b) { return bars + 8 * (kind + b); };
+    const uint32_t tmem_slot = s0 + L.misc;
+    volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + L.misc + 4);
+    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [2][32]
+    float *vsc = ksc + 2 * kChunk;                                       // [2][32]
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
-    constexpr uint32_t P_BYTES = 128u * kChunk * 2;
     uint8_t *sQ = smem + L.ops, *sK0 = sQ + Q_BYTES, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
     const uint32_t aQ = s0 + L.ops, aK0 = aQ + Q_BYTES, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
     const uint32_t ring = s0 + L.ring;
     const uint64_t policy = l2_policy_evict_first();
-    const F16Consts fk;
-
-    // This thread's M row: virtual head hl (CTA-local), hi (lanes 0-15) or lo
-    // part; in the softmax it handles tokens 16 * lo_part .. +15 of the chunk
-    // for both rows of its head.
-    const int hl = 16 * warp + (lane & 15);
-    const bool row_ok = hl < w.nh;
-    const int vh = w.h0 + hl;
-    const bool lo_part = lane >= 16;
-    const int half = lo_part ? 16 : 0;
-    const int len_row = row_ok ? row_len(P, w, vh) : 0;
-    const int row = 32 * warp + lane, row_hi = 32 * warp + (lane & 15), row_lo = row_hi + 16;
-    const bool warp_active = 16 * warp < w.nh;          // warp-uniform: its quadrant holds a real head
+    const int nquad = min(4, (w.nh + 15) / 16);         // quadrants that hold a real head
+    const int nch = (w.len + kChunk - 1) / kChunk;
 
     if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
     if (tid == 0) {
         for (int k = 0; k < RING; ++k) mbar_init(ring_bars + 8 * k, 1);
-        mbar_init(bar_qk0, 1);
-        mbar_init(bar_qk0 + 8, 1);
-        mbar_init(bar_pv0, 1);
-        mbar_init(bar_pv0 + 8, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarQk, b), 1);
+            mbar_init(bar(kBarPv, b), 1);
+            mbar_init(bar(kBarConv, b), kUmmaConvThreads);
+            mbar_init(bar(kBarSFree, b), 32 * nquad);
+            mbar_init(bar(kBarPReady, b), 32 * nquad);
+        }
+        *abort = 0u;
         fence_mbar_init();
     }
     load_table(P, w, const_cast<uint32_t *>(table));
-    for (int i = tid; i < 2 * 128 * kChunk / 8; i += 128)   // P rows of heads that do not exist stay 0
+    for (int i = tid; i < 2 * 128 * kChunk / 8; i += kUmmaThreads)    // P rows of heads that do not exist stay 0
         reinterpret_cast<uint4 *>(sP0)[i] = make_uint4(0u, 0u, 0u, 0u);
-    // Q row: q * 2^-eq as hi (or lo) f16, K-major
-    float qk2;
-    {
+
+    // softmax threads: this thread's M row (virtual head hl, hi or lo part)
+    const int hl = 16 * (warp & 3) + (lane & 15);
+    const bool row_ok = warp < 4 && hl < w.nh;
+    const int vh = w.h0 + hl;
+    const bool lo_part = lane >= 16;
+    const int half = lo_part ? 16 : 0;
+    const int len_row = row_ok ? row_len(P, w, vh) : 0;
+    const int row = 32 * (warp & 3) + lane, row_hi = 32 * (warp & 3) + (lane & 15), row_lo = row_hi + 16;
+    float qk2 = 0.0f;
+    if (warp < 4) {      // Q row: q * 2^-eq as hi (or lo) f16, K-major
         const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
         float mx = 0.0f;
         for (int c = 0; c < D / 4; ++c) {
@@ -1039,79 +1060,97 @@ decode_umma_kernel(Params P) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + (tmem_slot - s0));
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-    const uint32_t tO = tmem + 64;                        // S double buffer: columns 0-31, 32-63
+    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + L.misc);
+    const uint32_t tO = tmem + 64;
 
-    const int nch = (w.len + kChunk - 1) / kChunk;
-    int issued = 0;
-    if (warp == 0)
+    // softmax state (warps 0-3) and the issuer's commit record (warp 7, lane 0)
+    float m = -INFINITY, lsum = 0.0f;
+    int E = 12;
+    int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
+    uint32_t last_parity = 0;
+    int issued = 0;                  // chunks whose ring copy warp 7 started
+
+    if (warp == 7) {
+        // ---- ring refills and MMA issue
         for (; issued < RING && issued < nch; ++issued)
             issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
-
-    // K codes of chunk c (resident in its ring slot) -> f16 K tile c & 1 [32 tokens][D]
-    auto convert_k = [&](int c) {
-        const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + (c % RING) * L.slot_bytes);
-        uint8_t *dst = sK0 + (c & 1) * K_BYTES;
-        // lane = token: the 8 lanes of a store phase write 8 rows of one core
-        // matrix (8 bank groups); the reads stride 33 words (all banks)
-        for (int u = tid; u < kChunk * D / 8; u += 128) {
-            const int t = u % kChunk, c8 = u / kChunk;
-            uint32_t a0, a1, a2, a3;
-            codes4_to_f16x2(rawK[t * W + 2 * c8], a0, a1, fk);
-            codes4_to_f16x2(rawK[t * W + 2 * c8 + 1], a2, a3, fk);
-            *reinterpret_cast<uint4 *>(dst + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
-        }
-    };
-    auto issue_qk = [&](int c) {
-        tc_fence_after();
-        const uint32_t aK = aK0 + (c & 1) * K_BYTES, tS = tmem + 32 * (c & 1);
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1;
+            if (!mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort)) break;    // K(i), V(i) ready
+            if (issued < nch) {                                // chunk i's raw slot is free
+                issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
+                               ring_bars + 8 * (issued % RING), policy);
+                ++issued;
+            }
+            bool go = true;
+            if (lane == 0) {
+                if (i >= 2) go = mbar_wait_abortable(bar(kBarSFree, b), ((i - 2) >> 1) & 1, abort);
+                if (go) {
+                    tc_fence_after();
+                    const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-            umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16), umma_smem_desc(aK + ks * 256, 128, D * 16),
-                     IDESC_QK, ks > 0);
-        umma_commit(bar_qk0 + 8 * (c & 1));
-    };
-
-    float m = -INFINITY, lsum = 0.0f;                     // lsum over this thread's token halves
-    int E = 12;
-    float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
-    bool ok = true;
-    int ring_done = 0, qk_issued = 0, qk_done = 0, pv_issued = 0, pv_done = 0;
-    {   // prologue: chunk 0's keys and QK
-        const bool got = mbar_wait(ring_bars, 0);
-        if (got) convert_k(0);
-        fence_proxy_async_smem();
-        if (__syncthreads_or(!got)) {
-            ok = false;
-        } else {
-            ring_done = 1;
-            if (tid == 0) issue_qk(0);
-            qk_issued = 1;
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16),
+                                 umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
+                    umma_commit(bar(kBarQk, b));
+                    last_commit = kBarQk + b;
+                    last_parity = (i >> 1) & 1;
+                }
+                if (go && i >= 1) {                            // O += P(i-1) . V(i-1)
+                    const int j = i - 1, bj = j & 1;
+                    go = mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort);
+                    if (go) {
+                        tc_fence_after();
+                        const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
+                        umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
+                        umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512),
+                                 IDESC_PV, true);
+                        umma_commit(bar(kBarPv, bj));
+                        last_commit = kBarPv + bj;
+                        last_parity = (j >> 1) & 1;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, (int)go, 0)) break;
         }
-    }
-    for (int i = 0; ok && i < nch; ++i) {
-        const int k = i % RING;
-        const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
-        const uint32_t *rawV = rawK + kChunk * W;
-        uint8_t *sV = sV0 + (i & 1) * V_BYTES, *sP = sP0 + (i & 1) * P_BYTES;
-        bool good = true;
-        // (A) the next chunk's keys (its K tile was last read by QK of chunk i - 1, done)
-        if (i + 1 < nch) {
-            good = mbar_wait(ring_bars + 8 * ((i + 1) % RING), ((i + 1) / RING) & 1);
-            if (good) convert_k(i + 1);
+        if (lane == 0 && !*abort && nch > 0) {                // the last chunk's PV
+            const int j = nch - 1, bj = j & 1;
+            if (mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort)) {
+                tc_fence_after();
+                const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
+                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
+                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512), IDESC_PV,
+                         true);
+                umma_commit(bar(kBarPv, bj));
+                last_commit = kBarPv + bj;
+                last_parity = (j >> 1) & 1;
+            }
         }
-        // (B) this chunk's values -> f16 V^T tile i & 1 [D][32 tokens]; its last
-        // reader, PV of chunk i - 2, must be done (so must PV i - 1's predecessors)
-        while (good && pv_done < pv_issued - 1) {
-            good = mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1);
-            if (good) ++pv_done;
-        }
-        if (good) {
-            // lane = head dim d: row d of V^T, 8 tokens per 16-byte store; the 8
-            // lanes of a store phase write 8 rows (8 bank groups), four lanes
-            // read the same code word
-            for (int u = tid; u < D * (kChunk / 8); u += 128) {
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---- conversion (96 threads)
+        const int ct = tid - 128;
+        const F16Consts fk;
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1, k = i % RING;
+            const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
+            const uint32_t *rawV = rawK + kChunk * W;
+            if (!mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort)) break;
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)) break;   // K tile free
+            uint8_t *dK = sK0 + b * K_BYTES;
+            for (int u = ct; u < kChunk * D / 8; u += kUmmaConvThreads) {   // lane = token: 8 bank groups
+                const int t = u % kChunk, c8 = u / kChunk;
+                uint32_t a0, a1, a2, a3;
+                codes4_to_f16x2(rawK[t * W + 2 * c8], a0, a1, fk);
+                codes4_to_f16x2(rawK[t * W + 2 * c8 + 1], a2, a3, fk);
+                *reinterpret_cast<uint4 *>(dK + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
+            }
+            // V tile and scale table b free: PV(i-2) done, so softmax(i-2) is too
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
+            if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
+            else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
+            uint8_t *dV = sV0 + b * V_BYTES;
+            for (int u = ct; u < D * (kChunk / 8); u += kUmmaConvThreads) {  // lane = head dim: 8 bank groups
                 const int d = u % D, tg = u / D;
                 const uint32_t *src = rawV + (8 * tg) * W + (d >> 2);
                 const uint32_t e = (uint32_t)(d & 3);
@@ -1122,41 +1161,40 @@ decode_umma_kernel(Params P) {
                     h[j] = sub_1152_x2(and_xor_i<0x00FF00FFu>(prmt_r(src[2 * j * W], src[(2 * j + 1) * W], sel),
                                                             fk.bias),
                                        fk.bias);
-                *reinterpret_cast<uint4 *>(sV + kmaj_off(d, 8 * tg, kChunk)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(dV + kmaj_off(d, 8 * tg, kChunk)) = make_uint4(h[0], h[1], h[2], h[3]);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarConv, b));
         }
-        fence_proxy_async_smem();
-        if (__syncthreads_or(!good)) {
-            ok = false;
-            break;
-        }
-        if (i + 1 < nch) {
-            ++ring_done;
-            if (tid == 0) issue_qk(i + 1);       // overlaps this chunk's softmax
-            ++qk_issued;
-        }
-        // (C) S of chunk i: this thread's 16 tokens of its head (hi + lo rows)
-        good = mbar_wait(bar_qk0 + 8 * (qk_done & 1), (qk_done >> 1) & 1);
-        if (good) ++qk_done;
-        good = __all_sync(0xFFFFFFFFu, good);     // TMEM accesses below are warp-collective
-        if (good && warp_active) {
+    } else if (warp < nquad) {
+        // ---- softmax (quadrant warp)
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+        bool ok = true;
+        for (int i = 0; ok && i < nch; ++i) {
+            const int b = i & 1;
+            ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
+            ok = ok && mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort);     // the scale table
+            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             tc_fence_after();
-            float sv[32];
-            tmem_ld32(tmem + 32 * (i & 1) + lane_off, sv);
-            float z[16];
+            float sv[32], z[16];
+            tmem_ld32(tmem + 32 * b + lane_off, sv);      // TMEM addresses are warp-uniform
+            tc_fence_before();
+            mbar_arrive(bar(kBarSFree, b));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float other = __shfl_xor_sync(0xFFFFFFFFu, lo_part ? sv[j] : sv[16 + j], 16);
-                z[j] = sv[half + j] + other;
+            for (int j = 0; j < 16; ++j) {                // own half + the partner's row at those tokens
+                const float mine = lo_part ? sv[16 + j] : sv[j], send = lo_part ? sv[j] : sv[16 + j];
+                z[j] = mine + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
             }
+            const float *ks = ksc + b * kChunk + half, *vs = vsc + b * kChunk + half;
             const int t0 = i * kChunk + half;
             float cmax = -INFINITY, vmax = 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const bool valid = t0 + j < len_row;
-                z[j] = valid ? z[j] * __uint_as_float(rawK[(half + j) * W + D / 4]) * qk2 : -INFINITY;
+                z[j] = valid ? z[j] * ks[j] * qk2 : -INFINITY;
                 cmax = fmaxf(cmax, z[j]);
-                vmax = fmaxf(vmax, valid ? __uint_as_float(rawV[(half + j) * W + D / 4]) : 0.0f);
+                vmax = fmaxf(vmax, valid ? vs[j] : 0.0f);
             }
             cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));
             vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 16));
@@ -1174,18 +1212,10 @@ decode_umma_kernel(Params P) {
                 E = E_new;
                 wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
             }
-            // rescale this warp's O rows once PV of chunk i - 1 is done; rows
-            // that need none take factor 1
-            const bool rescale = pv_issued > 0 && __any_sync(0xFFFFFFFFu, need);
-            bool o_ready = true;
-            if (rescale && pv_done < pv_issued) {
-                o_ready = mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1);
-                if (o_ready) ++pv_done;
-                o_ready = __all_sync(0xFFFFFFFFu, o_ready);
-                if (o_ready) tc_fence_after();
-                else good = false;
-            }
-            if (rescale && o_ready) {
+            if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {      // O rows once PV(i-1) is done
+                ok = mbar_wait_abortable(bar(kBarPv, (i - 1) & 1), ((i - 1) >> 1) & 1, abort);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
@@ -1195,7 +1225,12 @@ decode_umma_kernel(Params P) {
                     tmem_st32(tO + lane_off + 32 * c, o);
                 }
             }
+            if (i >= 2) {                                       // P tile b free: PV(i-2) done
+                ok = mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            }
             const float m_ref = m == -INFINITY ? 0.0f : m;
+            uint8_t *dP = sP0 + b * P_BYTES;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {                 // tokens half + 8c .. +7, both rows of the head
                 uint32_t ph[4], pl[4];
@@ -1204,66 +1239,55 @@ decode_umma_kernel(Params P) {
                     const int j = 8 * c + 2 * e;
                     const float p0 = fast_exp2(z[j] - m_ref), p1 = fast_exp2(z[j + 1] - m_ref);
                     lsum += p0 + p1;
-                    const float vs0 = t0 + j < len_row ? __uint_as_float(rawV[(half + j) * W + D / 4]) : 0.0f;
-                    const float vs1 = t0 + j + 1 < len_row ? __uint_as_float(rawV[(half + j + 1) * W + D / 4]) : 0.0f;
-                    split_f16x2(p0 * vs0 * wscale, p1 * vs1 * wscale, ph[e], pl[e]);
+                    const float w0 = t0 + j < len_row ? vs[j] : 0.0f, w1 = t0 + j + 1 < len_row ? vs[j + 1] : 0.0f;
+                    split_f16x2(p0 * w0 * wscale, p1 * w1 * wscale, ph[e], pl[e]);
                 }
-                *reinterpret_cast<uint4 *>(sP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
                     make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                *reinterpret_cast<uint4 *>(sP + kmaj_off(row_lo, half + 8 * c, kChunk)) =
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_lo, half + 8 * c, kChunk)) =
                     make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(kBarPReady, b));
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!good)) {
-            ok = false;
-            break;
-        }
-        // raw buffer k is consumed: refill it; then O += P . V
-        if (warp == 0 && issued < nch) {
-            issue_chunk<D>(P, w, table, issued, ring + k * L.slot_bytes, ring_bars + 8 * k, policy);
-            ++issued;
-        }
-        if (tid == 0) {
+        // the last PV, then this warp's O rows (hi + lo) into the merge scratch
+        if (ok && nch > 0) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) & 1), ((nch - 1) >> 1) & 1, abort);
+        if (__all_sync(0xFFFFFFFFu, ok)) {
             tc_fence_after();
-            const uint32_t aP = aP0 + (i & 1) * P_BYTES, aV = aV0 + (i & 1) * V_BYTES;
-            umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, i > 0);
-            umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512), IDESC_PV, true);
-            umma_commit(bar_pv0 + 8 * (i & 1));
-        }
-        ++pv_issued;
-    }
-    // every MMA and copy this CTA started has finished before TMEM is freed (bounded)
-    for (; qk_done < qk_issued; ++qk_done)
-        if (!mbar_wait(bar_qk0 + 8 * (qk_done & 1), (qk_done >> 1) & 1)) { ok = false; break; }
-    for (; pv_done < pv_issued; ++pv_done)
-        if (!mbar_wait(bar_pv0 + 8 * (pv_done & 1), (pv_done >> 1) & 1)) { ok = false; break; }
-    if (warp == 0) drain(P, ring_bars, RING, ring_done, issued);
-    ok = !__syncthreads_or(!ok);                 // CTA-uniform: the TMEM loads below are warp-collective
-    tc_fence_after();
-    float *ml = reinterpret_cast<float *>(sQ);                    // [64][3]   (operand tiles are free)
-    float *accs = ml + kUmmaHeads * 3;                            // [64][D]
-    if (ok && warp_active) {
-        for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + lane_off + 32 * c, o);
+            float *ml = reinterpret_cast<float *>(sQ);                  // [64][3]   (operand tiles are free)
+            float *accs = ml + kUmmaHeads * 3;                          // [64][D]
+            // every PV has completed: no MMA reads the Q tile any more
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(tO + lane_off + 32 * c, o);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] += __shfl_xor_sync(0xFFFFFFFFu, o[j], 16);
-            if (!lo_part) {
+                for (int j = 0; j < 32; ++j) o[j] += __shfl_xor_sync(0xFFFFFFFFu, o[j], 16);
+                if (!lo_part) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) accs[hl * D + 32 * c + j] = o[j];
+                    for (int j = 0; j < 32; ++j) accs[hl * D + 32 * c + j] = o[j];
+                }
             }
+            const float l_row = lsum + __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+            if (!lo_part) {
+                ml[hl * 3] = m;
+                ml[hl * 3 + 1] = l_row;
+                ml[hl * 3 + 2] = (float)E;
+            }
+        } else {
+            *abort = 1u;
         }
-        const float l_row = lsum + __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
-        if (!lo_part) {
-            ml[hl * 3] = m;
-            ml[hl * 3 + 1] = l_row;
-            ml[hl * 3 + 2] = (float)E;
-        }
+    }
+    __syncthreads();
+    const bool failed = *abort != 0u;
+    if (failed && warp == 7 && lane == 0) {
+        // stop only after the newest MMA (and so every earlier one) completed
+        if (last_commit >= 0) mbar_wait(bars + 8 * last_commit, last_parity);
+        for (int c = max(0, issued - RING); c < issued; ++c)     // and the ring copies in flight
+            mbar_wait(ring_bars + 8 * (c % RING), (c / RING) & 1);
     }
     tc_fence_before();
-    const bool failed = __syncthreads_or(!ok);
+    __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, TCOLS);
@@ -1272,6 +1296,8 @@ decode_umma_kernel(Params P) {
         if (tid == 0) flag_error(P.status, kDevWaitTimeout);
         return;
     }
+    float *ml = reinterpret_cast<float *>(sQ);
+    float *accs = ml + kUmmaHeads * 3;
     merge_and_store<D>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
 }
 
@@ -1783,7 +1809,7 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
     if (kernel == kF32) return launch_f32<D>(P, st);
     if (kernel == kTcgen05) {
         const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
-        return launch_attn(decode_umma_kernel<D>, P, L.total, 128, st);
+        return launch_attn(decode_umma_kernel<D>, P, L.total, kUmmaThreads, st);
     }
     return (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
 }
@@ -1795,9 +1821,9 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     // (query row, head) pairs served per kv head: the rows of one sequence
     // share their kv group's K/V read like the heads of a GQA group
     const int r = a.num_rows * (a.num_heads / a.num_kv_heads);
-    // automatic: the mma.sync tensor-core family (the tcgen05 family is
-    // selectable; it does not yet beat it on any measured shape)
-    a.kernel = requested_kernel == kAuto ? kTensorCore : requested_kernel;
+    // automatic: tcgen05 when a kv head has enough (row, head) pairs to fill
+    // its CTAs (64 each); the mma.sync tensor-core family otherwise
+    a.kernel = requested_kernel != kAuto ? requested_kernel : (r >= kUmmaHeads ? kTcgen05 : kTensorCore);
     if (a.kernel == kTcgen05) {
         a.heads_per_cta = r < kUmmaHeads ? r : kUmmaHeads;
     } else if (a.kernel == kTensorCore) {
@@ -1816,7 +1842,7 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
         const int hd = a.head_size;
         const bool big_tile = hd == 256 || a.heads_per_cta > 8;
         const int per_sm = a.kernel == kF32       ? 1
-                           : a.kernel == kTcgen05 ? (hd == 64 ? 4 : hd == 128 ? 2 : 1)
+                           : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
                            : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
                                                    : (big_tile ? 1 : 3);
         const int64_t slots = (int64_t)per_sm * num_sms;

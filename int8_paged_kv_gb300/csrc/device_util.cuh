@@ -73,6 +73,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// mbar_wait that also gives up once *abort is set (by any thread of the CTA);
+// a thread whose own wait runs out of time sets it, so one stuck stage ends
+// every waiter of the CTA within one time limit.
+// Like mbar_try_wait, but the hardware may suspend the thread for up to
+// hint_ns while the phase is incomplete (fewer issue slots spent waiting).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity, volatile uint32_t *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_suspend(bar, parity, 2000u)) return true;
+        if ((i & 31u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1u;
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ bulk copies
 
 // One contiguous run of `bytes` (multiple of 16; both addresses 16-byte
@@ -165,7 +197,8 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w owns lanes 32(w%4)..).
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w owns lanes
+// 32(w%4)..); the address must be the same in every thread of the warp.
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "

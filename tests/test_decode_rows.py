@@ -135,13 +135,13 @@ def _sampled_rows_oracle(w, ok_, ov_, q, picks):
     return np.array(out)
 
 
-@pytest.mark.parametrize("kernel", [0, TC, CC, T5])
-def test_large_batch_four_rows_sampled(kernel):
-    """The large-batch workload with 4 query rows per sequence, in the
-    automatic launch plan; sampled (s, b, h) rows against the oracle."""
+@pytest.mark.parametrize("kernel,R", [(0, 4), (TC, 4), (CC, 4), (T5, 4), (0, 8)])
+def test_large_batch_many_rows_sampled(kernel, R):
+    """The large-batch workload with 4 or 8 query rows per sequence (8 rows x
+    8 heads fill the tcgen05 family's 64-pair CTAs: the automatic plan takes
+    it), sampled (s, b, h) rows against the oracle."""
     from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows
     w, ok_, ov_, kc, vc = _setup("large")
-    R = 4
     q = wl.query_rows(w, R)
     got = gpu_decode_rows(w, kc, vc, q, kernel=kernel)
     rng = np.random.default_rng(kernel)
@@ -152,7 +152,7 @@ def test_large_batch_four_rows_sampled(kernel):
     picks = sorted(picks)
     want = _sampled_rows_oracle(w, ok_, ov_, q, picks)
     sel = np.array([got[s, b, h] for s, b, h in picks])
-    assert_close(sel, want, f"large R 4 kernel {kernel}")
+    assert_close(sel, want, f"large R {R} kernel {kernel}")
     assert np.all(np.isfinite(got))
     assert device_status() == 0
 
