@@ -601,10 +601,11 @@ def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
 
 
 def run_configs(args) -> None:
-    """Decode throughput of every workload (both kernel families; 1 and 4
-    query rows per sequence on the batches that fill the GPU), one JSON line
-    per (workload, rows, family) -- a report next to the bench line, not a
-    bench line itself."""
+    """Decode throughput of every workload (single query: tensor-core and
+    CUDA-core families; 4 and 8 query rows per sequence on the batches that
+    fill the GPU: mma.sync and tcgen05 families), one JSON line per
+    (workload, rows, family) -- a report next to the bench line, not a bench
+    line itself."""
     import torch
 
     import int8_paged_kv_gb300 as pk
@@ -639,9 +640,10 @@ def run_configs(args) -> None:
         w.key = w.value = None
         # R > 1: causal decode of R query rows per sequence (pa_q8_decode_rows),
         # on the workloads whose batches fill the GPU
-        row_counts = (1, 4) if name in ("llama8b", "long", "large") else (1,)
-        for R, kernel in [(R, k) for R in row_counts
-                          for k in (pk.PA_Q8_KERNEL_TENSOR_CORE, pk.PA_Q8_KERNEL_CUDA_CORE)]:
+        runs = [(1, pk.PA_Q8_KERNEL_TENSOR_CORE), (1, pk.PA_Q8_KERNEL_CUDA_CORE)]
+        if name in ("llama8b", "long", "large"):
+            runs += [(R, k) for R in (4, 8) for k in (pk.PA_Q8_KERNEL_TENSOR_CORE, pk.PA_Q8_KERNEL_TCGEN05)]
+        for R, kernel in runs:
             nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, R)
             if R == 1:
                 plan = pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq, kernel=kernel)
@@ -676,7 +678,8 @@ def run_configs(args) -> None:
                 ts.append(a.elapsed_time(b))
             ms = float(np.median(ts))
             print(json.dumps({"kind": "decode per workload", "workload": name, "description": cfg.description,
-                              "query_rows": R, "kernel": {1: "cuda-core", 2: "tensor-core"}[kernel],
+                              "query_rows": R,
+                              "kernel": {1: "cuda-core", 2: "tensor-core", 3: "tcgen05"}[kernel],
                               "partition_tokens": plan["partition_tokens"], "ms": round(ms, 4),
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),

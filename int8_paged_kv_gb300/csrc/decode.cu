@@ -141,6 +141,7 @@ __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
 // Row of q / out (in units of head_size) of virtual head vh of the CTA's
 // group: sequence s, query row vh / r, head g * r + vh % r.
 __device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) {
+    if (P.R == 1) return (int64_t)w.s * P.H + (int64_t)w.g * P.r + vh;      // single query: no division
     const int b = vh / P.r;
     return ((int64_t)w.s * P.R + b) * P.H + (int64_t)w.g * P.r + (vh - b * P.r);
 }
@@ -149,7 +150,7 @@ __device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) 
 // first c - (R - 1 - b) tokens of the context ("attention.rs", attention_b:
 // t_len = base_pos + b + 1).
 __device__ __forceinline__ int row_len(const Params &P, const Work &w, int vh) {
-    const int cb = w.c - (P.R - 1 - vh / P.r);
+    const int cb = P.R == 1 ? w.c : w.c - (P.R - 1 - vh / P.r);
     return max(0, min(cb - w.t_begin, P.PT));
 }
 
