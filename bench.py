@@ -600,6 +600,69 @@ def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
     torch.cuda.empty_cache()
 
 
+def run_profile_rows(args) -> None:
+    """A profiler case, not a bench line: pa_q8_decode_rows with
+    --profile-rows R query rows per sequence over the large batch (its first
+    --seqs sequences when given), kernel family --kernel; prints the median
+    event time of --steps calls after --warmup."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    from int8_paged_kv_gb300 import build as pkbuild
+
+    pkbuild.build()
+    dev = torch.device("cuda", 0)
+    w = wl.build(WORKLOAD, with_append=False, with_kv=not args.seqs)
+    if args.seqs:
+        w = wl.subset(w, args.seqs)
+        key, value, slots = wl.sequence_rows(w, range(w.context_lens.size))
+    else:
+        key, value, slots = w.key, w.value, w.slot_mapping
+    cfg = w.cfg
+    S = int(w.context_lens.size)
+    H, Hk, D, B = cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    R = int(args.profile_rows)
+
+    def u32(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int32)).to(dev)
+
+    kc = torch.empty((w.num_blocks, Hk, B, D // 4 + 1), dtype=torch.int32, device=dev)
+    vc = torch.empty_like(kc)
+    for i in range(0, key.shape[0], 1 << 18):
+        pk.pa_q8_reshape_and_cache(torch.from_numpy(key[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                   torch.from_numpy(value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                   kc, vc, u32(slots[i:i + (1 << 18)]), num_kv_heads=Hk, head_size=D,
+                                   block_size=B)
+    key = value = w.key = w.value = None
+    q = torch.from_numpy(np.ascontiguousarray(wl.query_rows(w, R)[:S])).to(dev)
+    out = torch.empty_like(q)
+    bt, cl = u32(w.block_tables), u32(w.context_lens)
+    ws = torch.empty(max(16, pk.pa_q8_decode_rows_workspace_size(S, R, H, Hk, D, B, cfg.max_blocks_per_seq,
+                                                                 kernel=args.kernel,
+                                                                 partition_tokens=args.partition_tokens)),
+                     dtype=torch.uint8, device=dev)
+
+    def run():
+        pk.pa_q8_decode_rows(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale,
+                             workspace=ws, kernel=args.kernel, partition_tokens=args.partition_tokens)
+    for _ in range(max(3, args.warmup)):
+        run()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    sub = wl.Config(cfg.name, cfg.index, S, H, Hk, D, B, cfg.max_context)
+    nbytes = wl.algorithmic_decode_bytes(sub, w.context_lens, R)
+    ms = float(np.median(ts))
+    print(json.dumps({"kind": "profile case: multi-row decode", "seqs": S, "query_rows": R,
+                      "kernel": args.kernel, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                      "gbps": round(nbytes / ms / 1e6, 1), "device_status": pk.pa_q8_device_status()}))
+
+
 def run_configs(args) -> None:
     """Decode throughput of every workload (single query: tensor-core and
     CUDA-core families; 4 and 8 query rows per sequence on the batches that
@@ -700,6 +763,8 @@ def main():
                     help="print decode throughput of every workload instead of the bench line")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--profile-rows", type=int, default=0,
+                    help="profiler case: multi-row decode with this many query rows (not a bench line)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile-size case: only the first N sequences (not a bench number)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -713,6 +778,8 @@ def main():
         args.ref_step_seconds = min(4.0, max(0.05, 150.0 / (args.steps + args.warmup)))
     if args.configs:
         run_configs(args)
+    elif args.profile_rows:
+        run_profile_rows(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
