@@ -56,6 +56,8 @@ def _load():
         lib.oracle_combine.argtypes = [P, P, P, i32, i32, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i64]
         lib.oracle_decode_rows.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, f64]
+        lib.oracle_cq_append.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i64]
+        lib.oracle_cq_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, f64, P, i64]
         lib.oracle_reshape_and_cache_f32.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32]
         lib.oracle_decode_f32.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, f64, P, i64]
         _lib = lib
@@ -239,4 +241,58 @@ def decode_f32(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
     _load().oracle_decode_f32(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache),
                               _ptr(block_tables), _ptr(context_lens), S, H, num_kv_heads, D,
                               block_size, Nb, float(scale), rp, nr)
+    return out
+
+
+# -------------------------------------------------------- contiguous q8 cache
+# Per sequence: [max_t][kv_row] int8 codes (u32 words), then [max_t][kv_row/32]
+# f32 group scales; sequences back to back (see pa_q8_oracle.c).
+
+
+def cq_seq_words(max_t: int, num_kv_heads: int, head_size: int) -> int:
+    kv_row = num_kv_heads * head_size
+    return max_t * kv_row // 4 + max_t * kv_row // 32
+
+
+def cq_append(key: np.ndarray, value: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray,
+              slot_mapping: np.ndarray, *, num_kv_heads: int, head_size: int, max_t: int) -> None:
+    """Quantise rows (slot = sequence * max_t + position) into the contiguous
+    caches in place, one scale per 32-element group."""
+    T = int(slot_mapping.shape[0])
+    _need(slot_mapping, np.uint32, "slot_mapping")
+    _need(key_cache, np.uint32, "key_cache")
+    _need(value_cache, np.uint32, "value_cache")
+
+    def base_and_stride(a):
+        if a.dtype != np.float32:
+            raise TypeError("key/value must be float32")
+        if a.flags.c_contiguous:
+            return a, num_kv_heads * head_size
+        if a.ndim != 2 or a.strides[1] != 4:
+            raise ValueError("strided key/value must be 2-D views with contiguous rows")
+        return a, a.strides[0] // 4
+
+    k, ks = base_and_stride(key)
+    v, vs = base_and_stride(value)
+    _load().oracle_cq_append(ctypes.c_void_p(k.ctypes.data), ctypes.c_void_p(v.ctypes.data),
+                             _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), T, ks, vs,
+                             num_kv_heads, head_size, int(max_t))
+
+
+def cq_decode(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray, context_lens: np.ndarray, *,
+              num_kv_heads: int, max_t: int, scale: float, rows: np.ndarray | None = None) -> np.ndarray:
+    """fp64 decode over the contiguous caches: [S, H, D] or [n_rows, D]."""
+    _need(q, np.float32, "q")
+    for a, n in ((key_cache, "key_cache"), (value_cache, "value_cache"), (context_lens, "context_lens")):
+        _need(a, np.uint32, n)
+    S, H, D = q.shape
+    if rows is None:
+        out = np.empty((S, H, D), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        out = np.empty((rows.shape[0], D), dtype=np.float64)
+        rp, nr = _ptr(rows), rows.shape[0]
+    _load().oracle_cq_decode(_ptr(out), _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(context_lens),
+                             S, H, num_kv_heads, D, int(max_t), float(scale), rp, nr)
     return out

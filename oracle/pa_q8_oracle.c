@@ -27,6 +27,9 @@
  *    merge of (max, sum, weighted sum) partials by their log-sum-exp is
  *    written out in oracle_combine below.
  *
+ *  - the contiguous q8 cache with a side scale region of attention.rs
+ *    (kv_append_q8; one scale per 32-element group), its append and decode.
+ *
  *  - the f32 cache variant (paged_attn.comp, named by paged_attn_q8.comp's
  *    header comment as the same math over an f32 cache): a copy writer and
  *    the same fp64 decode over f32 values (end of this file).
@@ -369,6 +372,103 @@ void oracle_decode_f32(double *out, const float *q, const float *key_cache,
             const float *v = f32_token(value_cache, block_tables, max_blocks_per_seq, num_kv_heads,
                                        head_size, block_size, s, g, t);
             for (int d = 0; d < head_size; ++d) o[d] += p * (double)v[d];
+        }
+        for (int d = 0; d < head_size; ++d) o[d] /= l;
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * The contiguous q8 cache with a side scale region ("attention.rs",
+ * cherenkov qwen4_exp gpu: the kv_append_q8 dispatch with its parameters
+ * row = kv_row, t0, nb and scale_off = kv_q8_side(max_t, kv_row), launched as
+ * nb * (kv_row / 32) * 2 subgroups).  The shader is not on the page; the
+ * reading taken here:
+ *  - one sequence's cache: for each position t < max_t a row of
+ *    kv_row = num_kv_heads * head_size int8 codes, 4 per u32 word in
+ *    little-endian lanes (kv head major, as the rows arrive), then a side
+ *    region of f32 scales, one per 32-element group of a row (one subgroup
+ *    per group of K and of V), group j of position t at word
+ *    scale_off + t * kv_row / 32 + j, scale_off = max_t * kv_row / 4;
+ *  - a group is quantised like a token vector of the paged cache (amax over
+ *    its 32 values, codes clamp(round(x * 127/amax)), scale amax/127, 1.0
+ *    for an all-zero group);
+ *  - S sequences sit back to back, max_t * kv_row / 4 + max_t * kv_row / 32
+ *    words apart; a row's slot is s * max_t + t (0xFFFFFFFF skips it).
+ * ------------------------------------------------------------------------ */
+
+static int64_t cq_seq_words(int64_t max_t, int64_t kv_row) { return max_t * kv_row / 4 + max_t * kv_row / 32; }
+
+void oracle_cq_append(const float *key, const float *value, uint32_t *key_cache, uint32_t *value_cache,
+                      const uint32_t *slot_mapping, int64_t num_tokens, int64_t key_stride,
+                      int64_t value_stride, int num_kv_heads, int head_size, int64_t max_t)
+{
+    const int64_t kv_row = (int64_t)num_kv_heads * head_size;
+    const int64_t groups = kv_row / 32;
+    const int64_t sw = cq_seq_words(max_t, kv_row);
+    uint32_t g[9];
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        uint32_t slot = slot_mapping[i];
+        if (slot == PAD_SLOT) continue;
+        const int64_t s = slot / max_t, t = slot % max_t;
+        const int64_t codes = s * sw + t * (kv_row / 4);
+        const int64_t scales = s * sw + max_t * (kv_row / 4) + t * groups;
+        for (int64_t j = 0; j < groups; ++j) {
+            oracle_quantize_vector(key + i * key_stride + 32 * j, 32, g);
+            memcpy(key_cache + codes + 8 * j, g, 8 * sizeof(uint32_t));
+            key_cache[scales + j] = g[8];
+            oracle_quantize_vector(value + i * value_stride + 32 * j, 32, g);
+            memcpy(value_cache + codes + 8 * j, g, 8 * sizeof(uint32_t));
+            value_cache[scales + j] = g[8];
+        }
+    }
+}
+
+/* Dequantised element e (0 <= e < kv_row) of position t of sequence s. */
+static double cq_value(const uint32_t *cache, int64_t max_t, int64_t kv_row, int s, int64_t t, int64_t e)
+{
+    const int64_t base = (int64_t)s * cq_seq_words(max_t, kv_row);
+    const uint32_t word = cache[base + t * (kv_row / 4) + e / 4];
+    const double scale = (double)float_from_bits(cache[base + max_t * (kv_row / 4) + t * (kv_row / 32) + e / 32]);
+    return (double)code_at(word, (int)(e % 4)) * scale;
+}
+
+/* out[s, h, :] = softmax(scale * q[s,h] . K^T) V over positions
+ * [0, min(context_len, max_t)) of sequence s's contiguous cache, kv head
+ * g = h / (num_heads / num_kv_heads) (elements g*head_size ..); rows as in
+ * oracle_decode. */
+void oracle_cq_decode(double *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                      const uint32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                      int head_size, int64_t max_t, double scale, const int32_t *rows, int64_t n_rows)
+{
+    const int64_t kv_row = (int64_t)num_kv_heads * head_size;
+    int64_t n = rows ? n_rows : (int64_t)num_seqs * num_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        int s = rows ? rows[2 * i] : (int)(i / num_heads);
+        int h = rows ? rows[2 * i + 1] : (int)(i % num_heads);
+        int g = h / (num_heads / num_kv_heads);
+        const float *qv = q + ((int64_t)s * num_heads + h) * head_size;
+        double *o = out + i * head_size;
+        for (int d = 0; d < head_size; ++d) o[d] = 0.0;
+        int64_t c = context_lens[s];
+        if (c > max_t) c = max_t;
+        if (c == 0) continue;
+        double *z = (double *)malloc(sizeof(double) * (size_t)c);
+        double m = -INFINITY;
+        for (int64_t t = 0; t < c; ++t) {
+            double dot = 0.0;
+            for (int d = 0; d < head_size; ++d)
+                dot += (double)qv[d] * cq_value(key_cache, max_t, kv_row, s, t, (int64_t)g * head_size + d);
+            z[t] = scale * dot;
+            if (z[t] > m) m = z[t];
+        }
+        double l = 0.0;
+        for (int64_t t = 0; t < c; ++t) {
+            double p = exp(z[t] - m);
+            l += p;
+            for (int d = 0; d < head_size; ++d)
+                o[d] += p * cq_value(value_cache, max_t, kv_row, s, t, (int64_t)g * head_size + d);
         }
         for (int d = 0; d < head_size; ++d) o[d] /= l;
         free(z);
