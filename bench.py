@@ -663,6 +663,57 @@ def run_profile_rows(args) -> None:
                       "gbps": round(nbytes / ms / 1e6, 1), "device_status": pk.pa_q8_device_status()}))
 
 
+def run_contig_line(args, name, w, cl, q, flush, sink, peaks) -> None:
+    """The same contexts in the contiguous q8 cache (per-sequence code rows +
+    side scale region, max_t = the workload's largest context), appended by
+    pa_q8c_append and decoded by pa_q8c_decode."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    cfg = w.cfg
+    S, H, Hk, D = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size
+    max_t = cfg.max_context
+    dev = q.device
+    words = pk.pa_q8c_cache_words(max_t, Hk, D)
+    kc = torch.empty((S, words), dtype=torch.int32, device=dev)
+    vc = torch.empty_like(kc)
+    seq = np.repeat(np.arange(S, dtype=np.int64), w.context_lens.astype(np.int64))
+    pos = np.concatenate([np.arange(int(c), dtype=np.int64) for c in w.context_lens])
+    slots = (seq * max_t + pos).astype(np.uint32)
+    T = w.key.shape[0]
+    for i in range(0, T, 1 << 18):
+        sm = torch.from_numpy(np.ascontiguousarray(slots[i:i + (1 << 18)]).view(np.int32)).to(dev)
+        pk.pa_q8c_append(torch.from_numpy(w.key[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                         torch.from_numpy(w.value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                         kc, vc, sm, num_kv_heads=Hk, head_size=D, max_t=max_t)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(16, pk.pa_q8c_decode_workspace_size(S, H, Hk, D, max_t)), dtype=torch.uint8, device=dev)
+
+    def run():
+        pk.pa_q8c_decode(out, q, kc, vc, cl, num_kv_heads=Hk, max_t=max_t, scale=w.scale, workspace=ws)
+    for _ in range(max(3, args.warmup)):
+        torch.sum(flush, dim=0, out=sink)
+        run()
+    ts = []
+    for _ in range(args.steps):
+        torch.sum(flush, dim=0, out=sink)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = float(np.median(ts))
+    nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="q8c")
+    print(json.dumps({"kind": "decode per workload, contiguous q8 cache", "workload": name,
+                      "kernel": "tensor-core (32-element group scales)", "ms": round(ms, 4),
+                      "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
+                      "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                      "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
+    del kc, vc
+    torch.cuda.empty_cache()
+
+
 def run_configs(args) -> None:
     """Decode throughput of every workload (single query: tensor-core and
     CUDA-core families; 4 and 8 query rows per sequence on the batches that
@@ -700,6 +751,8 @@ def run_configs(args) -> None:
         bt, cl, out = u32(w.block_tables), u32(w.context_lens), torch.empty_like(q)
         if name in ("llama8b", "long", "large"):
             run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks)
+        if name in ("llama8b", "large"):
+            run_contig_line(args, name, w, cl, q, flush, sink, peaks)
         w.key = w.value = None
         # R > 1: causal decode of R query rows per sequence (pa_q8_decode_rows),
         # on the workloads whose batches fill the GPU

@@ -291,6 +291,49 @@ size_t pa_f32_decode_workspace_size(int num_seqs, int num_heads, int num_kv_head
                                     int head_size, int block_size, int max_blocks_per_seq,
                                     const pa_q8_decode_options *opts);
 
+/*
+ * ---- The contiguous q8 cache with a side scale region ----------------------
+ * "attention.rs" (cherenkov qwen4_exp gpu) appends a step's K/V rows to a
+ * per-sequence contiguous q8 cache with its kv_append_q8 dispatch (row =
+ * kv_row, t0, nb, scale_off = kv_q8_side(max_t, kv_row); nb * (kv_row/32) * 2
+ * subgroups) and attends over it.  The shader is not on the page; the layout
+ * read here, one u32 buffer per cache (K, V), sequences back to back:
+ *   sequence s at word s * pa_q8c_cache_words(max_t, num_kv_heads, head_size):
+ *     codes  [max_t][kv_row / 4] words, kv_row = num_kv_heads * head_size,
+ *            int8 code e of a row in byte e % 4 of word e / 4 (kv head major);
+ *     scales [max_t][kv_row / 32] f32 bit patterns, scale j of a row covering
+ *            codes 32j .. 32j + 31 (amax / 127 of that group, 1.0 when 0),
+ *            starting at word max_t * kv_row / 4 of the sequence (scale_off).
+ * A 32-element group is quantised like a paged token vector (same rounding,
+ * same words for the same values).
+ */
+size_t pa_q8c_cache_words(int64_t max_t, int num_kv_heads, int head_size);
+
+/* Quantise rows into the contiguous caches: row i (f32, kv_row floats, row
+ * stride key_stride / value_stride) goes to position slot % max_t of sequence
+ * slot / max_t, slot = slot_mapping[i]; 0xFFFFFFFF skips the row, slots >=
+ * num_seqs * max_t are skipped and flagged PA_Q8_DEV_BAD_SLOT.  head_size 64,
+ * 128 or 256. */
+int pa_q8c_append(const float *key, const float *value, int64_t key_stride, int64_t value_stride,
+                  uint32_t *key_cache, uint32_t *value_cache, const uint32_t *slot_mapping,
+                  int64_t num_tokens, int num_kv_heads, int head_size, int64_t max_t, int num_seqs,
+                  void *stream);
+
+/* Single-query decode over the contiguous caches: out[s, h] = softmax(scale *
+ * q[s, h] . K^T) . V over positions [0, min(context_lens[s], max_t)) of
+ * sequence s, K and V dequantised as code * group scale, kv head h / (num_heads
+ * / num_kv_heads); empty context -> zeros.  q, out [num_seqs][num_heads][head_size]
+ * f32, 16-byte aligned; caches 16-byte aligned; head_size 128 or 256 (64 is
+ * EUNSUPPORTED: its 8-byte scale rows cannot be bulk-copied).  opts: kernel
+ * AUTO or TENSOR_CORE, partition_tokens as for pa_q8_decode_ex. */
+int pa_q8c_decode(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                  const uint32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                  int head_size, int64_t max_t, float scale, void *workspace, size_t workspace_bytes,
+                  void *stream, const pa_q8_decode_options *opts);
+
+size_t pa_q8c_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                    int64_t max_t, const pa_q8_decode_options *opts);
+
 /* The launch plan pa_q8_decode_ex would use (no launch): kernel family,
  * tokens per partition, partitions per sequence (grid x), CTAs launched for
  * the attention kernel.  Any output pointer may be NULL.  Needs a current

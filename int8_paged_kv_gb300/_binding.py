@@ -67,6 +67,15 @@ def lib() -> ctypes.CDLL:
         L.pa_q8_decode_append.restype = i32
         L.pa_q8_decode_append.argtypes = ([P, P, P, P, i64, i64, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                            i32, i64, f32, P, sz, P, ctypes.POINTER(DecodeOptions)])
+        L.pa_q8c_cache_words.restype = sz
+        L.pa_q8c_cache_words.argtypes = [i64, i32, i32]
+        L.pa_q8c_append.restype = i32
+        L.pa_q8c_append.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i64, i32, P]
+        L.pa_q8c_decode.restype = i32
+        L.pa_q8c_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, f32, P, sz, P,
+                                    ctypes.POINTER(DecodeOptions)]
+        L.pa_q8c_decode_workspace_size.restype = sz
+        L.pa_q8c_decode_workspace_size.argtypes = [i32, i32, i32, i32, i64, ctypes.POINTER(DecodeOptions)]
         L.pa_f32_reshape_and_cache.restype = i32
         L.pa_f32_reshape_and_cache.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32, i64, P]
         L.pa_f32_decode.restype = i32
@@ -349,6 +358,56 @@ def pa_f32_decode(out, q, key_cache, value_cache, block_tables, context_lens, *,
     return out
 
 
+def pa_q8c_cache_words(max_t: int, num_kv_heads: int, head_size: int) -> int:
+    return int(lib().pa_q8c_cache_words(int(max_t), int(num_kv_heads), int(head_size)))
+
+
+def pa_q8c_append(key, value, key_cache, value_cache, slot_mapping, *, num_kv_heads: int, head_size: int,
+                  max_t: int, num_seqs: int | None = None, stream=None) -> None:
+    """Quantise rows into the contiguous caches (u32 [num_seqs, cache_words]);
+    slot = sequence * max_t + position (see include/pa_q8.h)."""
+    import torch
+    T = int(slot_mapping.numel())
+    if key.dim() != 2 or value.dim() != 2 or key.stride(1) != 1 or value.stride(1) != 1:
+        raise ValueError("key/value must be 2-D [num_tokens, >= num_kv_heads * head_size] with unit column stride")
+    ns = int(key_cache.shape[0]) if num_seqs is None else int(num_seqs)
+    rc = lib().pa_q8c_append(
+        _cuda(key, torch.float32, "key"), _cuda(value, torch.float32, "value"), int(key.stride(0)),
+        int(value.stride(0)), _cuda(key_cache, torch.uint32, "key_cache"),
+        _cuda(value_cache, torch.uint32, "value_cache"), _cuda(slot_mapping, torch.uint32, "slot_mapping"), T,
+        int(num_kv_heads), int(head_size), int(max_t), ns, _stream(stream))
+    _check("pa_q8c_append", rc)
+
+
+def pa_q8c_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_t, *,
+                                 partition_tokens: int = 0) -> int:
+    return int(lib().pa_q8c_decode_workspace_size(int(num_seqs), int(num_heads), int(num_kv_heads),
+                                                  int(head_size), int(max_t), _opts(0, partition_tokens)))
+
+
+def pa_q8c_decode(out, q, key_cache, value_cache, context_lens, *, num_kv_heads: int, max_t: int,
+                  scale: float, workspace=None, partition_tokens: int = 0, stream=None):
+    """out[S, H, D] = decode over the contiguous caches.  Returns `out`."""
+    import torch
+    S, H, D = q.shape
+    if out.shape != q.shape or not out.is_contiguous() or not q.is_contiguous():
+        raise ValueError("q and out must be contiguous [num_seqs, num_heads, head_size]")
+    if context_lens.numel() != S:
+        raise ValueError("context_lens does not match num_seqs")
+    need = pa_q8c_decode_workspace_size(S, H, num_kv_heads, D, max_t, partition_tokens=partition_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pa_q8c_decode(
+        _cuda(out, torch.float32, "out"), _cuda(q, torch.float32, "q"),
+        _cuda(key_cache, torch.uint32, "key_cache"), _cuda(value_cache, torch.uint32, "value_cache"),
+        _cuda(context_lens, torch.uint32, "context_lens"), S, H, int(num_kv_heads), D, int(max_t), float(scale),
+        ws_ptr, ws_bytes, _stream(stream), _opts(0, partition_tokens))
+    _check("pa_q8c_decode", rc)
+    return out
+
+
 def pa_q8_device_status(clear: bool = True, stream=None) -> int:
     bits = ctypes.c_uint32()
     _check("pa_q8_device_status", lib().pa_q8_device_status(ctypes.byref(bits), int(bool(clear)),
@@ -366,4 +425,4 @@ def header_functions() -> list[str]:
     import re
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_(?:q8|f32)_[a-z0-9_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pa_(?:q8c?|f32)_[a-z0-9_]+)\s*\(", text)))

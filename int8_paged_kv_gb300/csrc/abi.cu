@@ -293,6 +293,110 @@ size_t pa_f32_decode_workspace_size(int num_seqs, int num_heads, int num_kv_head
                           true);
 }
 
+size_t pa_q8c_cache_words(int64_t max_t, int num_kv_heads, int head_size) {
+    if (max_t <= 0 || num_kv_heads <= 0 || head_size <= 0 || head_size % 32 != 0) return 0;
+    const int64_t kv_row = (int64_t)num_kv_heads * head_size;
+    return (size_t)(max_t * (kv_row / 4) + max_t * (kv_row / 32));
+}
+
+int pa_q8c_append(const float *key, const float *value, int64_t key_stride, int64_t value_stride,
+                  uint32_t *key_cache, uint32_t *value_cache, const uint32_t *slot_mapping, int64_t num_tokens,
+                  int num_kv_heads, int head_size, int64_t max_t, int num_seqs, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || max_t <= 0 || num_seqs <= 0) return PA_Q8_EINVAL;
+    if (head_size % 32 != 0) return PA_Q8_EINVAL;
+    if (!head_size_ok(head_size)) return PA_Q8_EUNSUPPORTED;
+    const int64_t kv_row = (int64_t)num_kv_heads * head_size;
+    if (key_stride < kv_row || value_stride < kv_row) return PA_Q8_EINVAL;
+    if ((int64_t)num_seqs * max_t > (int64_t)0xFFFFFFFFu || kv_row / 64 > 65535) return PA_Q8_EUNSUPPORTED;
+    if (num_tokens == 0) return PA_Q8_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return PA_Q8_EINVAL;
+    if (!aligned4(key) || !aligned4(value) || !aligned4(key_cache) || !aligned4(value_cache) ||
+        !aligned4(slot_mapping))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int rc = device_info(&status, nullptr);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::WriterArgs a{key, value, key_cache, value_cache, slot_mapping, num_tokens, key_stride,
+                        value_stride, num_kv_heads, head_size, 1, num_seqs, status};
+    if (pa_q8::launch_cq_append(a, max_t, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
+namespace {
+
+int cq_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || max_t <= 0) return PA_Q8_EINVAL;
+    if (num_heads % num_kv_heads != 0 || head_size % 32 != 0) return PA_Q8_EINVAL;
+    if (head_size != 128 && head_size != 256) return PA_Q8_EUNSUPPORTED;
+    if (num_seqs > 65535 || (int64_t)num_kv_heads * (num_heads / num_kv_heads) > 65535) return PA_Q8_EUNSUPPORTED;
+    if (max_t > (int64_t)1 << 30) return PA_Q8_EUNSUPPORTED;
+    return PA_Q8_OK;
+}
+
+void cq_fill(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, 1, (int)max_t);
+    a.contiguous = 1;
+}
+
+int cq_plan(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int sms) {
+    pa_q8_decode_options o = opts ? *opts : pa_q8_decode_options{};
+    if (o.kernel != PA_Q8_KERNEL_AUTO && o.kernel != PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
+    o.kernel = PA_Q8_KERNEL_TENSOR_CORE;
+    return plan_for(a, &o, sms);
+}
+
+}  // namespace
+
+size_t pa_q8c_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t,
+                                    const pa_q8_decode_options *opts) {
+    if (cq_shape(num_seqs, num_heads, num_kv_heads, head_size, max_t) != PA_Q8_OK) return 0;
+    pa_q8::DecodeArgs a;
+    cq_fill(a, num_seqs, num_heads, num_kv_heads, head_size, max_t);
+    int sms = 0;
+    if (device_info(nullptr, &sms) != PA_Q8_OK) sms = 152;
+    if (cq_plan(a, opts, sms) != PA_Q8_OK) return 0;
+    return pa_q8::plan_workspace_bytes(a);
+}
+
+int pa_q8c_decode(float *out, const float *q, const uint32_t *key_cache, const uint32_t *value_cache,
+                  const uint32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                  int64_t max_t, float scale, void *workspace, size_t workspace_bytes, void *stream,
+                  const pa_q8_decode_options *opts) {
+    int rc = cq_shape(num_seqs, num_heads, num_kv_heads, head_size, max_t);
+    if (rc != PA_Q8_OK) return rc;
+    if (!out || !q || !key_cache || !value_cache || !context_lens) return PA_Q8_EINVAL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache) || !aligned4(context_lens))
+        return PA_Q8_EALIGN;
+    uint32_t *status = nullptr;
+    int sms = 0;
+    rc = device_info(&status, &sms);
+    if (rc != PA_Q8_OK) return rc;
+    pa_q8::DecodeArgs a;
+    cq_fill(a, num_seqs, num_heads, num_kv_heads, head_size, max_t);
+    rc = cq_plan(a, opts, sms);
+    if (rc != PA_Q8_OK) return rc;
+    const size_t need = pa_q8::plan_workspace_bytes(a);
+    if (!workspace || workspace_bytes < need) return PA_Q8_EWORKSPACE;
+    if (!aligned16(workspace)) return PA_Q8_EALIGN;
+    pa_q8::plan_workspace_layout(a, workspace);
+    a.out = out;
+    a.q = q;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.context_lens = context_lens;
+    a.num_blocks = num_seqs;
+    a.scale = scale;
+    a.status = status;
+    if (pa_q8::launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return PA_Q8_ECUDA;
+    }
+    return PA_Q8_OK;
+}
+
 size_t pa_q8_decode_rows_workspace_size(int num_seqs, int num_rows, int num_heads, int num_kv_heads,
                                         int head_size, int block_size, int max_blocks_per_seq,
                                         const pa_q8_decode_options *opts) {

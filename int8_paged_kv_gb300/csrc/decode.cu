@@ -101,6 +101,7 @@ struct Params {
     int64_t nk_stride, nv_stride;
     uint32_t *kc_w;         // the caches, written by the append
     uint32_t *vc_w;
+    int contiguous;         // contiguous q8 cache (decode_cq_kernel)
 };
 
 // Which CTA this is and the token range it owns.  The CTA serves virtual
@@ -901,6 +902,309 @@ decode_cc_kernel(Params P) {
     merge_and_store<D>(P, w, ml, accs, kCcSlots, NH, accs + kCcSlots * NH * D);
 }
 
+// ================================================= contiguous q8 cache
+//
+// The contiguous cache with a side scale region ("attention.rs": the
+// kv_append_q8 dispatch and kv_q8_side): per sequence, [max_t][kv_row] int8
+// codes (u32 words, kv_row = Hk * D) then [max_t][kv_row / 32] f32 scales,
+// one per 32-element group; sequences back to back.  P.Nb holds max_t (and
+// P.B = 1): position t of sequence s is token t, no block table.
+//
+// The tensor-core tile of decode_tc_kernel with three changes:
+//  - lane = token: each lane bulk-copies its token's K and V code rows (D
+//    bytes) and scale rows (D / 8 bytes) of kv head g into the chunk buffer;
+//    code rows sit WC = D/4 + 4 words apart (16-byte rows, WC = 4 mod 32);
+//  - the word maps kword = 4 ks + cq and vword = n + 8 jj are bank-conflict
+//    free at that stride, and keep each k-step of QK and each 4 n-tiles of PV
+//    inside one 32-element group;
+//  - QK accumulates each group separately and adds it times the token's
+//    group scale; PV weights are p * v_scale[token][group] per group.
+
+template <int D>
+__host__ __device__ constexpr int cq_wc() { return D / 4 + 4; }
+
+template <int D>
+__host__ __device__ constexpr uint32_t cq_slot_bytes() {
+    return 2u * (kChunk * cq_wc<D>() * 4u + kChunk * (D / 32) * 4u);
+}
+
+constexpr int kCqRing = 2;
+
+// [barriers] [q fragments (head size 256)] [chunk buffers: slot x ring]
+struct CqLayout {
+    uint32_t extra, ring, total;
+};
+
+template <int D>
+__host__ __device__ inline CqLayout make_cq_layout() {
+    CqLayout L{};
+    L.extra = align_up(PA_Q8_TC_SLOTS * kCqRing * 8, 128);
+    L.ring = align_up(L.extra + (D == 256 ? (uint32_t)(D / 16) * 32 * 16 : 0u), 128);
+    L.total = L.ring + PA_Q8_TC_SLOTS * kCqRing * cq_slot_bytes<D>();
+    return L;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_cq_chunk(const Params &P, const Work &w, int c, uint32_t slot, uint32_t bar,
+                                               uint64_t policy) {
+    constexpr int WC = cq_wc<D>();
+    constexpr uint32_t CODES = kChunk * WC * 4u, SCALES = kChunk * (D / 32) * 4u;
+    const int lane = threadIdx.x & 31;
+    const int t = c * kChunk + lane;                      // partition-relative token
+    const int n = min(kChunk, w.len - c * kChunk);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n * 2u * (D + D / 8));
+    __syncwarp();
+    if (t < w.len) {
+        fence_proxy_async_smem();
+        const int64_t kv_row = (int64_t)P.Hk * D, max_t = P.Nb;
+        const int64_t seq_words = max_t * (kv_row / 4) + max_t * (kv_row / 32);
+        const int64_t pos = (int64_t)w.t_begin + t;
+        const int64_t code = (int64_t)w.s * seq_words + pos * (kv_row / 4) + (int64_t)w.g * (D / 4);
+        const int64_t scale = (int64_t)w.s * seq_words + max_t * (kv_row / 4) + pos * (kv_row / 32) +
+                              (int64_t)w.g * (D / 32);
+        bulk_copy_g2s(slot + lane * WC * 4, P.kc + code, D, bar, policy);
+        bulk_copy_g2s(slot + CODES + lane * (D / 8), P.kc + scale, D / 8, bar, policy);
+        bulk_copy_g2s(slot + CODES + SCALES + lane * WC * 4, P.vc + code, D, bar, policy);
+        bulk_copy_g2s(slot + 2 * CODES + SCALES + lane * (D / 8), P.vc + scale, D / 8, bar, policy);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(PA_Q8_TC_SLOTS * 32, 2)
+decode_cq_kernel(Params P) {
+    constexpr int SLOTS = PA_Q8_TC_SLOTS;
+    constexpr int RING = kCqRing;
+    constexpr int WC = cq_wc<D>();
+    constexpr int G = D / 32;            // scale groups per row
+    constexpr int NKS = D / 16;
+    constexpr int NT = D / 8;
+    constexpr int NJ = D / 32;
+    constexpr bool kQInSmem = (D == 256);
+    constexpr uint32_t CODES = kChunk * WC * 4u, SCALES = kChunk * G * 4u;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    Work w;
+    if (!setup_work(P, w)) {
+        write_zero_rows<D>(P, w);
+        return;
+    }
+    const CqLayout L = make_cq_layout<D>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ts = warp;
+    const int gq = lane >> 2, cq = lane & 3;
+    const uint32_t bars = smem_addr(smem) + 8 * RING * ts;
+    const uint32_t ring = smem_addr(smem + L.ring) + RING * cq_slot_bytes<D>() * ts;
+    const int nchunks = (w.len + kChunk - 1) / kChunk;
+    const int my_n = ts < nchunks ? (nchunks - ts + SLOTS - 1) / SLOTS : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    if (lane == 0) {
+        for (int k = 0; k < RING; ++k) mbar_init(bars + 8 * k, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int issued = 0;
+    for (; issued < RING && issued < my_n; ++issued)
+        issue_cq_chunk<D>(P, w, ts + SLOTS * issued, ring + issued * cq_slot_bytes<D>(), bars + 8 * issued, policy);
+
+    const bool row_ok = gq < w.nh;
+    const int vh = w.h0 + gq;
+    const int len_row = row_ok ? row_len(P, w, vh) : w.len;
+    const int len_min = __reduce_min_sync(0xFFFFFFFFu, (unsigned)len_row);
+
+    uint32_t aq[kQInSmem ? 1 : NKS][4];
+    uint4 *qf = reinterpret_cast<uint4 *>(smem + L.extra);           // [NKS][32]
+    float qk2;
+    {
+        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
+        float mx = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+            const float4 v = row_ok ? __ldg(qv + 4 * ks + cq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
+        qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+            const float4 v = row_ok ? __ldg(qv + 4 * ks + cq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            uint32_t f0, f1, f2, f3;
+            split_f16x2(v.x * down, v.y * down, f0, f1);
+            split_f16x2(v.z * down, v.w * down, f2, f3);
+            if constexpr (kQInSmem) {
+                if (ts == 0) qf[ks * 32 + lane] = make_uint4(f0, f1, f2, f3);
+            } else {
+                aq[ks][0] = f0; aq[ks][1] = f1; aq[ks][2] = f2; aq[ks][3] = f3;
+            }
+        }
+        if constexpr (kQInSmem) __syncthreads();
+    }
+
+    float acc[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    float m = -INFINITY, lsum = 0.0f;
+    int E = 12;
+    float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+    const F16Consts fk;
+
+    bool ok = true;
+    int i = 0;
+    for (; i < my_n; ++i) {
+        const int k = i % RING;
+        if (!mbar_wait(bars + 8 * k, (i / RING) & 1)) {
+            if (lane == 0) flag_error(P.status, kDevWaitTimeout);
+            ok = false;
+            break;
+        }
+        const uint8_t *base = smem + L.ring + (RING * ts + k) * cq_slot_bytes<D>();
+        const uint32_t *sK = reinterpret_cast<const uint32_t *>(base);
+        const float *sKs = reinterpret_cast<const float *>(base + CODES);
+        const uint32_t *sV = reinterpret_cast<const uint32_t *>(base + CODES + SCALES);
+        const float *sVs = reinterpret_cast<const float *>(base + 2 * CODES + SCALES);
+        const int t0 = (ts + SLOTS * i) * kChunk;
+        const bool full = t0 + kChunk <= len_min;
+
+        // ---- S = sum over groups of (Q_g K_g^T) x the tokens' group scales
+        float s[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.0f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float sg[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sg[j][0] = sg[j][1] = sg[j][2] = sg[j][3] = 0.0f;
+#pragma unroll
+            for (int kh = 0; kh < 2; ++kh) {
+                const int ks = 2 * g + kh;
+                uint32_t a[4];
+                if constexpr (kQInSmem) {
+                    const uint4 f = qf[ks * 32 + lane];
+                    a[0] = f.x; a[1] = f.y; a[2] = f.z; a[3] = f.w;
+                } else {
+                    a[0] = aq[ks][0]; a[1] = aq[ks][1]; a[2] = aq[ks][2]; a[3] = aq[ks][3];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t b0, b1;
+                    codes4_to_f16x2(sK[(8 * j + gq) * WC + 4 * ks + cq], b0, b1, fk);
+                    mma_16816(sg[j], a, b0, b1);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float k0 = sKs[(8 * j + 2 * cq) * G + g], k1 = sKs[(8 * j + 2 * cq + 1) * G + g];
+                s[j][0] = fmaf(sg[j][0], k0, s[j][0]);
+                s[j][1] = fmaf(sg[j][1], k1, s[j][1]);
+                s[j][2] = fmaf(sg[j][2], k0, s[j][2]);
+                s[j][3] = fmaf(sg[j][3], k1, s[j][3]);
+            }
+        }
+        // ---- online softmax over this thread's 8 tokens: 8j + 2cq + e
+        float z[8];
+        float cmax = -INFINITY, vmax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = 8 * j + 2 * cq + e;
+                float zz = (s[j][e] + s[j][e + 2]) * qk2;
+                float vv = 0.0f;
+#pragma unroll
+                for (int g = 0; g < G; ++g) vv = fmaxf(vv, sVs[t * G + g]);
+                if (!full) {
+                    const bool valid = t0 + t < len_row;
+                    zz = valid ? zz : -INFINITY;
+                    vv = valid ? vv : 0.0f;
+                }
+                z[2 * j + e] = zz;
+                cmax = fmaxf(cmax, zz);
+                vmax = fmaxf(vmax, vv);
+            }
+        }
+        cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 1));
+        cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 2));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 2));
+        const int Ec = (int)(__float_as_uint(vmax) >> 23);
+        if (__any_sync(0xFFFFFFFFu, cmax > m + (float)kLazy || Ec > E)) {
+            const float m_new = fmaxf(m, cmax);
+            const int E_new = max(E, Ec);
+            const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+            const float ea = (E - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - E_new) << 23);
+            const float fa = alpha * ea;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                acc[n][0] *= fa; acc[n][1] *= fa; acc[n][2] *= fa; acc[n][3] *= fa;
+            }
+            lsum *= alpha;
+            m = m_new;
+            E = E_new;
+            wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+        }
+        const float m_ref = m == -INFINITY ? 0.0f : m;
+        float p[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            p[u] = fast_exp2(z[u] - m_ref);                  // masked tokens: 2^-inf = 0
+            lsum += p[u];
+            p[u] *= wscale;
+        }
+        // ---- O += P V, per scale group (its 4 n-tiles), two k-steps of 16 tokens
+#pragma unroll
+        for (int jj = 0; jj < NJ; ++jj) {
+            const int wd = gq + 8 * jj;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                float pw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int t = 16 * kk + 2 * cq + (u & 1) + 8 * (u >> 1);   // tokens of p[4kk + u]
+                    const bool valid = full || t0 + t < len_row;
+                    pw[u] = valid ? p[4 * kk + u] * sVs[t * G + jj] : 0.0f;
+                }
+                uint32_t ap[4];
+                split_f16x2(pw[0], pw[1], ap[0], ap[1]);
+                split_f16x2(pw[2], pw[3], ap[2], ap[3]);
+                const uint32_t *r0 = sV + (16 * kk + 2 * cq) * WC;
+                const uint32_t x0 = r0[wd], x1 = r0[WC + wd], x8 = r0[8 * WC + wd], x9 = r0[9 * WC + wd];
+                mma_16816(acc[4 * jj + 0], ap, codes_pair_to_f16x2<0>(x0, x1, fk), codes_pair_to_f16x2<0>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 1], ap, codes_pair_to_f16x2<1>(x0, x1, fk), codes_pair_to_f16x2<1>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 2], ap, codes_pair_to_f16x2<2>(x0, x1, fk), codes_pair_to_f16x2<2>(x8, x9, fk));
+                mma_16816(acc[4 * jj + 3], ap, codes_pair_to_f16x2<3>(x0, x1, fk), codes_pair_to_f16x2<3>(x8, x9, fk));
+            }
+        }
+        __syncwarp();
+        if (issued < my_n) {
+            issue_cq_chunk<D>(P, w, ts + SLOTS * issued, ring + k * cq_slot_bytes<D>(), bars + 8 * k, policy);
+            ++issued;
+        }
+    }
+    drain(P, bars, RING, i, issued);
+
+    if (__syncthreads_or(!ok)) return;
+    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
+    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+    float *ml = reinterpret_cast<float *>(smem + L.ring);            // [slot][8][3]
+    float *accs = ml + SLOTS * 8 * 3;                                 // [slot][8][D]
+    if (cq == 0) {
+        float *e = ml + (ts * 8 + gq) * 3;
+        e[0] = m; e[1] = lsum; e[2] = (float)E;
+    }
+    float *arow = accs + (ts * 8 + gq) * D;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        // acc[n]: columns 2cq, 2cq+1 of n-tile n = dims 4 (vword(2cq / 2cq+1)) + (n & 3)
+        arow[4 * (2 * cq + 8 * (n >> 2)) + (n & 3)] = acc[n][0] + acc[n][2];
+        arow[4 * (2 * cq + 1 + 8 * (n >> 2)) + (n & 3)] = acc[n][1] + acc[n][3];
+    }
+    __syncthreads();
+    merge_and_store<D>(P, w, ml, accs, SLOTS, 8, accs + SLOTS * 8 * D);
+}
+
 // ======================================================== tcgen05 (multi-row)
 //
 // Many virtual heads per kv head (multi-row decode: R query rows x r heads)
@@ -1672,6 +1976,7 @@ Params make_params(const DecodeArgs &a) {
     P.order = a.order; P.counters = a.counters; P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
     P.nk = a.new_key; P.nv = a.new_value;
     P.nk_stride = a.new_key_stride; P.nv_stride = a.new_value_stride;
+    P.contiguous = a.contiguous;
     P.kc_w = const_cast<uint32_t *>(a.key_cache);      // written only by the fused append
     P.vc_w = const_cast<uint32_t *>(a.value_cache);
     return P;
@@ -1808,6 +2113,14 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     if (kernel == kF32) return launch_f32<D>(P, st);
+    if (P.contiguous) {
+        if constexpr (D == 64) {
+            return cudaErrorInvalidValue;                 // head sizes 128 and 256 only
+        } else {
+            const CqLayout L = make_cq_layout<D>();
+            return launch_attn(decode_cq_kernel<D>, P, L.total, PA_Q8_TC_SLOTS * 32, st);
+        }
+    }
     if (kernel == kTcgen05) {
         const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
         return launch_attn(decode_umma_kernel<D>, P, L.total, kUmmaThreads, st);
@@ -1827,6 +2140,8 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     a.kernel = requested_kernel != kAuto ? requested_kernel : (r >= kUmmaHeads ? kTcgen05 : kTensorCore);
     if (a.kernel == kTcgen05) {
         a.heads_per_cta = r < kUmmaHeads ? r : kUmmaHeads;
+    } else if (a.kernel == kTensorCore && a.contiguous) {
+        a.heads_per_cta = r < 8 ? r : 8;                  // the contiguous-cache kernel: one head tile
     } else if (a.kernel == kTensorCore) {
         const int cap = a.head_size == 256 ? 16 : PA_Q8_TC_MAX_HEADS;
         a.heads_per_cta = r < cap ? r : cap;
@@ -1842,7 +2157,8 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
         // CTAs resident per SM for this kernel configuration
         const int hd = a.head_size;
         const bool big_tile = hd == 256 || a.heads_per_cta > 8;
-        const int per_sm = a.kernel == kF32       ? 1
+        const int per_sm = a.contiguous          ? (hd == 256 ? 1 : 2)
+                           : a.kernel == kF32       ? 1
                            : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
                            : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
                                                    : (big_tile ? 1 : 3);

@@ -25,6 +25,9 @@ struct WriterArgs {
 };
 
 cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream);
+// The contiguous q8 cache's append (per-sequence code rows + side scale
+// region, 32-element groups); a.num_blocks holds the number of sequences.
+cudaError_t launch_cq_append(const WriterArgs &a, int64_t max_t, cudaStream_t stream);
 // The f32 cache's writer: key_cache / value_cache hold f32 [blocks][Hk][B][D].
 cudaError_t launch_writer_f32(const WriterArgs &a, cudaStream_t stream);
 
@@ -70,6 +73,9 @@ struct DecodeArgs {
     const float *new_value;
     int64_t new_key_stride;
     int64_t new_value_stride;
+    // contiguous q8 cache (per sequence: code rows, then group scales); then
+    // block_size = 1, max_blocks_per_seq = max_t and block_tables is unused
+    int contiguous;
 };
 
 struct DecodePlanLimits {

@@ -121,6 +121,49 @@ cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ----------------------------------------------------- contiguous q8 cache
+//
+// The contiguous cache with a side scale region ("attention.rs", the
+// kv_append_q8 dispatch): per sequence, [max_t][kv_row] int8 codes (4 per
+// u32 word, kv_row = num_kv_heads * head_size) then [max_t][kv_row / 32] f32
+// scales, one per 32-element group; sequences back to back.  A row's slot is
+// sequence * max_t + position (0xFFFFFFFF skips it).  One warp per (token,
+// pair of groups): vectors K(g0), V(g0), K(g1), V(g1), eight lanes each, one
+// word per lane -- the paged writer's arithmetic on 32-value groups.
+template <bool kVec>
+__global__ void __launch_bounds__(kWriterWarps * 32)
+cq_append_kernel(const float *__restrict__ key, const float *__restrict__ value,
+                 uint32_t *__restrict__ key_cache, uint32_t *__restrict__ value_cache,
+                 const uint32_t *__restrict__ slot_mapping, int num_tokens, int64_t key_stride,
+                 int64_t value_stride, int kv_row, int64_t max_t, int64_t num_slots, uint32_t *status) {
+    const int lane = threadIdx.x & 31;
+    const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
+    if (tok >= num_tokens) return;
+    const int v = lane / kLanesPerVector, j = lane % kLanesPerVector;
+    const bool is_v = v & 1;
+    const int groups = kv_row / 32;
+    const int grp = 2 * blockIdx.y + (v >> 1);
+    const bool live = grp < groups;
+    const float *src = (is_v ? value + (int64_t)tok * value_stride : key + (int64_t)tok * key_stride) + 32 * grp + 4 * j;
+    const float4 x = live ? load4<kVec>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t slot = __ldg(slot_mapping + tok);
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+    for (int o = kLanesPerVector / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
+    const float scale = m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f;
+    if (slot == kPadSlot || !live) return;
+    if ((int64_t)slot >= num_slots) {
+        if (lane == 0) flag_error(status, kDevBadSlot);
+        return;
+    }
+    const int64_t s = slot / max_t, t = slot - s * max_t;
+    const int64_t base = s * (max_t * (kv_row / 4) + max_t * groups);
+    uint32_t *cache = is_v ? value_cache : key_cache;
+    cache[base + t * (kv_row / 4) + 8 * grp + j] = pack_word(x, inv);
+    if (j == 0) cache[base + max_t * (kv_row / 4) + t * groups + grp] = __float_as_uint(scale);
+}
+
 // ------------------------------------------------------------ f32 cache
 //
 // The f32 cache's writer: each (token, kv head) K and V vector is copied to
@@ -200,6 +243,27 @@ cudaError_t launch_writer(const WriterArgs &a, cudaStream_t stream) {
         case 256: return launch_d<256>(a, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_cq_append(const WriterArgs &a, int64_t max_t, cudaStream_t stream) {
+    const int kv_row = a.num_kv_heads * a.head_size;
+    const int64_t group_pairs = (kv_row / 32 + 1) / 2;
+    if (a.num_tokens > 0x7FFFFFFF - kWriterWarps || group_pairs > 65535 || kv_row % 32 != 0)
+        return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((a.num_tokens + kWriterWarps - 1) / kWriterWarps), (unsigned)group_pairs);
+    const bool vec = ((reinterpret_cast<uintptr_t>(a.key) | reinterpret_cast<uintptr_t>(a.value)) & 15u) == 0 &&
+                     (a.key_stride % 4) == 0 && (a.value_stride % 4) == 0;
+    const int64_t num_slots = a.num_blocks * max_t;        // num_blocks carries the sequence count
+    if (vec) {
+        cq_append_kernel<true><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens, a.key_stride,
+            a.value_stride, kv_row, max_t, num_slots, a.status);
+    } else {
+        cq_append_kernel<false><<<grid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens, a.key_stride,
+            a.value_stride, kv_row, max_t, num_slots, a.status);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_writer_f32(const WriterArgs &a, cudaStream_t stream) {

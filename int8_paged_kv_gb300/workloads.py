@@ -350,11 +350,12 @@ def algorithmic_decode_bytes(cfg: Config, context_lens: np.ndarray, num_rows: in
                              cache: str = "q8") -> int:
     """Bytes a decode must move: every context token's K and V vector once
     (q8: head_size code bytes + a 4-byte scale word each; f32: 4 * head_size
-    bytes), q in, out back (one vector per query row and head), the
+    bytes; q8c, the contiguous cache: head_size code bytes + one 4-byte scale
+    per 32 codes), q in, out back (one vector per query row and head), the
     block-table entries walked and the context lengths."""
     c = np.minimum(context_lens.astype(np.int64), cfg.max_blocks_per_seq * cfg.block_size)
     S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
-    vec = {"q8": D + 4, "f32": 4 * D}[cache]
+    vec = {"q8": D + 4, "f32": 4 * D, "q8c": D + D // 8}[cache]
     kv = int(c.sum()) * Hk * 2 * vec
     qo = 2 * S * int(num_rows) * H * D * 4
     bt = int((-(-c // B)).sum()) * 4

@@ -90,3 +90,17 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _binding.lib()
+
+
+def test_contiguous_cache_shape_checks_without_a_device(L):
+    import int8_paged_kv_gb300 as pk
+    assert pk.pa_q8c_cache_words(100, 2, 128) == 100 * 256 // 4 + 100 * 256 // 32
+    assert pk.pa_q8c_cache_words(100, 2, 100) == 0
+    # head size 64: refused on the host (8-byte scale rows cannot be bulk-copied)
+    rc = L.pa_q8c_decode(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 2, 8, 2, 64, 100, ctypes.c_float(0.1),
+                         None, 0, None, None)
+    assert rc == -2
+    assert L.pa_q8c_decode(ALIGNED, ALIGNED, ALIGNED, ALIGNED, ALIGNED, 2, 8, 3, 128, 100, ctypes.c_float(0.1),
+                           None, 0, None, None) == -1
+    assert pk.pa_q8c_decode_workspace_size(4, 8, 2, 128, 4096) > 0
+    assert pk.pa_q8c_decode_workspace_size(4, 8, 2, 64, 4096) == 0
