@@ -2493,6 +2493,16 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     const int64_t np = (max_ctx + pt - 1) / pt;
     if (np > 0x7FFFFFFF || np < 1) return false;
     a.num_partitions = (int)np;
+    {
+        const int hd = a.head_size;
+        const bool big_tile = hd == 256 || a.heads_per_cta > 8;
+        const int per_sm = a.contiguous          ? (hd == 256 ? 1 : 2)
+                           : a.kernel == kF32       ? 1
+                           : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
+                           : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
+                                                   : (big_tile ? 1 : 3);
+        a.one_wave = np == 1 && (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups <= (int64_t)per_sm * num_sms;
+    }
     return true;
 }
 
@@ -2528,7 +2538,8 @@ int64_t plan_num_ctas(const DecodeArgs &a) {
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
-    const Params P = make_params(a);
+    Params P = make_params(a);
+    if (a.one_wave) P.order = nullptr;       // every CTA starts at once: no order, no prep kernel
     switch (a.head_size) {
         case 64: return launch_d<64>(P, a.kernel, stream);
         case 128: return launch_d<128>(P, a.kernel, stream);

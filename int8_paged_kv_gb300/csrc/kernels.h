@@ -57,6 +57,8 @@ struct DecodeArgs {
     int num_partitions;    // partitions per sequence (grid x)
     int heads_per_cta;     // query heads one CTA serves (one kv head's group, or part of it)
     int head_groups;       // CTAs per (seq, kv head, partition) along the group
+    int one_wave;          // one partition per context and every CTA resident at once: no
+                           // ordering and no combine counters, so no prep kernel
     // workspace: sequence order [S] (u64: clamped length << 32 | sequence,
     // longest context first); when
     // partitions > 1 also arrival counters [S][Hk * head_groups] (u32),
