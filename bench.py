@@ -584,6 +584,7 @@ def run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks) -> No
             ts.append(a.elapsed_time(b))
         ms = float(np.median(ts))
         print(json.dumps({"kind": "decode step with append", "workload": name, "step": label,
+                          "cpu_oracle_gbps": args.oracle_rates["append"],
                           "new_tokens": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                           "gbps": round(nbytes / ms / 1e6, 1),
                           "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1)}),
@@ -628,6 +629,7 @@ def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
     ms = float(np.median(ts))
     nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="f32")
     print(json.dumps({"kind": "decode per workload, f32 cache", "workload": name, "kernel": "f32 cuda-core",
+                      "cpu_oracle_gbps": args.oracle_rates["f32"],
                       "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
                       "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
@@ -741,12 +743,148 @@ def run_contig_line(args, name, w, cl, q, flush, sink, peaks) -> None:
     ms = float(np.median(ts))
     nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="q8c")
     print(json.dumps({"kind": "decode per workload, contiguous q8 cache", "workload": name,
+                      "cpu_oracle_gbps": args.oracle_rates["contig"],
                       "kernel": "tensor-core (32-element group scales)", "ms": round(ms, 4),
                       "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
                       "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
     del kc, vc
     torch.cuda.empty_cache()
+
+
+def run_profile_variant(args) -> None:
+    """A profiler case, not a bench line: the f32-cache decode (--profile-f32)
+    or the contiguous-cache decode (--profile-contig) over the large batch's
+    contexts (its first --seqs sequences when given); prints the median event
+    time of --steps calls after --warmup."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    from int8_paged_kv_gb300 import build as pkbuild
+
+    pkbuild.build()
+    dev = torch.device("cuda", 0)
+    w = wl.build(WORKLOAD, with_append=False, with_kv=not args.seqs)
+    if args.seqs:
+        w = wl.subset(w, args.seqs)
+        key, value, slots = wl.sequence_rows(w, range(w.context_lens.size))
+    else:
+        key, value, slots = w.key, w.value, w.slot_mapping
+    cfg = w.cfg
+    S = int(w.context_lens.size)
+    H, Hk, D, B = cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    scfg = wl.Config(cfg.name, cfg.index, S, H, Hk, D, B, cfg.max_context)
+
+    def u32(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int32)).to(dev)
+
+    q = torch.from_numpy(np.ascontiguousarray(w.q[:S])).to(dev)
+    out = torch.empty_like(q)
+    cl = u32(w.context_lens)
+    step = 1 << 18
+    if args.profile_f32:
+        kc = torch.empty((w.num_blocks, Hk, B, D), dtype=torch.float32, device=dev)
+        vc = torch.empty_like(kc)
+        for i in range(0, key.shape[0], step):
+            pk.pa_f32_reshape_and_cache(torch.from_numpy(key[i:i + step].reshape(-1, Hk * D)).to(dev),
+                                        torch.from_numpy(value[i:i + step].reshape(-1, Hk * D)).to(dev),
+                                        kc, vc, u32(slots[i:i + step]), num_kv_heads=Hk, head_size=D, block_size=B)
+        bt = u32(w.block_tables)
+        ws = torch.empty(max(16, pk.pa_f32_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq)),
+                         dtype=torch.uint8, device=dev)
+
+        def run():
+            pk.pa_f32_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale, workspace=ws)
+        kind, nbytes = "f32 cache", wl.algorithmic_decode_bytes(scfg, w.context_lens, cache="f32")
+    else:
+        max_t = cfg.max_context
+        words = pk.pa_q8c_cache_words(max_t, Hk, D)
+        kc = torch.empty((S, words), dtype=torch.int32, device=dev)
+        vc = torch.empty_like(kc)
+        seq = np.repeat(np.arange(S, dtype=np.int64), w.context_lens.astype(np.int64))
+        pos = np.concatenate([np.arange(int(c), dtype=np.int64) for c in w.context_lens])
+        cs = (seq * max_t + pos).astype(np.uint32)
+        for i in range(0, key.shape[0], step):
+            pk.pa_q8c_append(torch.from_numpy(key[i:i + step].reshape(-1, Hk * D)).to(dev),
+                             torch.from_numpy(value[i:i + step].reshape(-1, Hk * D)).to(dev),
+                             kc, vc, u32(cs[i:i + step]), num_kv_heads=Hk, head_size=D, max_t=max_t)
+        ws = torch.empty(max(16, pk.pa_q8c_decode_workspace_size(S, H, Hk, D, max_t)), dtype=torch.uint8,
+                         device=dev)
+
+        def run():
+            pk.pa_q8c_decode(out, q, kc, vc, cl, num_kv_heads=Hk, max_t=max_t, scale=w.scale, workspace=ws)
+        kind, nbytes = "contiguous q8 cache", wl.algorithmic_decode_bytes(scfg, w.context_lens, cache="q8c")
+    for _ in range(max(3, args.warmup)):
+        run()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = float(np.median(ts))
+    print(json.dumps({"kind": f"profile case: {kind} decode", "seqs": S, "ms": round(ms, 4),
+                      "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
+                      "device_status": pk.pa_q8_device_status()}))
+
+
+def oracle_rates(w, n: int) -> dict:
+    """GB/s of the CPU oracle on the first n sequences of a workload, for the
+    report's variants (single query, 4 and 8 query rows, f32 cache,
+    contiguous cache, append + decode); caches are written untimed, the
+    timed call is the oracle's function for the variant."""
+    import oracle
+    cfg = w.cfg
+    sub = wl.subset(w, n)
+    n = int(sub.context_lens.size)
+    Hk, D, B = cfg.num_kv_heads, cfg.head_size, cfg.block_size
+    scfg = wl.Config(cfg.name, cfg.index, n, cfg.num_heads, Hk, D, B, cfg.max_context)
+    k, v, sm = wl.sequence_rows(sub, range(n))
+    kc, vc = wl.empty_cache(sub), wl.empty_cache(sub)
+    oracle.reshape_and_cache(k, v, kc, vc, sm, num_kv_heads=Hk, head_size=D, block_size=B)
+    q = np.ascontiguousarray(sub.q[:n])
+    args = dict(num_kv_heads=Hk, block_size=B, scale=sub.scale)
+    out = {}
+
+    def rate(name, fn, nbytes):
+        t0 = time.perf_counter()
+        fn()
+        out[name] = round(nbytes / (time.perf_counter() - t0) / 1e9, 4)
+    rate("q8", lambda: oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args),
+         wl.algorithmic_decode_bytes(scfg, sub.context_lens))
+    for R in (4, 8):
+        qr = np.ascontiguousarray(wl.query_rows(w, R)[:n])
+        rate(f"rows{R}", lambda: oracle.decode_rows(qr, kc, vc, sub.block_tables, sub.context_lens, **args),
+             wl.algorithmic_decode_bytes(scfg, sub.context_lens, R))
+    fk = np.zeros((sub.num_blocks, Hk, B, D), dtype=np.float32)
+    fv = np.zeros_like(fk)
+    oracle.reshape_and_cache_f32(k, v, fk, fv, sm, num_kv_heads=Hk, head_size=D, block_size=B)
+    rate("f32", lambda: oracle.decode_f32(q, fk, fv, sub.block_tables, sub.context_lens, **args),
+         wl.algorithmic_decode_bytes(scfg, sub.context_lens, cache="f32"))
+    max_t = cfg.max_context
+    words = oracle.cq_seq_words(max_t, Hk, D)
+    ck = np.zeros((n, words), dtype=np.uint32)
+    cv = np.zeros_like(ck)
+    cslots = np.concatenate([s * max_t + np.arange(int(c)) for s, c in enumerate(sub.context_lens)]).astype(np.uint32)
+    oracle.cq_append(k, v, ck, cv, cslots, num_kv_heads=Hk, head_size=D, max_t=max_t)
+    rate("contig", lambda: oracle.cq_decode(q, ck, cv, sub.context_lens, num_kv_heads=Hk, max_t=max_t,
+                                            scale=sub.scale),
+         wl.algorithmic_decode_bytes(scfg, sub.context_lens, cache="q8c"))
+    nk, nv = wl.new_token_rows(w, 1)
+    nk, nv = np.ascontiguousarray(nk[:n].reshape(n, -1)), np.ascontiguousarray(nv[:n].reshape(n, -1))
+    pos = np.minimum(sub.context_lens.astype(np.int64), cfg.max_blocks_per_seq * B) - 1
+    nslots = (sub.block_tables[np.arange(n), pos // B].astype(np.int64) * B + pos % B).astype(np.uint32)
+
+    def append_decode():
+        oracle.reshape_and_cache(nk, nv, kc, vc, nslots, num_kv_heads=Hk, head_size=D, block_size=B)
+        oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args)
+    rate("append", append_decode, wl.algorithmic_decode_bytes(scfg, sub.context_lens) +
+         wl.algorithmic_writer_bytes(Hk, D, nslots))
+    out["sample"] = f"first {n} sequences ({int(sub.context_lens.sum())} context tokens), fp64 C oracle"
+    out["cores"] = oracle.num_threads()
+    return out
 
 
 def run_configs(args) -> None:
@@ -768,6 +906,9 @@ def run_configs(args) -> None:
     for name in wl.CONFIGS:
         w = wl.build(name, with_append=False)
         cfg = w.cfg
+        ora = oracle_rates(w, {"tiny": 2, "llama8b": 4, "long": 1, "large": 8, "edge": 8}[name])
+        args.oracle_rates = ora
+        print(json.dumps({"kind": "cpu oracle sample", "workload": name, **ora}), flush=True)
         S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
 
         def u32(x):
@@ -831,6 +972,7 @@ def run_configs(args) -> None:
             print(json.dumps({"kind": "decode per workload", "workload": name, "description": cfg.description,
                               "query_rows": R,
                               "kernel": {1: "cuda-core", 2: "tensor-core", 3: "tcgen05"}[kernel],
+                              "cpu_oracle_gbps": ora["q8" if R == 1 else f"rows{R}"],
                               "partition_tokens": plan["partition_tokens"], "ms": round(ms, 4),
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
@@ -853,6 +995,8 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--profile-rows", type=int, default=0,
                     help="profiler case: multi-row decode with this many query rows (not a bench line)")
+    ap.add_argument("--profile-f32", action="store_true", help="profiler case: f32-cache decode")
+    ap.add_argument("--profile-contig", action="store_true", help="profiler case: contiguous-cache decode")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile-size case: only the first N sequences (not a bench number)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -870,6 +1014,8 @@ def main():
         run_configs(args)
     elif args.profile_rows:
         run_profile_rows(args)
+    elif args.profile_f32 or args.profile_contig:
+        run_profile_variant(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
