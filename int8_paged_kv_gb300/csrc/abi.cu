@@ -177,6 +177,27 @@ int decode_impl(float *out, const float *q, const uint32_t *key_cache, const uin
     return PA_Q8_OK;
 }
 
+int cq_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || max_t <= 0) return PA_Q8_EINVAL;
+    if (num_heads % num_kv_heads != 0 || head_size % 32 != 0) return PA_Q8_EINVAL;
+    if (head_size != 128 && head_size != 256) return PA_Q8_EUNSUPPORTED;
+    if (num_seqs > 65535 || (int64_t)num_kv_heads * (num_heads / num_kv_heads) > 65535) return PA_Q8_EUNSUPPORTED;
+    if (max_t > (int64_t)1 << 30) return PA_Q8_EUNSUPPORTED;
+    return PA_Q8_OK;
+}
+
+void cq_fill(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
+    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, 1, (int)max_t);
+    a.contiguous = 1;
+}
+
+int cq_plan(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int sms) {
+    pa_q8_decode_options o = opts ? *opts : pa_q8_decode_options{};
+    if (o.kernel != PA_Q8_KERNEL_AUTO && o.kernel != PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
+    o.kernel = PA_Q8_KERNEL_TENSOR_CORE;
+    return plan_for(a, &o, sms);
+}
+
 }  // namespace
 
 extern "C" {
@@ -325,30 +346,6 @@ int pa_q8c_append(const float *key, const float *value, int64_t key_stride, int6
     return PA_Q8_OK;
 }
 
-namespace {
-
-int cq_shape(int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
-    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 || max_t <= 0) return PA_Q8_EINVAL;
-    if (num_heads % num_kv_heads != 0 || head_size % 32 != 0) return PA_Q8_EINVAL;
-    if (head_size != 128 && head_size != 256) return PA_Q8_EUNSUPPORTED;
-    if (num_seqs > 65535 || (int64_t)num_kv_heads * (num_heads / num_kv_heads) > 65535) return PA_Q8_EUNSUPPORTED;
-    if (max_t > (int64_t)1 << 30) return PA_Q8_EUNSUPPORTED;
-    return PA_Q8_OK;
-}
-
-void cq_fill(pa_q8::DecodeArgs &a, int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t) {
-    fill_shape(a, num_seqs, num_heads, num_kv_heads, head_size, 1, (int)max_t);
-    a.contiguous = 1;
-}
-
-int cq_plan(pa_q8::DecodeArgs &a, const pa_q8_decode_options *opts, int sms) {
-    pa_q8_decode_options o = opts ? *opts : pa_q8_decode_options{};
-    if (o.kernel != PA_Q8_KERNEL_AUTO && o.kernel != PA_Q8_KERNEL_TENSOR_CORE) return PA_Q8_EINVAL;
-    o.kernel = PA_Q8_KERNEL_TENSOR_CORE;
-    return plan_for(a, &o, sms);
-}
-
-}  // namespace
 
 size_t pa_q8c_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size, int64_t max_t,
                                     const pa_q8_decode_options *opts) {
