@@ -244,17 +244,30 @@ __host__ __device__ inline Layout make_layout(int D, int streams, int ring, int 
 
 // Load the partition's block-table slice (one entry per piece of
 // min(B, 32) tokens); entries out of range become kPadSlot and are flagged.
+// Four entries per thread are loaded before any is stored, so a long
+// partition's table costs one memory round trip, not one per pass.
 __device__ void load_table(const Params &P, const Work &w, uint32_t *table) {
+    constexpr int U = 4;
     const int n = (w.len + (1 << P.log2ptok) - 1) >> P.log2ptok;
     const uint32_t *row = P.bt + (int64_t)w.s * P.Nb;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int tabs = w.t_begin + (i << P.log2ptok);
-        uint32_t pb = __ldg(row + (tabs >> P.log2B));
-        if ((int64_t)pb >= P.num_blocks) {
-            flag_error(P.status, kDevBadBlock);
-            pb = kPadSlot;
+    for (int i0 = threadIdx.x; i0 < n; i0 += U * blockDim.x) {
+        uint32_t pb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            pb[u] = i < n ? __ldg(row + ((w.t_begin + (i << P.log2ptok)) >> P.log2B)) : 0u;
         }
-        table[i] = pb;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < n) {
+                if ((int64_t)pb[u] >= P.num_blocks) {
+                    flag_error(P.status, kDevBadBlock);
+                    pb[u] = kPadSlot;
+                }
+                table[i] = pb[u];
+            }
+        }
     }
 }
 
@@ -315,13 +328,16 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
     const int nwarps = blockDim.x >> 5;
     for (int hh = warp; hh < w.nh; hh += nwarps) {
         const int64_t row0 = qrow(P, w, w.h0 + hh) * P.NP;
-        float M = -INFINITY;
-        for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
+        // up to 32 partitions: each lane's (m, l) is read once
+        const float2 ml0 = lane < np ? __ldcg(reinterpret_cast<const float2 *>(P.pml + (row0 + lane) * 2))
+                                     : make_float2(-INFINITY, 0.0f);
+        float M = ml0.x;
+        for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
         if (M == -INFINITY) M = 0.0f;       // a query row that sees no token: weights 0, row 0
-        float L = 0.0f;
-        for (int p = lane; p < np; p += 32)
+        float L = lane < np ? ml0.y * fast_exp2(ml0.x - M) : 0.0f;
+        for (int p = lane + 32; p < np; p += 32)
             L += __ldcg(P.pml + (row0 + p) * 2 + 1) * fast_exp2(__ldcg(P.pml + (row0 + p) * 2) - M);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
@@ -331,8 +347,9 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
         }
     }
     __syncthreads();
-    // four output elements per thread at a time, so their loads overlap
-    constexpr int U = 4;
+    // four output elements per thread at a time, eight partitions deep, so
+    // their loads overlap; the sum still runs over p in order
+    constexpr int U = 4, PU = 8;
     const int n_out = w.nh * D;
     for (int i0 = threadIdx.x; i0 < n_out; i0 += U * blockDim.x) {
         float a[U], M[U];
@@ -347,12 +364,23 @@ __device__ void combine_rows(const Params &P, const Work &w, int np, float *scra
             M[u] = scratch[2 * hh];
             a[u] = 0.0f;
         }
-#pragma unroll 2
-        for (int p = 0; p < np; ++p) {
+        for (int p0 = 0; p0 < np; p0 += PU) {
+            float v[U][PU], m[U][PU];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                a[u] = fmaf(__ldcg(P.pacc + (prow[u] + p) * D + dd[u]),
-                            fast_exp2(__ldcg(P.pml + (prow[u] + p) * 2) - M[u]), a[u]);
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int j = 0; j < PU; ++j) {
+                    const int p = min(p0 + j, np - 1);
+                    v[u][j] = __ldcg(P.pacc + (prow[u] + p) * D + dd[u]);
+                    m[u][j] = __ldcg(P.pml + (prow[u] + p) * 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int j = 0; j < PU; ++j)
+                    if (p0 + j < np) a[u] = fmaf(v[u][j], fast_exp2(m[u][j] - M[u]), a[u]);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -500,6 +528,19 @@ decode_tc_kernel(Params P) {
         for (int k = 0; k < RING; ++k) mbar_init(bars + 8 * k, 1);
         fence_mbar_init();
     }
+    const int nh_tile = max(0, min(8, w.nh - 8 * ht));
+    const bool row_ok = gq < nh_tile;
+    const int vh = w.h0 + 8 * ht + gq;                      // this thread's virtual head
+    // q is loaded before the block table so the two round trips overlap
+    // (head size 256 reads q below, into shared memory)
+    float4 qraw[kQInSmem ? 1 : NKS];
+    if constexpr (!kQInSmem) {
+        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks)
+            qraw[ks] = row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
     if (P.nk) append_tokens<D>(P, w);
     load_table(P, w, const_cast<uint32_t *>(table));
     __syncthreads();
@@ -510,10 +551,6 @@ decode_tc_kernel(Params P) {
             issue_chunk<D>(P, w, table, ts + SLOTS * issued, ring + issued * L.slot_bytes,
                            bars + 8 * issued, policy);
     }
-
-    const int nh_tile = max(0, min(8, w.nh - 8 * ht));
-    const bool row_ok = gq < nh_tile;
-    const int vh = w.h0 + 8 * ht + gq;                      // this thread's virtual head
     // tokens this row sees in the partition (query row b sees c - (R-1-b));
     // chunks below the warp's smallest length need no masking
     const int len_row = row_ok ? row_len(P, w, vh) : w.len;
@@ -527,10 +564,14 @@ decode_tc_kernel(Params P) {
     {
         const float4 *qv = reinterpret_cast<const float4 *>(
             P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
+        auto qload = [&](int ks) -> float4 {
+            if constexpr (kQInSmem) return row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            else return qraw[ks];
+        };
         float mx = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
-            const float4 v = row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = qload(ks);
             mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -540,7 +581,7 @@ decode_tc_kernel(Params P) {
         qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
-            const float4 v = row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = qload(ks);
             uint32_t f0, f1, f2, f3;
             split_f16x2(v.x * down, v.y * down, f0, f1);
             split_f16x2(v.z * down, v.w * down, f2, f3);
@@ -2193,15 +2234,38 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
     }
     __syncthreads();
     if (S <= (int)blockDim.x) {
-        // one thread per sequence: its rank is the number of smaller keys
-        // (all distinct), read from shared memory as broadcasts
-        if ((int)threadIdx.x < S) {
-            const unsigned long long mine = keys[threadIdx.x];
-            int rank = 0;
-            for (int j = 0; j < S; ++j) rank += keys[j] < mine;
-            order[rank] = ((unsigned long long)(cap - (int64_t)(mine >> 32)) << 32) | threadIdx.x;
+        // G threads per sequence (a power of two, at most a warp): each counts
+        // the smaller keys (all distinct) in its stride of the S keys, the
+        // group sums them into the sequence's rank
+        int G = 1;
+        while (G < 32 && 2 * G * S <= (int)blockDim.x) G <<= 1;
+        const int i = threadIdx.x / G, part = threadIdx.x % G;
+        int rank = 0;
+        const unsigned long long mine = i < S ? keys[i] : 0ull;
+        if (i < S) {
+#pragma unroll 8
+            for (int j = part; j < S; j += G) rank += keys[j] < mine;
         }
+        for (int o = G >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        if (i < S && part == 0)
+            order[rank] = ((unsigned long long)(cap - (int64_t)(mine >> 32)) << 32) | (unsigned)i;
         return;
+    }
+    // bitonic sort of the n (power of two) keys, ascending
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long a = keys[i], b = keys[l];
+                    if ((a > b) == ((i & k) == 0)) {
+                        keys[i] = b;
+                        keys[l] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
     }
     for (int i = threadIdx.x; i < S; i += blockDim.x)
         order[i] = ((unsigned long long)(cap - (int64_t)(keys[i] >> 32)) << 32) | (keys[i] & 0xFFFFFFFFull);

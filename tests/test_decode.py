@@ -176,6 +176,42 @@ def test_plan_is_what_the_benchmark_times():
     assert plan["num_partitions"] * plan["partition_tokens"] >= cfg.max_context
 
 
+@pytest.mark.parametrize("S", [300, 1500, 9000])
+def test_prep_orders_sequences_longest_first(S):
+    """The order the prep kernel leaves at the start of the workspace (one
+    u64 per sequence: clamped length << 32 | sequence) is longest first, ties
+    by sequence index, for batches it ranks (<= 1024) and sorts (<= 8192),
+    and the identity beyond; the grid runs sequences in that order."""
+    import torch
+    import int8_paged_kv_gb300 as pk
+    from tests.gpu_helpers import dev_u32, device_status
+    rng = np.random.default_rng(S + 1)
+    lens = rng.integers(0, 41, size=S)
+    lens[:5] = [40, 40, 0, 40, 33]
+    w, ok_, ov_, kc, vc = _random_case(S, 4, 2, 64, 16, lens.tolist(), seed=S)
+    cap = w.block_tables.shape[1] * 16                # 48: sequence 3's three blocks are all in the table
+    cl = lens.astype(np.uint32)
+    cl[3] = 10_000                                   # clamped to the table's capacity
+    plan = pk.pa_q8_decode_plan(S, 4, 2, 64, 16, w.block_tables.shape[1], kernel=TC)
+    assert plan["num_ctas"] > 3 * torch.cuda.get_device_properties(0).multi_processor_count   # prep runs
+    ws = torch.zeros(pk.pa_q8_decode_workspace_size(S, 4, 2, 64, 16, w.block_tables.shape[1], kernel=TC),
+                     dtype=torch.uint8, device="cuda")
+    q = torch.from_numpy(w.q).cuda()
+    pk.pa_q8_decode(torch.empty_like(q), q, kc, vc, dev_u32(w.block_tables), dev_u32(cl),
+                    num_kv_heads=2, block_size=16, scale=w.scale, workspace=ws, kernel=TC)
+    assert device_status(clear=True) == 0
+    keys = ws[:8 * S].cpu().numpy().view(np.uint64)
+    seq = (keys & np.uint64(0xFFFFFFFF)).astype(np.int64)
+    length = (keys >> np.uint64(32)).astype(np.int64)
+    clamped = np.minimum(cl.astype(np.int64), cap)
+    assert np.array_equal(np.sort(seq), np.arange(S))
+    assert np.array_equal(length, clamped[seq])
+    if S <= 8192:
+        assert np.array_equal(seq, np.lexsort((np.arange(S), -clamped)))
+    else:
+        assert np.array_equal(seq, np.arange(S))
+
+
 @pytest.mark.parametrize("S", [1500, 9000])
 def test_many_sequences_take_every_ordering_path(S):
     """More sequences than one prep CTA ranks (sorting network) and more than
