@@ -88,7 +88,7 @@ def recorded_traffic() -> dict | None:
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_paged_kv_gb300", "csrc")
-    for name in ("decode.cu", "device_util.cuh"):
+    for name in ("decode.cu", "decode_common.cuh", "device_util.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_q8.so")
-SOURCES = ["abi.cu", "writer.cu", "decode.cu"]
+SOURCES = ["abi.cu", "writer.cu", "decode.cu", "decode_umma.cu", "decode_f32.cu", "decode_cq.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

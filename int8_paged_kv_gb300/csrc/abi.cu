@@ -1,6 +1,6 @@
 // C ABI of libpa_q8.so: argument checks, launch planning, status strings.
 // Every check happens on the host before anything is queued; the kernels
-// are in writer.cu and decode.cu.
+// are in writer.cu and the decode*.cu files.
 #include <cstdint>
 #include <cstring>
 #include <mutex>

@@ -1,0 +1,477 @@
+// Shared machinery of the decode kernels (one copy per translation unit):
+// the launch parameters, the work split and block-table walk, the bulk-copy
+// chunk ring, the CTA merge of warp states and the split-context combine.
+// The kernel families live in decode.cu (tensor-core and CUDA-core tiles,
+// the prep kernel and the plan), decode_umma.cu (tcgen05), decode_f32.cu
+// (the f32 cache) and decode_cq.cu (the contiguous q8 cache).
+#pragma once
+
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "device_util.cuh"
+#include "kernels.h"
+
+namespace pa_q8 {
+
+struct Params {
+    float *out;
+    const float *q;
+    const uint32_t *kc;
+    const uint32_t *vc;
+    const uint32_t *bt;
+    const uint32_t *cl;
+    int S, H, Hk, B, Nb;
+    int log2B;              // block_size is a power of two
+    int log2ptok;           // piece = min(block_size, 32) tokens
+    int64_t num_blocks;
+    float scale_log2;       // scale * log2(e)
+    int PT;                 // tokens per partition
+    int NP;                 // partitions per sequence (grid x)
+    int r;                  // num_heads / num_kv_heads
+    int R;                  // query rows per sequence (1 = single-query decode)
+    int rv;                 // R * r: (row, head) "virtual heads" per kv head
+    int heads_per_cta;
+    int head_groups;
+    const unsigned long long *order;  // [S]: (clamped length << 32 | sequence) of grid z,
+                                      // longest context first
+    uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
+    float *pml;             // [S][R][H][NP][2]
+    float *pacc;            // [S][R][H][NP][D]
+    uint32_t *status;
+    // fused append of the newest R tokens (nk == nullptr: none)
+    const float *nk;
+    const float *nv;
+    int64_t nk_stride, nv_stride;
+    uint32_t *kc_w;         // the caches, written by the append
+    uint32_t *vc_w;
+    int contiguous;         // contiguous q8 cache (decode_cq_kernel)
+};
+
+// Launchers of the families in their own translation units (head sizes
+// 64 / 128 / 256 as they support; anything else is cudaErrorInvalidValue).
+cudaError_t launch_umma_family(const Params &P, int head_size, cudaStream_t st);
+cudaError_t launch_f32_family(const Params &P, int head_size, cudaStream_t st);
+cudaError_t launch_cq_family(const Params &P, int head_size, cudaStream_t st);
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kChunk = 32;                 // tokens per warp chunk
+constexpr int kLazy = 8;                   // rescale only when a logit passes the reference max by 2^8
+constexpr int kVScaleBias = 131;           // weights carry 2^(131 - E): p * vs * 2^(131-E) < 2^13
+
+// (row, head) pairs one tcgen05 CTA serves
+constexpr int kUmmaHeads = 64;
+
+#ifndef PA_Q8_TC_SLOTS
+#define PA_Q8_TC_SLOTS 4                   // token-slot warps per head tile
+#endif
+#ifndef PA_Q8_TC_RING_64
+#define PA_Q8_TC_RING_64 3                 // chunk buffers per slot, head size 64
+#endif
+#ifndef PA_Q8_TC_RING_128
+#define PA_Q8_TC_RING_128 2
+#endif
+#ifndef PA_Q8_TC_RING_256
+#define PA_Q8_TC_RING_256 2
+#endif
+// Virtual heads per tensor-core CTA for head sizes 64 / 128.  Each head tile
+// converts the chunk's codes itself, so a 16-head CTA does twice the work of
+// an 8-head one on one CTA per SM; two 8-head CTAs (three per SM) finish
+// sooner, their second K/V read mostly served by L2.
+#ifndef PA_Q8_TC_MAX_HEADS
+#define PA_Q8_TC_MAX_HEADS 8
+#endif
+#ifndef PA_Q8_TC_MINB_128
+#define PA_Q8_TC_MINB_128 3                // CTAs per SM the register budget targets
+#endif
+
+
+// Which CTA this is and the token range it owns.  The CTA serves virtual
+// heads h0 .. h0 + nh - 1 of kv head g: virtual head vh is query row
+// b = vh / r, head g * r + vh % r of that row.
+struct Work {
+    int s, g, h0, nh, p;
+    int c;          // clamped context length
+    int t_begin;    // first logical token of the partition
+    int len;        // tokens in the partition
+    bool single;    // the partition is the whole context
+};
+
+__device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
+    w.p = blockIdx.x;
+    w.g = blockIdx.y / P.head_groups;
+    const int hg = blockIdx.y % P.head_groups;
+    w.h0 = hg * P.heads_per_cta;
+    w.nh = min(P.heads_per_cta, P.rv - w.h0);
+    const int64_t cap = (int64_t)P.Nb * P.B;
+    if (P.order) {
+        // written by the prep kernel that precedes this grid on the stream
+        grid_dependency_wait();
+        const unsigned long long e = __ldcg(P.order + blockIdx.z);
+        w.s = (int)(e & 0xFFFFFFFFull);
+        w.c = (int)(e >> 32);
+    } else {
+        w.s = (int)blockIdx.z;
+        const int64_t craw = __ldg(P.cl + w.s);
+        w.c = (int)(craw < cap ? craw : cap);
+    }
+    w.t_begin = w.p * P.PT;
+    w.len = min(w.c - w.t_begin, P.PT);
+    w.single = w.c <= P.PT;
+    return w.len > 0;
+}
+
+// Row of q / out (in units of head_size) of virtual head vh of the CTA's
+// group: sequence s, query row vh / r, head g * r + vh % r.
+__device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) {
+    if (P.R == 1) return (int64_t)w.s * P.H + (int64_t)w.g * P.r + vh;      // single query: no division
+    const int b = vh / P.r;
+    return ((int64_t)w.s * P.R + b) * P.H + (int64_t)w.g * P.r + (vh - b * P.r);
+}
+
+// Tokens of this partition virtual head vh attends to: query row b sees the
+// first c - (R - 1 - b) tokens of the context ("attention.rs", attention_b:
+// t_len = base_pos + b + 1).
+__device__ __forceinline__ int row_len(const Params &P, const Work &w, int vh) {
+    const int cb = P.R == 1 ? w.c : w.c - (P.R - 1 - vh / P.r);
+    return max(0, min(cb - w.t_begin, P.PT));
+}
+
+// Fused append: quantise the sequence's newest R tokens (positions c-R ..
+// c-1 of the clamped context; row b of the new K/V rows is position c-R+b)
+// that fall in this CTA's partition, for its kv head, and store their K and V
+// token vectors in the cache -- the writer's arithmetic, one warp per vector.
+// Every CTA whose tiles hold such a token stores it, all with the same bits,
+// so a tile copy observes the token's words whichever store it sees; the
+// caller's CTA barrier (after the proxy fence here) orders the stores before
+// this CTA's bulk copies.
+template <int D>
+__device__ void append_tokens(const Params &P, const Work &w) {
+    constexpr int WORDS = D / 4;
+    constexpr int NW = (WORDS + 31) / 32;          // words per lane (head size 64: lanes 0..15)
+    const int first = w.c - P.R;                    // position of new row 0 (may be < 0)
+    const int t_lo = max(first, w.t_begin), t_hi = min(w.c, w.t_begin + P.PT);
+    const int nvec = 2 * max(0, t_hi - t_lo);       // (token, K or V) vectors
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int v = warp; v < nvec; v += (int)(blockDim.x >> 5)) {
+        const int t = t_lo + (v >> 1);
+        const bool is_v = v & 1;
+        const int64_t row = (int64_t)w.s * P.R + (t - first);
+        const float4 *src = reinterpret_cast<const float4 *>(
+            (is_v ? P.nv + row * P.nv_stride : P.nk + row * P.nk_stride) + (int64_t)w.g * D);
+        float4 x[NW];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const int wd = lane + 32 * i;
+            x[i] = wd < WORDS ? __ldg(src + wd) : make_float4(0.f, 0.f, 0.f, 0.f);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
+        const float scale = m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f;
+        const uint32_t pb = __ldg(P.bt + (int64_t)w.s * P.Nb + (t >> P.log2B));
+        if ((int64_t)pb >= P.num_blocks) {         // warp-uniform; the table walk flags it
+            continue;
+        }
+        uint32_t *dst = (is_v ? P.vc_w : P.kc_w) +
+                        (((int64_t)pb * P.Hk + w.g) * P.B + (t & (P.B - 1))) * (WORDS + 1);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const int wd = lane + 32 * i;
+            if (wd < WORDS) dst[wd] = pack_word(x[i], inv);
+        }
+        if (lane == 0) dst[WORDS] = __float_as_uint(scale);
+    }
+    fence_proxy_async_global();
+}
+
+// Zero output rows of a sequence whose context is empty (partition 0 only).
+template <int D>
+__device__ void write_zero_rows(const Params &P, const Work &w) {
+    if (w.p != 0 || w.c != 0) return;
+    for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
+        const int hh = i / D, d = i % D;
+        P.out[qrow(P, w, w.h0 + hh) * D + d] = 0.0f;
+    }
+}
+
+__host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout (bytes from the dynamic base).
+struct Layout {
+    uint32_t bars;        // [streams][ring] full barriers
+    uint32_t table;       // physical block of each piece of the partition
+    uint32_t extra;       // kernel-specific (q fragments, or q and weights)
+    uint32_t ring;        // [streams][ring] chunk buffers
+    uint32_t slot_bytes;  // one chunk: K rows [32][W] then V rows [32][W]
+    uint32_t total;
+};
+
+__host__ __device__ inline Layout make_layout(int D, int streams, int ring, int PT, int B,
+                                              uint32_t extra_bytes) {
+    Layout L{};
+    const int W = D / 4 + 1;
+    const int ptok = B < kChunk ? B : kChunk;
+    const int pieces = (PT + ptok - 1) / ptok + 1;
+    L.bars = 0;
+    L.table = align_up(streams * ring * 8, 16);
+    L.extra = align_up(L.table + pieces * 4, 128);
+    L.ring = align_up(L.extra + extra_bytes, 128);
+    L.slot_bytes = align_up(2u * kChunk * W * 4, 128);
+    L.total = L.ring + streams * ring * L.slot_bytes;
+    return L;
+}
+
+// Load the partition's block-table slice (one entry per piece of
+// min(B, 32) tokens); entries out of range become kPadSlot and are flagged.
+// Four entries per thread are loaded before any is stored, so a long
+// partition's table costs one memory round trip, not one per pass.
+__device__ void load_table(const Params &P, const Work &w, uint32_t *table) {
+    constexpr int U = 4;
+    const int n = (w.len + (1 << P.log2ptok) - 1) >> P.log2ptok;
+    const uint32_t *row = P.bt + (int64_t)w.s * P.Nb;
+    for (int i0 = threadIdx.x; i0 < n; i0 += U * blockDim.x) {
+        uint32_t pb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            pb[u] = i < n ? __ldg(row + ((w.t_begin + (i << P.log2ptok)) >> P.log2B)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < n) {
+                if ((int64_t)pb[u] >= P.num_blocks) {
+                    flag_error(P.status, kDevBadBlock);
+                    pb[u] = kPadSlot;
+                }
+                table[i] = pb[u];
+            }
+        }
+    }
+}
+
+// Copy chunk c of the partition (32 tokens; pieces of min(B, 32) tokens,
+// each a contiguous run of one (block, kv head) tile) into the chunk buffer
+// at `slot`, completing on `bar`.  Whole warp; lane i copies piece i.
+template <int D>
+__device__ __forceinline__ void issue_chunk(const Params &P, const Work &w, const uint32_t *table,
+                                            int c, uint32_t slot, uint32_t bar, uint64_t policy) {
+    constexpr int W = D / 4 + 1;
+    const int lane = threadIdx.x & 31;
+    const int t = c * kChunk + (lane << P.log2ptok);   // partition-relative token
+    uint32_t bytes = 0;
+    int64_t base = 0;
+    if (lane < (kChunk >> P.log2ptok) && t < w.len) {
+        const uint32_t pb = table[t >> P.log2ptok];
+        if (pb != kPadSlot) {
+            const int off = (w.t_begin + t) & (P.B - 1);
+            base = (((int64_t)pb * P.Hk + w.g) << P.log2B) * W + (int64_t)off * W;
+            bytes = (uint32_t)W * 4 << P.log2ptok;
+        }
+    }
+    const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes) * 2u;
+    if (lane == 0) mbar_arrive_expect_tx(bar, total);
+    __syncwarp();
+    if (bytes) {
+        fence_proxy_async_smem();
+        const uint32_t dst = slot + (((uint32_t)lane * W * 4) << P.log2ptok);
+        bulk_copy_g2s(dst, P.kc + base, bytes, bar, policy);
+        bulk_copy_g2s(dst + kChunk * W * 4, P.vc + base, bytes, bar, policy);
+    }
+}
+
+// Wait (bounded) for chunk buffers still being filled before a warp leaves.
+__device__ void drain(const Params &P, uint32_t bars, int ring, int consumed, int issued) {
+    if ((threadIdx.x & 31) != 0) return;
+    for (int i = consumed; i < issued; ++i) {
+        if (!mbar_wait(bars + 8 * (i % ring), (i / ring) & 1)) {
+            flag_error(P.status, kDevWaitTimeout);
+            return;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- epilogue
+//
+// Merge the per-warp online-softmax states of the CTA (m in log2 units, l,
+// acc scaled by 2^(E - 139)) and write the output rows, or this
+// partition's partial (M, L, A) for the combine kernel.
+// Log-sum-exp merge of all np partitions of this CTA's heads (run by the
+// last CTA of a (sequence, head group) to finish):
+// out = sum_p A_p 2^(M_p - M*) / sum_p L_p 2^(M_p - M*), M* = max M_p.
+// The partials of other CTAs are read through L2 (__ldcg).  scratch holds
+// (M*, 1/L) per head.
+template <int D>
+__device__ void combine_rows(const Params &P, const Work &w, int np, float *scratch) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    for (int hh = warp; hh < w.nh; hh += nwarps) {
+        const int64_t row0 = qrow(P, w, w.h0 + hh) * P.NP;
+        // up to 32 partitions: each lane's (m, l) is read once
+        const float2 ml0 = lane < np ? __ldcg(reinterpret_cast<const float2 *>(P.pml + (row0 + lane) * 2))
+                                     : make_float2(-INFINITY, 0.0f);
+        float M = ml0.x;
+        for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        if (M == -INFINITY) M = 0.0f;       // a query row that sees no token: weights 0, row 0
+        float L = lane < np ? ml0.y * fast_exp2(ml0.x - M) : 0.0f;
+        for (int p = lane + 32; p < np; p += 32)
+            L += __ldcg(P.pml + (row0 + p) * 2 + 1) * fast_exp2(__ldcg(P.pml + (row0 + p) * 2) - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        if (lane == 0) {
+            scratch[2 * hh] = M;
+            scratch[2 * hh + 1] = L > 0.0f ? 1.0f / L : 0.0f;
+        }
+    }
+    __syncthreads();
+    // four output elements per thread at a time, eight partitions deep, so
+    // their loads overlap; the sum still runs over p in order
+    constexpr int U = 4, PU = 8;
+    const int n_out = w.nh * D;
+    for (int i0 = threadIdx.x; i0 < n_out; i0 += U * blockDim.x) {
+        float a[U], M[U];
+        int64_t prow[U];
+        int dd[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = min(i0 + u * (int)blockDim.x, n_out - 1);
+            const int hh = i / D;
+            dd[u] = i % D;
+            prow[u] = qrow(P, w, w.h0 + hh) * P.NP;
+            M[u] = scratch[2 * hh];
+            a[u] = 0.0f;
+        }
+        for (int p0 = 0; p0 < np; p0 += PU) {
+            float v[U][PU], m[U][PU];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int j = 0; j < PU; ++j) {
+                    const int p = min(p0 + j, np - 1);
+                    v[u][j] = __ldcg(P.pacc + (prow[u] + p) * D + dd[u]);
+                    m[u][j] = __ldcg(P.pml + (prow[u] + p) * 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int j = 0; j < PU; ++j)
+                    if (p0 + j < np) a[u] = fmaf(v[u][j], fast_exp2(m[u][j] - M[u]), a[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < n_out) {
+                const int hh = i / D;
+                P.out[qrow(P, w, w.h0 + hh) * D + dd[u]] = a[u] * scratch[2 * hh + 1];
+            }
+        }
+    }
+}
+
+template <int D>
+__device__ void merge_and_store(const Params &P, const Work &w, const float *ml, const float *accs,
+                                int n_slots, int heads_stride, float *fac) {
+    // ml: [slot][head][3] = (m, l, E); accs: [slot][head][D]; fac: scratch
+    // [head][n_slots + 2] = per-slot factors, M, L, then room for the
+    // combine's weights.  Called by every thread of the CTA.
+    for (int hh = threadIdx.x; hh < w.nh; hh += blockDim.x) {
+        float M = -INFINITY;
+        for (int sl = 0; sl < n_slots; ++sl) M = fmaxf(M, ml[(sl * heads_stride + hh) * 3]);
+        float Lsum = 0.0f;
+        float *f = fac + hh * (n_slots + 2);
+        for (int sl = 0; sl < n_slots; ++sl) {
+            const float *e = ml + (sl * heads_stride + hh) * 3;
+            float x = 0.0f;
+            if (e[0] != -INFINITY) {
+                const float wgt = fast_exp2(e[0] - M);
+                Lsum += e[1] * wgt;
+                x = wgt * ldexpf(1.0f, __float2int_rn(e[2]) - kVScaleBias);
+            }
+            f[sl] = x;
+        }
+        f[n_slots] = M;
+        f[n_slots + 1] = Lsum;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < w.nh * D; i += blockDim.x) {
+        const int hh = i / D, d = i % D;
+        const float *f = fac + hh * (n_slots + 2);
+        float A = 0.0f;
+        for (int sl = 0; sl < n_slots; ++sl) A = fmaf(accs[(sl * heads_stride + hh) * D + d], f[sl], A);
+        const int64_t qr = qrow(P, w, w.h0 + hh);
+        if (w.single) {
+            // a query row that sees no token (L = 0) gets a zero row
+            P.out[qr * D + d] = f[n_slots + 1] > 0.0f ? A / f[n_slots + 1] : 0.0f;
+        } else {
+            const int64_t row = qr * P.NP + w.p;
+            P.pacc[row * D + d] = A;
+            if (d == 0) {
+                P.pml[row * 2] = f[n_slots];
+                P.pml[row * 2 + 1] = f[n_slots + 1];
+            }
+        }
+    }
+    if (w.single) return;
+    // Split context: the last CTA of this (sequence, head group) to arrive
+    // merges every partition (threadfence / counter handshake).
+    __threadfence();
+    __syncthreads();
+    const int np = (w.c + P.PT - 1) / P.PT;
+    int *last = reinterpret_cast<int *>(fac);
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(P.counters + (int64_t)w.s * gridDim.y + blockIdx.y, 1u);
+        *last = (prev == (uint32_t)(np - 1));
+    }
+    __syncthreads();
+    const bool is_last = *last != 0;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    combine_rows<D>(P, w, np, fac);
+}
+
+// The attention grid is launched as a programmatic dependent of the prep
+// kernel before it on the stream: its launch overlaps the prep kernel, and
+// each CTA waits (griddepcontrol.wait) before it reads the prep's output.
+template <typename K, typename A>
+cudaError_t launch_attn_arg(K kernel, const Params &P, const A &arg, uint32_t smem_bytes, int threads,
+                            cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.NP, P.Hk * P.head_groups, P.S);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = P.order ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, arg);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename K>
+cudaError_t launch_attn(K kernel, const Params &P, uint32_t smem_bytes, int threads, cudaStream_t st) {
+    return launch_attn_arg(kernel, P, P, smem_bytes, threads, st);
+}
+
+}  // namespace
+}  // namespace pa_q8

@@ -1,0 +1,426 @@
+// Multi-row decode on 5th-generation tensor cores: decode_umma_kernel
+// (tcgen05.mma, f32 accumulators in TMEM, warp-specialised conversion,
+// softmax and issue roles).
+#include "decode_common.cuh"
+
+namespace pa_q8 {
+namespace {
+
+// ======================================================== tcgen05 (multi-row)
+//
+// Many virtual heads per kv head (multi-row decode: R query rows x r heads)
+// make the contraction GEMM-shaped, so it runs on the 5th-generation tensor
+// cores: one CTA serves up to 64 virtual heads of one kv head for one
+// partition.  TMEM lane quadrant q holds M rows 32q .. 32q+31: rows 32q + j
+// (j < 16) the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq like
+// the mma.sync kernel), rows 32q + 16 + j its lo part, so a logit's two
+// halves are one shuffle apart.  TMEM holds S twice (columns 0-31, 32-63) and
+// O (D columns).
+//
+// Warp roles, linked only by mbarriers (every wait bounded and abortable):
+//  - warps 0-3, softmax: warp q owns quadrant q (idle when it holds no head).
+//    Per chunk: S row -> online softmax (hi/lo partner threads take 16 tokens
+//    each; lazy rescale of O rows in TMEM) -> P tile rows (w = p * v_scale *
+//    2^(131 - E), split hi/lo like the mma.sync kernel).
+//  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
+//    the other families) become f16 K [32][D] and V^T [D][32] tiles (K-major
+//    core matrices) and the token scales a small table.
+//  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
+//    and, one chunk behind, O += P.V (M 128, N D, K 32).
+// K, V^T, P and S are double buffered by chunk parity.  Signals per buffer
+// b = chunk & 1: conv[b] (96 conversion threads), s_free[b] / p_ready[b]
+// (the active softmax threads), qk[b] / pv[b] (tcgen05.commit).  A waiter
+// never falls two phases behind: the next phase of each barrier needs a step
+// that follows the wait.
+
+constexpr int kUmmaThreads = 256;
+constexpr int kUmmaConvThreads = 96;
+
+template <int D>
+__host__ __device__ constexpr int umma_ring() { return 3; }
+template <int D>
+__host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 64 ? 128u : (D == 128 ? 256u : 512u); }
+// resident CTAs per SM: TMEM (512 columns) and registers (2 x 256 threads x 128)
+template <int D>
+__host__ __device__ constexpr int umma_ctas_per_sm() { return D == 256 ? 1 : 2; }
+
+// Byte offset of element (r, k) of an f16 operand tile with kdim columns in
+// the K-major core-matrix layout (LBO = 128, SBO = kdim / 8 * 128).
+__device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
+    return (uint32_t)(((r >> 3) * (kdim >> 3) + (k >> 3)) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// barrier slots (8 bytes each) after the ring's
+enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarConv = 4, kBarSFree = 6, kBarPReady = 8, kUmmaBars = 10 };
+
+struct UmmaLayout {
+    uint32_t misc, scales, table, ops, ring, slot_bytes, total;
+};
+
+// [barriers: ring, kUmmaBars] [TMEM address, abort flag] [token scales 2 x
+// (K, V) x 32] [table] [operand tiles Q, K x2, V^T x2, P x2] [raw chunk ring].
+// Total at least a 1/(n+1) share of the shared memory, so no more CTAs share
+// an SM than its TMEM serves.
+template <int D>
+__host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
+    constexpr int RING = umma_ring<D>();
+    UmmaLayout L{};
+    const int ptok = B < kChunk ? B : kChunk;
+    const int pieces = (PT + ptok - 1) / ptok + 1;
+    L.misc = (RING + kUmmaBars) * 8;
+    L.scales = align_up(L.misc + 8, 16);
+    L.table = L.scales + 2 * 2 * kChunk * 4;
+    L.ops = align_up(L.table + pieces * 4, 128);
+    const uint32_t ops_bytes = 128u * D * 2 + 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * 32 * 2);
+    L.ring = align_up(L.ops + ops_bytes, 128);
+    L.slot_bytes = align_up(2u * kChunk * (D / 4 + 1) * 4, 128);
+    L.total = L.ring + RING * L.slot_bytes;
+    const uint32_t floor_bytes = 232448u / (umma_ctas_per_sm<D>() + 1) + 128u;
+    if (L.total < floor_bytes) L.total = floor_bytes;
+    return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kUmmaThreads, umma_ctas_per_sm<D>())
+decode_umma_kernel(Params P) {
+    constexpr int RING = umma_ring<D>();
+    constexpr int W = D / 4 + 1;
+    constexpr uint32_t TCOLS = umma_tmem_cols<D>();
+    constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
+    constexpr uint32_t P_BYTES = 128u * kChunk * 2;
+    constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D);
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    Work w;
+    if (!setup_work(P, w)) {
+        write_zero_rows<D>(P, w);
+        return;
+    }
+    const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t s0 = smem_addr(smem);
+    const uint32_t ring_bars = s0, bars = s0 + 8 * RING;
+    auto bar = [&](int kind, int b) { return bars + 8 * (kind + b); };
+    const uint32_t tmem_slot = s0 + L.misc;
+    volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + L.misc + 4);
+    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [2][32]
+    float *vsc = ksc + 2 * kChunk;                                       // [2][32]
+    const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
+    uint8_t *sQ = smem + L.ops, *sK0 = sQ + Q_BYTES, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
+    const uint32_t aQ = s0 + L.ops, aK0 = aQ + Q_BYTES, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
+    const uint32_t ring = s0 + L.ring;
+    const uint64_t policy = l2_policy_evict_first();
+    const int nquad = min(4, (w.nh + 15) / 16);         // quadrants that hold a real head
+    const int nch = (w.len + kChunk - 1) / kChunk;
+
+    if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
+    if (tid == 0) {
+        for (int k = 0; k < RING; ++k) mbar_init(ring_bars + 8 * k, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarQk, b), 1);
+            mbar_init(bar(kBarPv, b), 1);
+            mbar_init(bar(kBarConv, b), kUmmaConvThreads);
+            mbar_init(bar(kBarSFree, b), 32 * nquad);
+            mbar_init(bar(kBarPReady, b), 32 * nquad);
+        }
+        *abort = 0u;
+        fence_mbar_init();
+    }
+    load_table(P, w, const_cast<uint32_t *>(table));
+    for (int i = tid; i < 2 * 128 * kChunk / 8; i += kUmmaThreads)    // P rows of heads that do not exist stay 0
+        reinterpret_cast<uint4 *>(sP0)[i] = make_uint4(0u, 0u, 0u, 0u);
+
+    // softmax threads: this thread's M row (virtual head hl, hi or lo part)
+    const int hl = 16 * (warp & 3) + (lane & 15);
+    const bool row_ok = warp < 4 && hl < w.nh;
+    const int vh = w.h0 + hl;
+    const bool lo_part = lane >= 16;
+    const int half = lo_part ? 16 : 0;
+    const int len_row = row_ok ? row_len(P, w, vh) : 0;
+    const int row = 32 * (warp & 3) + lane, row_hi = 32 * (warp & 3) + (lane & 15), row_lo = row_hi + 16;
+    float qk2 = 0.0f;
+    if (warp < 4) {      // Q row: q * 2^-eq as hi (or lo) f16, K-major
+        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
+        float mx = 0.0f;
+        for (int c = 0; c < D / 4; ++c) {
+            const float4 v = row_ok ? __ldg(qv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
+        qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
+        for (int c = 0; c < D / 8; ++c) {
+            const float4 a = row_ok ? __ldg(qv + 2 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = row_ok ? __ldg(qv + 2 * c + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+            uint32_t h[4], l[4];
+            split_f16x2(a.x * down, a.y * down, h[0], l[0]);
+            split_f16x2(a.z * down, a.w * down, h[1], l[1]);
+            split_f16x2(b.x * down, b.y * down, h[2], l[2]);
+            split_f16x2(b.z * down, b.w * down, h[3], l[3]);
+            *reinterpret_cast<uint4 *>(sQ + kmaj_off(row, 8 * c, D)) =
+                lo_part ? make_uint4(l[0], l[1], l[2], l[3]) : make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + L.misc);
+    const uint32_t tO = tmem + 64;
+
+    // softmax state (warps 0-3) and the issuer's commit record (warp 7, lane 0)
+    float m = -INFINITY, lsum = 0.0f;
+    int E = 12;
+    int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
+    uint32_t last_parity = 0;
+    int issued = 0;                  // chunks whose ring copy warp 7 started
+
+    if (warp == 7) {
+        // ---- ring refills and MMA issue
+        for (; issued < RING && issued < nch; ++issued)
+            issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1;
+            if (!mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort)) break;    // K(i), V(i) ready
+            if (issued < nch) {                                // chunk i's raw slot is free
+                issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
+                               ring_bars + 8 * (issued % RING), policy);
+                ++issued;
+            }
+            bool go = true;
+            if (lane == 0) {
+                if (i >= 2) go = mbar_wait_abortable(bar(kBarSFree, b), ((i - 2) >> 1) & 1, abort);
+                if (go) {
+                    tc_fence_after();
+                    const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16),
+                                 umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
+                    umma_commit(bar(kBarQk, b));
+                    last_commit = kBarQk + b;
+                    last_parity = (i >> 1) & 1;
+                }
+                if (go && i >= 1) {                            // O += P(i-1) . V(i-1)
+                    const int j = i - 1, bj = j & 1;
+                    go = mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort);
+                    if (go) {
+                        tc_fence_after();
+                        const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
+                        umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
+                        umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512),
+                                 IDESC_PV, true);
+                        umma_commit(bar(kBarPv, bj));
+                        last_commit = kBarPv + bj;
+                        last_parity = (j >> 1) & 1;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, (int)go, 0)) break;
+        }
+        if (lane == 0 && !*abort && nch > 0) {                // the last chunk's PV
+            const int j = nch - 1, bj = j & 1;
+            if (mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort)) {
+                tc_fence_after();
+                const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
+                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
+                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512), IDESC_PV,
+                         true);
+                umma_commit(bar(kBarPv, bj));
+                last_commit = kBarPv + bj;
+                last_parity = (j >> 1) & 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---- conversion (96 threads)
+        const int ct = tid - 128;
+        const F16Consts fk;
+        for (int i = 0; i < nch; ++i) {
+            const int b = i & 1, k = i % RING;
+            const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
+            const uint32_t *rawV = rawK + kChunk * W;
+            if (!mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort)) break;
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)) break;   // K tile free
+            uint8_t *dK = sK0 + b * K_BYTES;
+            for (int u = ct; u < kChunk * D / 8; u += kUmmaConvThreads) {   // lane = token: 8 bank groups
+                const int t = u % kChunk, c8 = u / kChunk;
+                uint32_t a0, a1, a2, a3;
+                codes4_to_f16x2(rawK[t * W + 2 * c8], a0, a1, fk);
+                codes4_to_f16x2(rawK[t * W + 2 * c8 + 1], a2, a3, fk);
+                *reinterpret_cast<uint4 *>(dK + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
+            }
+            // V tile and scale table b free: PV(i-2) done, so softmax(i-2) is too
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
+            if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
+            else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
+            uint8_t *dV = sV0 + b * V_BYTES;
+            for (int u = ct; u < D * (kChunk / 8); u += kUmmaConvThreads) {  // lane = head dim: 8 bank groups
+                const int d = u % D, tg = u / D;
+                const uint32_t *src = rawV + (8 * tg) * W + (d >> 2);
+                const uint32_t e = (uint32_t)(d & 3);
+                const uint32_t sel = e | (e << 4) | ((e + 4) << 8) | ((e + 4) << 12);
+                uint32_t h[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    h[j] = sub_1152_x2(and_xor_i<0x00FF00FFu>(prmt_r(src[2 * j * W], src[(2 * j + 1) * W], sel),
+                                                            fk.bias),
+                                       fk.bias);
+                *reinterpret_cast<uint4 *>(dV + kmaj_off(d, 8 * tg, kChunk)) = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarConv, b));
+        }
+    } else if (warp < nquad) {
+        // ---- softmax (quadrant warp)
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+        bool ok = true;
+        for (int i = 0; ok && i < nch; ++i) {
+            const int b = i & 1;
+            ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
+            ok = ok && mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort);     // the scale table
+            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            tc_fence_after();
+            float sv[32], z[16];
+            tmem_ld32(tmem + 32 * b + lane_off, sv);      // TMEM addresses are warp-uniform
+            tc_fence_before();
+            mbar_arrive(bar(kBarSFree, b));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {                // own half + the partner's row at those tokens
+                const float mine = lo_part ? sv[16 + j] : sv[j], send = lo_part ? sv[j] : sv[16 + j];
+                z[j] = mine + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+            }
+            const float *ks = ksc + b * kChunk + half, *vs = vsc + b * kChunk + half;
+            const int t0 = i * kChunk + half;
+            float cmax = -INFINITY, vmax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const bool valid = t0 + j < len_row;
+                z[j] = valid ? z[j] * ks[j] * qk2 : -INFINITY;
+                cmax = fmaxf(cmax, z[j]);
+                vmax = fmaxf(vmax, valid ? vs[j] : 0.0f);
+            }
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 16));
+            const int Ec = (int)(__float_as_uint(vmax) >> 23);
+            const bool need = cmax > m + (float)kLazy || Ec > E;
+            float fa = 1.0f;
+            if (need) {
+                const float m_new = fmaxf(m, cmax);
+                const int E_new = max(E, Ec);
+                const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+                const float ea = (E - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - E_new) << 23);
+                fa = alpha * ea;
+                lsum *= alpha;
+                m = m_new;
+                E = E_new;
+                wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+            }
+            if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {      // O rows once PV(i-1) is done
+                ok = mbar_wait_abortable(bar(kBarPv, (i - 1) & 1), ((i - 1) >> 1) & 1, abort);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tO + lane_off + 32 * c, o);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= fa;
+                    tmem_st32(tO + lane_off + 32 * c, o);
+                }
+            }
+            if (i >= 2) {                                       // P tile b free: PV(i-2) done
+                ok = mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            }
+            const float m_ref = m == -INFINITY ? 0.0f : m;
+            uint8_t *dP = sP0 + b * P_BYTES;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {                 // tokens half + 8c .. +7, both rows of the head
+                uint32_t ph[4], pl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 8 * c + 2 * e;
+                    const float p0 = fast_exp2(z[j] - m_ref), p1 = fast_exp2(z[j + 1] - m_ref);
+                    lsum += p0 + p1;
+                    const float w0 = t0 + j < len_row ? vs[j] : 0.0f, w1 = t0 + j + 1 < len_row ? vs[j + 1] : 0.0f;
+                    split_f16x2(p0 * w0 * wscale, p1 * w1 * wscale, ph[e], pl[e]);
+                }
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
+                    make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_lo, half + 8 * c, kChunk)) =
+                    make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(kBarPReady, b));
+        }
+        // the last PV, then this warp's O rows (hi + lo) into the merge scratch
+        if (ok && nch > 0) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) & 1), ((nch - 1) >> 1) & 1, abort);
+        if (__all_sync(0xFFFFFFFFu, ok)) {
+            tc_fence_after();
+            float *ml = reinterpret_cast<float *>(sQ);                  // [64][3]   (operand tiles are free)
+            float *accs = ml + kUmmaHeads * 3;                          // [64][D]
+            // every PV has completed: no MMA reads the Q tile any more
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(tO + lane_off + 32 * c, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] += __shfl_xor_sync(0xFFFFFFFFu, o[j], 16);
+                if (!lo_part) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) accs[hl * D + 32 * c + j] = o[j];
+                }
+            }
+            const float l_row = lsum + __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+            if (!lo_part) {
+                ml[hl * 3] = m;
+                ml[hl * 3 + 1] = l_row;
+                ml[hl * 3 + 2] = (float)E;
+            }
+        } else {
+            *abort = 1u;
+        }
+    }
+    __syncthreads();
+    const bool failed = *abort != 0u;
+    if (failed && warp == 7 && lane == 0) {
+        // stop only after the newest MMA (and so every earlier one) completed
+        if (last_commit >= 0) mbar_wait(bars + 8 * last_commit, last_parity);
+        for (int c = max(0, issued - RING); c < issued; ++c)     // and the ring copies in flight
+            mbar_wait(ring_bars + 8 * (c % RING), (c / RING) & 1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+    }
+    if (failed) {
+        if (tid == 0) flag_error(P.status, kDevWaitTimeout);
+        return;
+    }
+    float *ml = reinterpret_cast<float *>(sQ);
+    float *accs = ml + kUmmaHeads * 3;
+    merge_and_store<D>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
+}
+
+template <int D>
+cudaError_t launch_umma(const Params &P, cudaStream_t st) {
+    const UmmaLayout L = make_umma_layout<D>(P.PT, P.B);
+    return launch_attn(decode_umma_kernel<D>, P, L.total, kUmmaThreads, st);
+}
+
+}  // namespace
+
+cudaError_t launch_umma_family(const Params &P, int head_size, cudaStream_t st) {
+    switch (head_size) {
+        case 64: return launch_umma<64>(P, st);
+        case 128: return launch_umma<128>(P, st);
+        case 256: return launch_umma<256>(P, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa_q8
