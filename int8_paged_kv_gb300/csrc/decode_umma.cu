@@ -26,7 +26,7 @@ namespace {
 //    the other families) become f16 K [32][D] and V^T [D][32] tiles (K-major
 //    core matrices) and the token scales a small table.
 //  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
-//    and, one chunk behind, O += P.V (M 128, N D, K 32).
+//    and O += P.V (M 128, N D, K 32), each as soon as its inputs are ready.
 // K, V^T, P and S are double buffered by chunk parity.  Signals per buffer
 // b = chunk & 1: conv[b] (96 conversion threads), s_free[b] / p_ready[b]
 // (the active softmax threads), qk[b] / pv[b] (tcgen05.commit).  A waiter
@@ -176,59 +176,76 @@ decode_umma_kernel(Params P) {
     int issued = 0;                  // chunks whose ring copy warp 7 started
 
     if (warp == 7) {
-        // ---- ring refills and MMA issue
+        // ---- ring refills and MMA issue.  Lane 0 polls both inputs and
+        // issues whichever MMA is ready: QK(nq) once chunk nq is converted
+        // (and S buffer nq & 1 was read), PV(np) once P(np) is written.  PV
+        // never waits for a later chunk's conversion, so the V tile it frees
+        // is ready for that conversion as early as possible.  A barrier
+        // cannot run two phases ahead of the poll: its next phase needs an
+        // MMA this warp has not issued yet.
         for (; issued < RING && issued < nch; ++issued)
             issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
-        for (int i = 0; i < nch; ++i) {
-            const int b = i & 1;
-            if (!mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort)) break;    // K(i), V(i) ready
-            if (issued < nch) {                                // chunk i's raw slot is free
-                issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
-                               ring_bars + 8 * (issued % RING), policy);
-                ++issued;
-            }
-            bool go = true;
+        int nq = 0, np = 0;                                   // next QK / PV to issue
+        uint64_t idle_since = 0;
+        uint32_t polls = 0;
+        while (np < nch) {
+            int act = 0;
             if (lane == 0) {
-                if (i >= 2) go = mbar_wait_abortable(bar(kBarSFree, b), ((i - 2) >> 1) & 1, abort);
-                if (go) {
-                    tc_fence_after();
-                    const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16),
-                                 umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
-                    umma_commit(bar(kBarQk, b));
-                    last_commit = kBarQk + b;
-                    last_parity = (i >> 1) & 1;
-                }
-                if (go && i >= 1) {                            // O += P(i-1) . V(i-1)
-                    const int j = i - 1, bj = j & 1;
-                    go = mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort);
-                    if (go) {
-                        tc_fence_after();
-                        const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
-                        umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
-                        umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512),
-                                 IDESC_PV, true);
-                        umma_commit(bar(kBarPv, bj));
-                        last_commit = kBarPv + bj;
-                        last_parity = (j >> 1) & 1;
+                if (nq < nch && mbar_try_wait(bar(kBarConv, nq & 1), (nq >> 1) & 1) &&
+                    (nq < 2 || mbar_try_wait(bar(kBarSFree, nq & 1), ((nq - 2) >> 1) & 1)))
+                    act |= 1;
+                if (np < nq && mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1)) act |= 2;
+                if (act == 0) {
+                    // nothing ready: suspend briefly on the older pending input, then
+                    // poll again; give up after the wait limit or on the CTA's abort
+                    if (np < nq) mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, 256u);
+                    else mbar_try_wait_suspend(bar(kBarConv, nq & 1), (nq >> 1) & 1, 256u);
+                    if (polls++ == 0) idle_since = global_timer_ns();
+                    if ((polls & 15u) == 0) {
+                        if (*abort) act = 4;
+                        else if (global_timer_ns() - idle_since > kWaitLimitNs) {
+                            *abort = 1u;
+                            act = 4;
+                        }
                     }
+                } else {
+                    polls = 0;
                 }
             }
-            if (!__shfl_sync(0xFFFFFFFFu, (int)go, 0)) break;
-        }
-        if (lane == 0 && !*abort && nch > 0) {                // the last chunk's PV
-            const int j = nch - 1, bj = j & 1;
-            if (mbar_wait_abortable(bar(kBarPReady, bj), (j >> 1) & 1, abort)) {
+            act = __shfl_sync(0xFFFFFFFFu, act, 0);
+            if (act & 4) break;
+            if (lane == 0 && (act & 1)) {                        // S = Q . K(nq)^T
                 tc_fence_after();
+                const int b = nq & 1;
+                const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16),
+                             umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
+                umma_commit(bar(kBarQk, b));
+                last_commit = kBarQk + b;
+                last_parity = (nq >> 1) & 1;
+            }
+            if (lane == 0 && (act & 2)) {                        // O += P(np) . V(np)
+                tc_fence_after();
+                const int bj = np & 1;
                 const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
-                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, j > 0);
-                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512), IDESC_PV,
-                         true);
+                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, np > 0);
+                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512),
+                         IDESC_PV, true);
                 umma_commit(bar(kBarPv, bj));
                 last_commit = kBarPv + bj;
-                last_parity = (j >> 1) & 1;
+                last_parity = (np >> 1) & 1;
+            }
+            if (act & 2) ++np;
+            if (act & 1) {
+                // chunk nq's raw slot is free (converted): refill it, after the MMAs are on their way
+                if (issued < nch) {
+                    issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
+                                   ring_bars + 8 * (issued % RING), policy);
+                    ++issued;
+                }
+                ++nq;
             }
         }
         __syncwarp();
