@@ -292,6 +292,9 @@ decode_umma_kernel(Params P) {
         // ---- softmax (quadrant warp)
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
         float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
+        // chunks below every row's length in this warp need no masking (0 when a
+        // lane holds no head: that warp always masks)
+        const int len_full = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)(row_ok ? len_row : 0));
         bool ok = true;
         for (int i = 0; ok && i < nch; ++i) {
             const int b = i & 1;
@@ -308,15 +311,33 @@ decode_umma_kernel(Params P) {
                 const float mine = lo_part ? sv[16 + j] : sv[j], send = lo_part ? sv[j] : sv[16 + j];
                 z[j] = mine + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
             }
-            const float *ks = ksc + b * kChunk + half, *vs = vsc + b * kChunk + half;
+            // this thread's 16 token scales, as 16-byte vectors
+            float ks[16], vs[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 a = reinterpret_cast<const float4 *>(ksc + b * kChunk + half)[q4];
+                const float4 c = reinterpret_cast<const float4 *>(vsc + b * kChunk + half)[q4];
+                ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
+                vs[4 * q4] = c.x; vs[4 * q4 + 1] = c.y; vs[4 * q4 + 2] = c.z; vs[4 * q4 + 3] = c.w;
+            }
             const int t0 = i * kChunk + half;
             float cmax = -INFINITY, vmax = 0.0f;
+            if ((i + 1) * kChunk <= len_full) {                 // warp-uniform: every row sees the whole chunk
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const bool valid = t0 + j < len_row;
-                z[j] = valid ? z[j] * ks[j] * qk2 : -INFINITY;
-                cmax = fmaxf(cmax, z[j]);
-                vmax = fmaxf(vmax, valid ? vs[j] : 0.0f);
+                for (int j = 0; j < 16; ++j) {
+                    z[j] = z[j] * ks[j] * qk2;
+                    cmax = fmaxf(cmax, z[j]);
+                    vmax = fmaxf(vmax, vs[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const bool valid = t0 + j < len_row;
+                    z[j] = valid ? z[j] * ks[j] * qk2 : -INFINITY;
+                    vs[j] = valid ? vs[j] : 0.0f;
+                    cmax = fmaxf(cmax, z[j]);
+                    vmax = fmaxf(vmax, vs[j]);
+                }
             }
             cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));
             vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 16));
@@ -361,8 +382,7 @@ decode_umma_kernel(Params P) {
                     const int j = 8 * c + 2 * e;
                     const float p0 = fast_exp2(z[j] - m_ref), p1 = fast_exp2(z[j + 1] - m_ref);
                     lsum += p0 + p1;
-                    const float w0 = t0 + j < len_row ? vs[j] : 0.0f, w1 = t0 + j + 1 < len_row ? vs[j + 1] : 0.0f;
-                    split_f16x2(p0 * w0 * wscale, p1 * w1 * wscale, ph[e], pl[e]);
+                    split_f16x2(p0 * vs[j] * wscale, p1 * vs[j + 1] * wscale, ph[e], pl[e]);
                 }
                 *reinterpret_cast<uint4 *>(dP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
                     make_uint4(ph[0], ph[1], ph[2], ph[3]);
