@@ -23,17 +23,20 @@ namespace {
 //    each; lazy rescale of O rows in TMEM) -> P tile rows (w = p * v_scale *
 //    2^(131 - E), split hi/lo like the mma.sync kernel).
 //  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
-//    the other families) become f16 K [32][D] and V^T [D][32] tiles (K-major
-//    core matrices) and the token scales a small table.
+//    the other families) become f16 K and V tiles [32 tokens][D] in the
+//    same core-matrix layout (K-major for QK's B, MN-major for PV's B) and
+//    the token scales a small table.
 //  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
 //    and O += P.V (M 128, N D, K 32), each as soon as its inputs are ready.
-// K, V^T, P and S are double buffered by chunk parity.  Signals per buffer
+// K, V, P and S are double buffered by chunk parity.  Signals per buffer
 // b = chunk & 1: conv[b] (96 conversion threads), s_free[b] / p_ready[b]
 // (the active softmax threads), qk[b] / pv[b] (tcgen05.commit).  A waiter
 // never falls two phases behind: the next phase of each barrier needs a step
 // that follows the wait.
 
 constexpr int kUmmaThreads = 256;
+// instruction-descriptor bit: the B operand is MN-major (N contiguous)
+constexpr uint32_t kUmmaBMnMajor = 1u << 16;
 constexpr int kUmmaConvThreads = 96;
 
 template <int D>
@@ -58,7 +61,7 @@ struct UmmaLayout {
 };
 
 // [barriers: ring, kUmmaBars] [TMEM address, abort flag] [token scales 2 x
-// (K, V) x 32] [table] [operand tiles Q, K x2, V^T x2, P x2] [raw chunk ring].
+// (K, V) x 32] [table] [operand tiles Q, K x2, V x2, P x2] [raw chunk ring].
 // Total at least a 1/(n+1) share of the shared memory, so no more CTAs share
 // an SM than its TMEM serves.
 template <int D>
@@ -88,7 +91,7 @@ decode_umma_kernel(Params P) {
     constexpr uint32_t TCOLS = umma_tmem_cols<D>();
     constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
     constexpr uint32_t P_BYTES = 128u * kChunk * 2;
-    constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D);
+    constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D) | kUmmaBMnMajor;
 
     extern __shared__ __align__(128) uint8_t smem[];
     Work w;
@@ -230,8 +233,10 @@ decode_umma_kernel(Params P) {
                 tc_fence_after();
                 const int bj = np & 1;
                 const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
-                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, 128, 512), IDESC_PV, np > 0);
-                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 256, 128, 512),
+                // V tile: token rows of D dims = the MN-major B layout, 8-token
+                // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart
+                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, D * 16, 128), IDESC_PV, np > 0);
+                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 2 * D * 16, D * 16, 128),
                          IDESC_PV, true);
                 umma_commit(bar(kBarPv, bj));
                 last_commit = kBarPv + bj;
@@ -272,18 +277,12 @@ decode_umma_kernel(Params P) {
             if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
             else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
             uint8_t *dV = sV0 + b * V_BYTES;
-            for (int u = ct; u < D * (kChunk / 8); u += kUmmaConvThreads) {  // lane = head dim: 8 bank groups
-                const int d = u % D, tg = u / D;
-                const uint32_t *src = rawV + (8 * tg) * W + (d >> 2);
-                const uint32_t e = (uint32_t)(d & 3);
-                const uint32_t sel = e | (e << 4) | ((e + 4) << 8) | ((e + 4) << 12);
-                uint32_t h[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    h[j] = sub_1152_x2(and_xor_i<0x00FF00FFu>(prmt_r(src[2 * j * W], src[(2 * j + 1) * W], sel),
-                                                            fk.bias),
-                                       fk.bias);
-                *reinterpret_cast<uint4 *>(dV + kmaj_off(d, 8 * tg, kChunk)) = make_uint4(h[0], h[1], h[2], h[3]);
+            for (int u = ct; u < kChunk * D / 8; u += kUmmaConvThreads) {   // as K: the PV B operand is MN-major
+                const int t = u % kChunk, c8 = u / kChunk;
+                uint32_t a0, a1, a2, a3;
+                codes4_to_f16x2(rawV[t * W + 2 * c8], a0, a1, fk);
+                codes4_to_f16x2(rawV[t * W + 2 * c8 + 1], a2, a3, fk);
+                *reinterpret_cast<uint4 *>(dV + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(kBarConv, b));

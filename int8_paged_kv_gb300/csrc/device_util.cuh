@@ -154,8 +154,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 //
 // tcgen05 with one CTA (cta_group::1): f16 operands in shared memory, f32
 // accumulators in tensor memory (TMEM: 128 lanes x 512 32-bit columns per
-// SM).  Operand tiles use the K-major layout without swizzle: 8-row x 16-byte
-// core matrices, LBO bytes apart along K and SBO bytes apart along M/N.
+// SM).  Operand tiles use the canonical layouts without swizzle: 8 x 16-byte
+// core matrices, LBO bytes apart along K and SBO bytes apart along M/N.  In
+// the K-major layout a core matrix holds 8 M/N rows of 8 K elements; an
+// MN-major B operand (instruction-descriptor bit 16) holds 8 K rows of 8 N
+// elements.
 
 __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
@@ -309,13 +312,6 @@ __device__ __forceinline__ uint32_t pack_word(float4 x, float inv) {
     return prmt_i<0x5410u>(prmt_i<0x0040u>(c0, c1), prmt_i<0x0040u>(c2, c3));
 }
 
-
-// Byte permute with a run-time selector.
-__device__ __forceinline__ uint32_t prmt_r(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
 
 // (a & MASK) ^ c in one LOP3, MASK an immediate
 template <uint32_t MASK>
