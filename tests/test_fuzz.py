@@ -1,0 +1,67 @@
+"""Seeded random shapes against the fp64 oracle (oracle.decode_rows: row b
+of R sees the first c - (R-1-b) tokens; R = 1 is the single-query decode).
+Every case draws a head size, GQA ratio, block size, batch, context mix
+(empty, one token, block edges, ragged), query rows, kernel family, forced or
+planned partition size, logit scale and value spread.  The caches are written
+by both writers and must agree bit for bit; the decode must satisfy
+|gpu - oracle| <= 1e-5 + 1e-4 |oracle| elementwise (the 1e-5 taken in units
+of value scale x logit scale outside the workloads' ranges), and rows that
+see no token must be exact zeros."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases(n=24, seed=2026):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        D = int(rng.choice([64, 128, 256]))
+        Hk = int(rng.choice([1, 2, 3, 4, 8]))
+        r = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+        while Hk * r > 64:
+            r //= 2
+        B = int(rng.choice([4, 8, 16, 32, 64]))
+        S = int(rng.integers(1, 13))
+        R = int(rng.choice([1, 1, 2, 3, 5]))
+        kernel = int(rng.choice([0, 1, 2, 3]))
+        pt = int(rng.choice([0, 0, 128, 256, 384]))
+        edge = [0, 1, B - 1, B, B + 1, 2 * B + 3]
+        lens = [int(rng.choice(edge)) if rng.random() < 0.4 else int(rng.integers(1, 700)) for _ in range(S)]
+        out.append(dict(i=i, D=D, Hk=Hk, H=Hk * r, B=B, S=S, R=R, kernel=kernel, pt=pt, lens=lens,
+                        scale_mult=float(rng.choice([0.5, 1.0, 3.0])), dist=float(rng.choice([1.0, 2.0]))))
+    return out
+
+
+CASES = _cases()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int8_paged_kv_gb300 import build
+    build.build()
+    import oracle
+    oracle.build()
+
+
+@pytest.mark.parametrize("c", CASES, ids=lambda c: (f"{c['i']}-D{c['D']}-H{c['H']}-Hk{c['Hk']}-B{c['B']}-S{c['S']}"
+                                                    f"-R{c['R']}-k{c['kernel']}-pt{c['pt']}"))
+def test_random_shape_against_oracle(c):
+    from tests.gpu_helpers import (assert_close, device_status, gpu_decode_rows, oracle_decode_rows,
+                                   random_case)
+    w, ok_, ov_, kc, vc = random_case(c["S"], c["H"], c["Hk"], c["D"], c["B"], c["lens"], seed=1000 + c["i"],
+                                      scale_mult=c["scale_mult"], dist=c["dist"])
+    q = np.random.default_rng(c["i"]).standard_normal((c["S"], c["R"], c["H"], c["D"])).astype(np.float32)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    got = gpu_decode_rows(w, kc, vc, q, kernel=c["kernel"], partition_tokens=c["pt"])
+    # the workloads' ranges (values ~N(0,1), logits ~1) take the bound as stated;
+    # wider values or sharper logits take its 1e-5 part in units of the value
+    # scale times the logit scale, since f32 rounding is relative to those
+    unit = c["dist"] * max(1.0, c["dist"] * c["scale_mult"])
+    assert_close(got / unit, want / unit, str(c))
+    for s, n in enumerate(c["lens"]):
+        for b in range(c["R"]):
+            if n - (c["R"] - 1 - b) <= 0:
+                assert np.all(got[s, b] == 0.0), (s, b)
+    assert device_status() == 0
