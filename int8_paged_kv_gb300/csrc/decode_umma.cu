@@ -129,6 +129,9 @@ decode_umma_kernel(Params P) {
         *abort = 0u;
         fence_mbar_init();
     }
+    // fused append: the newest tokens' vectors are stored (and fenced for the
+    // async proxy) before the barrier that precedes the first bulk copy
+    if (P.nk) append_tokens<D>(P, w);
     load_table(P, w, const_cast<uint32_t *>(table));
     for (int i = tid; i < 2 * 128 * kChunk / 8; i += kUmmaThreads)    // P rows of heads that do not exist stay 0
         reinterpret_cast<uint4 *>(sP0)[i] = make_uint4(0u, 0u, 0u, 0u);

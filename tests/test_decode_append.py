@@ -189,3 +189,23 @@ def test_large_batch_sampled():
                          num_kv_heads=Hk, block_size=cfg.block_size, scale=w.scale, rows=rows)
     assert_close(got[rows[:, 0], 0, rows[:, 1]], want, "large fused step")
     assert device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [3, 0])
+def test_fused_step_on_tcgen05(kernel):
+    """The tcgen05 family (asked for, and chosen automatically at >= 64 (row,
+    head) pairs per kv head: R = 8 rows x 8 heads) stores the new tokens too."""
+    from tests.gpu_helpers import assert_close, dev_u32, device_status, host_u32
+    import int8_paged_kv_gb300 as pk
+    lens = [129, 1, 0, 700, 64, 2000]
+    S, H, Hk, D, R = len(lens), 16, 2, 128, 8
+    w, ok_, ov_, _, _ = _case(lens, H=H, Hk=Hk, D=D, seed=31)
+    q = np.random.default_rng(31).standard_normal((S, R, H, D)).astype(np.float32)
+    key, value = _rows(S, R, Hk, D, seed=32)
+    want, wk, wv = _oracle_step(w, ok_, ov_, q, key, value)
+    kc, vc = dev_u32(ok_), dev_u32(ov_)
+    got = _gpu_step(w, kc, vc, q, key, value, kernel=kernel)
+    assert np.array_equal(host_u32(kc), wk), "K cache words"
+    assert np.array_equal(host_u32(vc), wv), "V cache words"
+    assert_close(got, want, f"kernel {kernel}")
+    assert device_status() == 0

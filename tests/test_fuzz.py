@@ -65,3 +65,64 @@ def test_random_shape_against_oracle(c):
             if n - (c["R"] - 1 - b) <= 0:
                 assert np.all(got[s, b] == 0.0), (s, b)
     assert device_status() == 0
+
+
+def _variant_cases(n, seed, Ds, Bs):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        D = int(rng.choice(Ds))
+        Hk = int(rng.choice([1, 2, 4, 8]))
+        r = int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.choice(Bs))
+        S = int(rng.integers(1, 9))
+        edge = [0, 1, B - 1, B, B + 1]
+        lens = [int(rng.choice(edge)) if rng.random() < 0.4 else int(rng.integers(1, 600)) for _ in range(S)]
+        out.append(dict(i=i, D=D, Hk=Hk, H=Hk * r, B=B, S=S, lens=lens, R=int(rng.choice([1, 2, 3])),
+                        kernel=int(rng.choice([0, 1, 2, 3])), pt=int(rng.choice([0, 128, 256]))))
+    return out
+
+
+def _ids(c):
+    return f"{c['i']}-D{c['D']}-H{c['H']}-Hk{c['Hk']}-B{c['B']}-S{c['S']}-R{c['R']}-k{c['kernel']}-pt{c['pt']}"
+
+
+@pytest.mark.parametrize("c", _variant_cases(12, 7, [64, 128, 256], [8, 16, 32, 64]), ids=_ids)
+def test_random_f32_cache_against_oracle(c):
+    """The f32 cache (oracle.reshape_and_cache_f32 / decode_f32): writer bit for bit, decode in tolerance."""
+    from tests.gpu_helpers import assert_close, device_status
+    from tests.test_f32 import _case, _gpu, _oracle
+    case = _case(c["S"], c["H"], c["Hk"], c["D"], c["B"], c["lens"], seed=2000 + c["i"])
+    assert_close(_gpu(case, pt=c["pt"]), _oracle(case), _ids(c))
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("c", _variant_cases(12, 8, [128, 256], [16]), ids=_ids)
+def test_random_contiguous_cache_against_oracle(c):
+    """The contiguous q8 cache (oracle.cq_append / cq_decode), max_t past the longest context."""
+    import oracle
+    from tests.gpu_helpers import assert_close, device_status
+    from tests.test_contig import _case, _gpu
+    max_t = max(c["lens"]) + 7
+    kc, vc, q, *_ = _case(c["S"], c["H"], c["Hk"], c["D"], max_t, c["lens"], seed=3000 + c["i"])
+    cl = np.array(c["lens"], dtype=np.uint32)
+    scale = float(np.float32(c["D"] ** -0.5))
+    want = oracle.cq_decode(q, kc, vc, cl, num_kv_heads=c["Hk"], max_t=max_t, scale=scale)
+    assert_close(_gpu(kc, vc, q, cl, c["Hk"], max_t, scale, c["pt"]), want, _ids(c))
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("c", _variant_cases(12, 9, [64, 128, 256], [8, 16, 32]), ids=_ids)
+def test_random_fused_append_against_oracle(c):
+    """Fused append + decode (append, then attend): cache words bit for bit, outputs in tolerance."""
+    from tests.gpu_helpers import assert_close, dev_u32, device_status, host_u32, random_case
+    from tests.test_decode_append import _gpu_step, _oracle_step, _rows
+    w, ok_, ov_, _, _ = random_case(c["S"], c["H"], c["Hk"], c["D"], c["B"], c["lens"], seed=4000 + c["i"])
+    q = np.random.default_rng(c["i"]).standard_normal((c["S"], c["R"], c["H"], c["D"])).astype(np.float32)
+    key, value = _rows(c["S"], c["R"], c["Hk"], c["D"], seed=c["i"])
+    want, wk, wv = _oracle_step(w, ok_, ov_, q, key, value)
+    kc, vc = dev_u32(ok_), dev_u32(ov_)
+    got = _gpu_step(w, kc, vc, q, key, value, kernel=c["kernel"], partition_tokens=c["pt"])
+    assert np.array_equal(host_u32(kc), wk) and np.array_equal(host_u32(vc), wv), _ids(c)
+    assert_close(got, want, _ids(c))
+    assert device_status() == 0
