@@ -49,7 +49,7 @@ typedef enum pa_q8_status {
     PA_Q8_OK = 0,
     PA_Q8_EINVAL = -1,        /* a size <= 0, a NULL pointer, H % Hk != 0, D or B not a multiple of 4 */
     PA_Q8_EUNSUPPORTED = -2,  /* valid but without a kernel: head_size not in {64,128,256},
-                                 block_size not a power of two in [4,128], ... */
+                                 block_size not a power of two in [4,1024], ... */
     PA_Q8_EALIGN = -3,        /* a pointer or stride without the alignment stated below */
     PA_Q8_ECUDA = -4,         /* the CUDA runtime refused a launch or query */
     PA_Q8_EWORKSPACE = -5     /* workspace_bytes below pa_q8_decode_workspace_size() */
@@ -71,7 +71,8 @@ typedef enum pa_q8_status {
 typedef struct pa_q8_decode_options {
     int kernel;            /* PA_Q8_KERNEL_*                                           */
     int partition_tokens;  /* context tokens per split-context partition; 0 = automatic;
-                              otherwise a multiple of 128 and of block_size            */
+                              otherwise a multiple of 128 (at most 16384); partitions
+                              need not align with blocks                                */
 } pa_q8_decode_options;
 
 /*
@@ -233,8 +234,9 @@ int pa_q8_decode_rows(float *out, const float *q,
  *                   major); 16-byte aligned, strides multiples of 4 floats
  *   key_cache,
  *   value_cache     written (the new tokens' slots) and read
- * Every other argument, the workspace (pa_q8_decode_rows_workspace_size) and
- * the status codes are those of pa_q8_decode_rows.  A slot whose block id is
+ * Every other argument, the workspace (pa_q8_decode_rows_workspace_size),
+ * the kernel families (each stores the new tokens itself) and the status
+ * codes are those of pa_q8_decode_rows.  A slot whose block id is
  * >= num_blocks is neither written nor read, and flagged
  * PA_Q8_DEV_BAD_BLOCK.
  */
