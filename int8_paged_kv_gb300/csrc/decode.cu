@@ -319,6 +319,256 @@ decode_tc_kernel(Params P) {
     merge_and_store<D>(P, w, ml, accs, SLOTS, HT * 8, accs + SLOTS * HT * 8 * D);
 }
 
+// ============================================== tensor cores, 16 heads per warp
+//
+// For 9 .. 16 (query row, head) pairs per kv head at head sizes 64 / 128
+// (multi-row decodes): the tensor-core tile with two 8-head A tiles per warp
+// (u = 0, 1: virtual heads h0 + 8u + gq).  Every chunk's codes become B
+// fragments once and feed both tiles' MMAs, so the conversion -- most of a
+// warp's instructions -- serves 16 heads without leaving registers.  The q
+// fragments of both tiles live in shared memory; the token scales are read
+// once for both.
+
+template <int D>
+__host__ __device__ constexpr uint32_t tc2_extra_bytes() { return 2u * (D / 16) * 32 * 16; }
+
+template <int D>
+__global__ void __launch_bounds__(PA_Q8_TC_SLOTS * 32, 2)
+decode_tc2_kernel(Params P) {
+    constexpr int SLOTS = PA_Q8_TC_SLOTS;
+    constexpr int RING = tc_ring<D>();
+    constexpr int W = D / 4 + 1;
+    constexpr int NKS = D / 16;
+    constexpr int NT = D / 8;
+    constexpr int NJ = D / 32;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    Work w;
+    if (!setup_work(P, w)) {
+        write_zero_rows<D>(P, w);
+        return;
+    }
+    const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc2_extra_bytes<D>());
+    const int ts = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, cq = lane & 3;
+    const uint32_t bars = smem_addr(smem + L.bars) + 8 * RING * ts;
+    const uint32_t ring = smem_addr(smem + L.ring) + RING * L.slot_bytes * ts;
+    const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
+    uint4 *qf = reinterpret_cast<uint4 *>(smem + L.extra);           // [2][NKS][32]
+    const int nchunks = (w.len + kChunk - 1) / kChunk;
+    const int my_n = ts < nchunks ? (nchunks - ts + SLOTS - 1) / SLOTS : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    if (lane == 0) {
+        for (int k = 0; k < RING; ++k) mbar_init(bars + 8 * k, 1);
+        fence_mbar_init();
+    }
+    if (P.nk) append_tokens<D>(P, w);
+    load_table(P, w, const_cast<uint32_t *>(table));
+
+    bool row_ok[2];
+    int len_row[2];
+    float qk2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        row_ok[u] = 8 * u + gq < w.nh;
+        const int vh = w.h0 + 8 * u + gq;
+        len_row[u] = row_ok[u] ? row_len(P, w, vh) : w.len;
+        // q of this row scaled by 2^-eq into [1, 2) in magnitude, as hi/lo f16
+        // pairs; warp u writes tile u's fragments
+        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok[u] ? vh : w.h0) * D);
+        float mx = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+            const float4 v = row_ok[u] ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        const float down = __uint_as_float((uint32_t)(127 - eq) << 23);
+        qk2[u] = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
+        if (ts == u) {
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) {
+                const float4 v = row_ok[u] ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t f0, f1, f2, f3;
+                split_f16x2(v.x * down, v.y * down, f0, f1);
+                split_f16x2(v.z * down, v.w * down, f2, f3);
+                qf[(u * NKS + ks) * 32 + lane] = make_uint4(f0, f1, f2, f3);
+            }
+        }
+    }
+    __syncthreads();
+
+    int issued = 0;
+    for (; issued < RING && issued < my_n; ++issued)
+        issue_chunk<D>(P, w, table, ts + SLOTS * issued, ring + issued * L.slot_bytes, bars + 8 * issued, policy);
+    const int len_min = __reduce_min_sync(0xFFFFFFFFu, (unsigned)min(len_row[0], len_row[1]));
+
+    float acc[2][NT][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[u][n][0] = acc[u][n][1] = acc[u][n][2] = acc[u][n][3] = 0.0f;
+    float m[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.0f, 0.0f};
+    int E[2] = {12, 12};
+    float wscale[2];
+    wscale[0] = wscale[1] = __uint_as_float((uint32_t)(kVScaleBias + 127 - 12) << 23);
+
+    const F16Consts fk;
+    bool ok = true;
+    int i = 0;
+    for (; i < my_n; ++i) {
+        const int k = i % RING;
+        if (!mbar_wait(bars + 8 * k, (i / RING) & 1)) {
+            if (lane == 0) flag_error(P.status, kDevWaitTimeout);
+            ok = false;
+            break;
+        }
+        const uint32_t *sK = reinterpret_cast<const uint32_t *>(smem + L.ring) + (RING * ts + k) * (L.slot_bytes / 4);
+        const uint32_t *sV = sK + kChunk * W;
+        const int t0 = (ts + SLOTS * i) * kChunk;
+        const bool full = t0 + kChunk <= len_min;
+
+        // ---- S = Q K^T for both tiles from one conversion of the codes
+        float s[2][4][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[u][j][0] = s[u][j][1] = s[u][j][2] = s[u][j][3] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+            const int wd = kword<D>(cq, ks);
+            const uint4 f0 = qf[ks * 32 + lane], f1 = qf[(NKS + ks) * 32 + lane];
+            const uint32_t a0[4] = {f0.x, f0.y, f0.z, f0.w}, a1[4] = {f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t b0, b1;
+                codes4_to_f16x2(sK[(8 * j + gq) * W + wd], b0, b1, fk);
+                mma_16816(s[0][j], a0, b0, b1);
+                mma_16816(s[1][j], a1, b0, b1);
+            }
+        }
+        // ---- online softmax per tile over this thread's 8 tokens 8j + 2cq + e
+        float ksv[8], vsv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = 8 * j + 2 * cq + e;
+                ksv[2 * j + e] = __uint_as_float(sK[t * W + D / 4]);
+                vsv[2 * j + e] = __uint_as_float(sV[t * W + D / 4]);
+            }
+        uint32_t ap[2][2][4];                 // [tile][k-step][4]: P as hi/lo f16 pairs
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            float z[8], vs[8];
+            float cmax = -INFINITY, vmax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 8 * j + 2 * cq + e;
+                    float zz = (s[u][j][e] + s[u][j][e + 2]) * ksv[2 * j + e] * qk2[u];
+                    float vv = vsv[2 * j + e];
+                    if (!full) {
+                        const bool valid = t0 + t < len_row[u];
+                        zz = valid ? zz : -INFINITY;
+                        vv = valid ? vv : 0.0f;
+                    }
+                    z[2 * j + e] = zz;
+                    vs[2 * j + e] = vv;
+                    cmax = fmaxf(cmax, zz);
+                    vmax = fmaxf(vmax, vv);
+                }
+            }
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 1));
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 2));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 1));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 2));
+            const int Ec = (int)(__float_as_uint(vmax) >> 23);
+            if (__any_sync(0xFFFFFFFFu, cmax > m[u] + (float)kLazy || Ec > E[u])) {
+                const float m_new = fmaxf(m[u], cmax);
+                const int E_new = max(E[u], Ec);
+                const float alpha = (m[u] == -INFINITY) ? 0.0f : fast_exp2(m[u] - m_new);
+                const float ea = (E[u] - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E[u] - E_new) << 23);
+                const float fa = alpha * ea;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    acc[u][n][0] *= fa; acc[u][n][1] *= fa; acc[u][n][2] *= fa; acc[u][n][3] *= fa;
+                }
+                lsum[u] *= alpha;
+                m[u] = m_new;
+                E[u] = E_new;
+                wscale[u] = __uint_as_float((uint32_t)(kVScaleBias + 127 - E[u]) << 23);
+            }
+            const float m_ref = m[u] == -INFINITY ? 0.0f : m[u];
+            float pw[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float p = fast_exp2(z[x] - m_ref);
+                lsum[u] += p;
+                pw[x] = p * vs[x] * wscale[u];
+            }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                split_f16x2(pw[4 * kk + 0], pw[4 * kk + 1], ap[u][kk][0], ap[u][kk][1]);
+                split_f16x2(pw[4 * kk + 2], pw[4 * kk + 3], ap[u][kk][2], ap[u][kk][3]);
+            }
+        }
+        // ---- O += P V for both tiles from one conversion of the codes
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t *r0 = sV + (16 * kk + 2 * cq) * W;
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+                const int wd = vword<D>(gq, jj);
+                const uint32_t x0 = r0[wd], x1 = r0[W + wd], x8 = r0[8 * W + wd], x9 = r0[9 * W + wd];
+                uint32_t b[4][2];
+                b[0][0] = codes_pair_to_f16x2<0>(x0, x1, fk); b[0][1] = codes_pair_to_f16x2<0>(x8, x9, fk);
+                b[1][0] = codes_pair_to_f16x2<1>(x0, x1, fk); b[1][1] = codes_pair_to_f16x2<1>(x8, x9, fk);
+                b[2][0] = codes_pair_to_f16x2<2>(x0, x1, fk); b[2][1] = codes_pair_to_f16x2<2>(x8, x9, fk);
+                b[3][0] = codes_pair_to_f16x2<3>(x0, x1, fk); b[3][1] = codes_pair_to_f16x2<3>(x8, x9, fk);
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    mma_16816(acc[0][4 * jj + e4], ap[0][kk], b[e4][0], b[e4][1]);
+                    mma_16816(acc[1][4 * jj + e4], ap[1][kk], b[e4][0], b[e4][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (issued < my_n) {
+            issue_chunk<D>(P, w, table, ts + SLOTS * issued, ring + k * L.slot_bytes, bars + 8 * k, policy);
+            ++issued;
+        }
+    }
+    drain(P, bars, RING, i, issued);
+
+    if (__syncthreads_or(!ok)) return;
+    float *ml = reinterpret_cast<float *>(smem + L.ring);            // [slot][16][3]
+    float *accs = ml + SLOTS * 16 * 3;                                // [slot][16][D]
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        float l = lsum[u];
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+        const int hl = 8 * u + gq;
+        if (cq == 0) {
+            float *e = ml + (ts * 16 + hl) * 3;
+            e[0] = m[u]; e[1] = l; e[2] = (float)E[u];
+        }
+        float *arow = accs + (ts * 16 + hl) * D;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            arow[4 * vword<D>(2 * cq, n / 4) + (n & 3)] = acc[u][n][0] + acc[u][n][2];
+            arow[4 * vword<D>(2 * cq + 1, n / 4) + (n & 3)] = acc[u][n][1] + acc[u][n][3];
+        }
+    }
+    __syncthreads();
+    merge_and_store<D>(P, w, ml, accs, SLOTS, 16, accs + SLOTS * 16 * D);
+}
+
 // ============================================================== CUDA cores
 //
 // Warp ts owns chunks ts, ts + 4, ... of the partition.  QK: lane = token;
@@ -639,6 +889,12 @@ template <int D>
 cudaError_t launch_tc(const Params &P, cudaStream_t st) {
     constexpr int SLOTS = PA_Q8_TC_SLOTS;
     constexpr int RING = tc_ring<D>();
+    if constexpr (D <= 128) {       // 9 .. 16 pairs: two 8-head tiles per warp
+        if (P.heads_per_cta > 8) {
+            const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc2_extra_bytes<D>());
+            return launch_attn(decode_tc2_kernel<D>, P, L.total, SLOTS * 32, st);
+        }
+    }
     if constexpr (D == 256) {       // 16-head CTAs: head size 256 only (make_plan)
         if (P.heads_per_cta > 8) {
             const Layout L = make_layout(D, SLOTS, RING, P.PT, P.B, tc_extra_bytes<D, 2>());
@@ -703,7 +959,13 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     } else if (a.kernel == kTensorCore && a.contiguous) {
         a.heads_per_cta = r < 8 ? r : 8;                  // the contiguous-cache kernel: one head tile
     } else if (a.kernel == kTensorCore) {
-        const int cap = a.head_size == 256 ? 16 : PA_Q8_TC_MAX_HEADS;
+        // head size 256: 16-head CTAs.  At 64 / 128, more than 8 pairs take the
+        // two-tile kernel (16 per CTA) when it needs fewer CTA-equivalents: a
+        // 16-head CTA costs about 1.75 eight-head ones (measured on the
+        // 256-sequence batch at 16 pairs), so 24 or 40 pairs stay on 8-head CTAs
+        const int n8 = (r + 7) / 8, n16 = (r + 15) / 16;
+        const bool wide = PA_Q8_TC_WIDE && a.head_size <= 128 && r > 8 && 7 * n16 < 4 * n8;
+        const int cap = (a.head_size == 256 || wide) ? 16 : PA_Q8_TC_MAX_HEADS;
         a.heads_per_cta = r < cap ? r : cap;
     } else {
         int hp = a.kernel == kF32 ? 8 : 16;
@@ -721,7 +983,8 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
                            : a.kernel == kF32       ? 1
                            : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
                            : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
-                                                   : (big_tile ? 1 : 3);
+                           : hd == 256              ? 1
+                                                   : (big_tile ? 2 : 3);
         const int64_t slots = (int64_t)per_sm * num_sms;
         const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
         if (units >= slots) {
@@ -752,7 +1015,8 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
                            : a.kernel == kF32       ? 1
                            : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
                            : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
-                                                   : (big_tile ? 1 : 3);
+                           : hd == 256              ? 1
+                                                   : (big_tile ? 2 : 3);
         a.one_wave = np == 1 && (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups <= (int64_t)per_sm * num_sms;
     }
     return true;

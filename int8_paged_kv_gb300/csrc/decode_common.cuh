@@ -82,12 +82,17 @@ constexpr int kUmmaHeads = 64;
 #ifndef PA_Q8_TC_RING_256
 #define PA_Q8_TC_RING_256 2
 #endif
-// Virtual heads per tensor-core CTA for head sizes 64 / 128.  Each head tile
-// converts the chunk's codes itself, so a 16-head CTA does twice the work of
-// an 8-head one on one CTA per SM; two 8-head CTAs (three per SM) finish
-// sooner, their second K/V read mostly served by L2.
+// Virtual heads per one-tile tensor-core CTA (decode_tc_kernel) at head
+// sizes 64 / 128.  Several such CTAs per kv head each read the K/V (the
+// second read mostly from L2) and convert its codes again.
 #ifndef PA_Q8_TC_MAX_HEADS
 #define PA_Q8_TC_MAX_HEADS 8
+#endif
+// More than 8 pairs per kv head at head sizes 64 / 128 may instead take the
+// two-tile kernel (decode_tc2_kernel: 16 heads per CTA, one conversion for
+// both tiles); 0 keeps every group on one-tile CTAs
+#ifndef PA_Q8_TC_WIDE
+#define PA_Q8_TC_WIDE 1
 #endif
 #ifndef PA_Q8_TC_MINB_128
 #define PA_Q8_TC_MINB_128 3                // CTAs per SM the register budget targets
