@@ -67,8 +67,10 @@ constexpr int kChunk = 32;                 // tokens per warp chunk
 constexpr int kLazy = 8;                   // rescale only when a logit passes the reference max by 2^8
 constexpr int kVScaleBias = 131;           // weights carry 2^(131 - E): p * vs * 2^(131-E) < 2^13
 
-// (row, head) pairs one tcgen05 CTA serves
+// (row, head) pairs one tcgen05 CTA serves; the automatic plan takes tcgen05
+// above kUmmaAutoPairs pairs per kv head
 constexpr int kUmmaHeads = 64;
+constexpr int kUmmaAutoPairs = 32;
 
 #ifndef PA_Q8_TC_SLOTS
 #define PA_Q8_TC_SLOTS 4                   // token-slot warps per head tile
