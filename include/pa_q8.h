@@ -153,8 +153,7 @@ int pa_q8_decode(float *out, const float *q,
  *   - Sizes whose partials exceed the buffer return PA_Q8_EWORKSPACE
  *     (pa_q8_decode_workspace_size() gives the bytes a shape needs).
  *   - The first call on a device looks up the buffer's device address
- *     (cudaGetSymbolAddress) with that device current; make it before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) with that device current and caches it.
  *   - All calls on a device share the buffer: calls whose work overlaps on
  *     the GPU (different streams, concurrent launches) race on it.  The
  *     buffer keeps the previous call's contents, none of which is read as
