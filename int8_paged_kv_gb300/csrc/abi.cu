@@ -503,10 +503,9 @@ int pa_q8_selftest_wait_timeout(uint32_t timeout_us, void *stream) {
 // the first call on each device looks the address up with
 // cudaGetSymbolAddress while that device is current and caches it.  All
 // calls on a device share the buffer, and calls whose kernels overlap on the
-// GPU race on it.  The buffer
-// keeps the previous call's partials; nothing in it needs to start at zero,
-// since every partial the combine step reads is written earlier in the same
-// call.
+// GPU race on it.  The buffer keeps the previous call's partials; nothing in
+// it needs to start at zero, since every partial the combine step reads is
+// written earlier in the same call.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = PA_Q8_NOALLOC_SCRATCH_BYTES;
