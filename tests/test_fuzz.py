@@ -13,7 +13,7 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def _cases(n=24, seed=2026):
+def _cases(n=64, seed=2026):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
@@ -87,7 +87,7 @@ def _ids(c):
     return f"{c['i']}-D{c['D']}-H{c['H']}-Hk{c['Hk']}-B{c['B']}-S{c['S']}-R{c['R']}-k{c['kernel']}-pt{c['pt']}"
 
 
-@pytest.mark.parametrize("c", _variant_cases(12, 7, [64, 128, 256], [8, 16, 32, 64]), ids=_ids)
+@pytest.mark.parametrize("c", _variant_cases(20, 7, [64, 128, 256], [8, 16, 32, 64]), ids=_ids)
 def test_random_f32_cache_against_oracle(c):
     """The f32 cache (oracle.reshape_and_cache_f32 / decode_f32): writer bit for bit, decode in tolerance."""
     from tests.gpu_helpers import assert_close, device_status
@@ -97,7 +97,7 @@ def test_random_f32_cache_against_oracle(c):
     assert device_status() == 0
 
 
-@pytest.mark.parametrize("c", _variant_cases(12, 8, [128, 256], [16]), ids=_ids)
+@pytest.mark.parametrize("c", _variant_cases(20, 8, [128, 256], [16]), ids=_ids)
 def test_random_contiguous_cache_against_oracle(c):
     """The contiguous q8 cache (oracle.cq_append / cq_decode), max_t past the longest context."""
     import oracle
@@ -112,7 +112,7 @@ def test_random_contiguous_cache_against_oracle(c):
     assert device_status() == 0
 
 
-@pytest.mark.parametrize("c", _variant_cases(12, 9, [64, 128, 256], [8, 16, 32]), ids=_ids)
+@pytest.mark.parametrize("c", _variant_cases(20, 9, [64, 128, 256], [8, 16, 32]), ids=_ids)
 def test_random_fused_append_against_oracle(c):
     """Fused append + decode (append, then attend): cache words bit for bit, outputs in tolerance."""
     from tests.gpu_helpers import assert_close, dev_u32, device_status, host_u32, random_case
