@@ -43,6 +43,7 @@ WORKLOAD = "large"
 METRIC = "q8 paged decode: effective KV HBM GB/s (% of GB300 peak) and seqs/s"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20          # read (not written) between steps: evicts L2 with clean lines
+NOMINAL_HBM_GBS = 8000.0            # GB300 HBM3e, nominal ~8 TB/s (reported beside the measured copy peak)
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
@@ -370,6 +371,7 @@ def run_ours(args) -> None:
         ev_d1.record(stream)
 
     bytes_w = wl.algorithmic_writer_bytes(Hk, D, a.slot_mapping)
+    rows_w = int(np.count_nonzero(a.slot_mapping != wl.PAD_SLOT))    # token rows the writer stores
     bytes_d = wl.algorithmic_decode_bytes(cfg, w.context_lens)
     # writer, prep (sequence order; skipped when every CTA of a one-partition
     # plan is resident at once), attention (combine fused in)
@@ -514,11 +516,16 @@ def run_ours(args) -> None:
                          "step starts with an L2 of clean foreign lines; the decode reads 1.6 GB of KV "
                          "per step"},
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "seqs_per_s": round(world * S / (ms_per_step * 1e-3), 1),
         "decode": {"ms": round(dec_avg_ms, 4), "gbps": round(dec_gbs, 1),
+                   "pct_of_hbm_peak": round(100 * dec_gbs / peaks["hbm_gbs"], 2),
+                   "pct_of_nominal_hbm": round(100 * dec_gbs / NOMINAL_HBM_GBS, 2),
+                   "seqs_per_s": round(S / (dec_avg_ms * 1e-3), 1),
                    "algorithmic_bytes": int(bytes_d)},
         "writer": {"ms": round(sum(wr_ms) / len(wr_ms), 4),
                    "gbps": round(bytes_w / (sum(wr_ms) / len(wr_ms) * 1e-3) / 1e9, 1),
+                   "tokens_per_s": round(rows_w / (sum(wr_ms) / len(wr_ms) * 1e-3), 1),
                    "algorithmic_bytes": int(bytes_w)},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
@@ -587,7 +594,8 @@ def run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks) -> No
                           "cpu_oracle_gbps": args.oracle_rates["append"],
                           "new_tokens": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                           "gbps": round(nbytes / ms / 1e6, 1),
-                          "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1)}),
+                          "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                          "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1)}),
               flush=True)
 
 
@@ -632,6 +640,7 @@ def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
                       "cpu_oracle_gbps": args.oracle_rates["f32"],
                       "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                      "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1),
                       "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
     del kc, vc
     torch.cuda.empty_cache()
@@ -747,6 +756,7 @@ def run_contig_line(args, name, w, cl, q, flush, sink, peaks) -> None:
                       "kernel": "tensor-core (32-element group scales)", "ms": round(ms, 4),
                       "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                      "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1),
                       "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
     del kc, vc
     torch.cuda.empty_cache()
@@ -854,6 +864,14 @@ def oracle_rates(w, n: int) -> dict:
         out[name] = round(nbytes / (time.perf_counter() - t0) / 1e9, 4)
     rate("q8", lambda: oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args),
          wl.algorithmic_decode_bytes(scfg, sub.context_lens))
+    if cfg.name in ("tiny", "llama8b", "edge"):          # also on one host core
+        cores = oracle.num_threads()
+        oracle.set_num_threads(1)
+        try:
+            rate("q8_one_core", lambda: oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args),
+                 wl.algorithmic_decode_bytes(scfg, sub.context_lens))
+        finally:
+            oracle.set_num_threads(cores)
     for R in (4, 8):
         qr = np.ascontiguousarray(wl.query_rows(w, R)[:n])
         rate(f"rows{R}", lambda: oracle.decode_rows(qr, kc, vc, sub.block_tables, sub.context_lens, **args),
@@ -976,6 +994,7 @@ def run_configs(args) -> None:
                               "partition_tokens": plan["partition_tokens"], "ms": round(ms, 4),
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
+                              "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1),
                               "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
         if name in ("llama8b", "large"):
             run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks)

@@ -49,6 +49,7 @@ def _load():
         P = ctypes.c_void_p
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.oracle_num_threads.restype = i32
+        lib.oracle_set_num_threads.argtypes = [i32]
         lib.oracle_quantize_vector.argtypes = [P, i32, P]
         lib.oracle_reshape_and_cache.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32]
         lib.oracle_decode_partial.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64,
@@ -75,6 +76,11 @@ def _need(a, dtype, name):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the parallel loops from now on (results do not depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def quantize_vector(x: np.ndarray) -> np.ndarray:

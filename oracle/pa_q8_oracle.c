@@ -83,6 +83,17 @@ static int quantise_one(float t)
     return (int)r;
 }
 
+/* Threads the parallel loops use from now on (rows are independent, so the
+ * count changes no result); n <= 0 leaves it unchanged. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
