@@ -231,6 +231,37 @@ class OracleBench:
                 "sample_bytes": wbytes + dbytes, "cores": self.oracle.num_threads()}
 
 
+def check_parity(ob, w, out, kc, vc) -> dict:
+    """Sampled parity of the timed step's results against the oracle, once,
+    before the timed loop: decode rows (all heads of the longest, the
+    shortest and two seeded sequences) within 1e-5 + 1e-4 |oracle|, and the
+    first 128 stored appended rows' cache words bit for bit (they go to free
+    slots, which no sequence reads)."""
+    import torch
+    cfg, a = w.cfg, w.append
+    H, Hk, B = cfg.num_heads, cfg.num_kv_heads, cfg.block_size
+    lens = w.context_lens
+    seqs = {int(np.argmax(lens)), int(np.argmin(lens))}
+    seqs |= {int(x) for x in np.random.default_rng(7).choice(cfg.num_seqs, 2, replace=False)}
+    seqs = sorted(seqs)
+    rows = np.array([[s, h] for s in seqs for h in range(H)], dtype=np.int32)
+    want = ob.oracle.decode(w.q, ob.kc, ob.vc, w.block_tables, w.context_lens, num_kv_heads=Hk,
+                            block_size=B, scale=w.scale, rows=rows)
+    got = out.cpu().numpy()[rows[:, 0], rows[:, 1]].astype(np.float64)
+    ratio = float(np.max(np.abs(got - want) / (1e-5 + 1e-4 * np.abs(want))))
+    idx = np.nonzero(a.slot_mapping != wl.PAD_SLOT)[0][:128]
+    sm = a.slot_mapping[idx]
+    ob.oracle.reshape_and_cache(np.ascontiguousarray(a.key_view()[idx]), np.ascontiguousarray(a.value_view()[idx]),
+                                ob.kc, ob.vc, sm, num_kv_heads=Hk, head_size=cfg.head_size, block_size=B)
+    blk, off = (sm // B).astype(np.int64), (sm % B).astype(np.int64)
+    tb, to = torch.from_numpy(blk).to(kc.device), torch.from_numpy(off).to(kc.device)
+    same = (np.array_equal(kc[tb, :, to, :].cpu().numpy().view(np.uint32), ob.kc[blk, :, off, :]) and
+            np.array_equal(vc[tb, :, to, :].cpu().numpy().view(np.uint32), ob.vc[blk, :, off, :]))
+    return {"decode_rows": int(len(rows)), "sequences": seqs, "max_err_over_bound": round(ratio, 4),
+            "writer_vectors": int(len(idx)) * Hk * 2, "writer_bit_exact": bool(same),
+            "ok": bool(ratio <= 1.0 and same)}
+
+
 def cpu_line_fields(samp: dict, step_bytes_w: int, step_bytes_d: int) -> dict:
     t_step = samp["writer_s_per_byte"] * step_bytes_w + samp["decode_s_per_byte"] * step_bytes_d
     return {"value": round((step_bytes_w + step_bytes_d) / t_step / 1e9, 4), "unit": UNIT,
@@ -386,6 +417,11 @@ def run_ours(args) -> None:
         flush_l2()
         step()
     torch.cuda.synchronize()
+    # the warm-up steps' results against the oracle, before anything is timed
+    parity = check_parity(ob, w, out, kc, vc) if ob is not None else None
+    if parity is not None and not parity["ok"]:
+        print(json.dumps({"parity": parity}), flush=True)
+        raise SystemExit("bench: the step's results do not match the oracle")
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -537,6 +573,7 @@ def run_ours(args) -> None:
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "parity": parity,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)
