@@ -627,8 +627,9 @@ def run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks) -> No
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
         ms = float(np.median(ts))
+        par = parity_fields(args, "append", out4.view(S, H, D))
         print(json.dumps({"kind": "decode step with append", "workload": name, "step": label,
-                          "cpu_oracle_gbps": args.oracle_rates["append"],
+                          "cpu_oracle_gbps": args.oracle_rates["append"], **par,
                           "new_tokens": S, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                           "gbps": round(nbytes / ms / 1e6, 1),
                           "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
@@ -673,8 +674,9 @@ def run_f32_line(args, name, w, bt, cl, q, flush, sink, peaks) -> None:
         ts.append(a.elapsed_time(b))
     ms = float(np.median(ts))
     nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="f32")
+    par = parity_fields(args, "f32", out)
     print(json.dumps({"kind": "decode per workload, f32 cache", "workload": name, "kernel": "f32 cuda-core",
-                      "cpu_oracle_gbps": args.oracle_rates["f32"],
+                      "cpu_oracle_gbps": args.oracle_rates["f32"], **par,
                       "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
                       "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1),
@@ -788,8 +790,9 @@ def run_contig_line(args, name, w, cl, q, flush, sink, peaks) -> None:
         ts.append(a.elapsed_time(b))
     ms = float(np.median(ts))
     nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens, cache="q8c")
+    par = parity_fields(args, "contig", out)
     print(json.dumps({"kind": "decode per workload, contiguous q8 cache", "workload": name,
-                      "cpu_oracle_gbps": args.oracle_rates["contig"],
+                      "cpu_oracle_gbps": args.oracle_rates["contig"], **par,
                       "kernel": "tensor-core (32-element group scales)", "ms": round(ms, 4),
                       "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                       "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
@@ -893,12 +896,14 @@ def oracle_rates(w, n: int) -> dict:
     oracle.reshape_and_cache(k, v, kc, vc, sm, num_kv_heads=Hk, head_size=D, block_size=B)
     q = np.ascontiguousarray(sub.q[:n])
     args = dict(num_kv_heads=Hk, block_size=B, scale=sub.scale)
-    out = {}
+    out, refs = {}, {}
 
     def rate(name, fn, nbytes):
         t0 = time.perf_counter()
-        fn()
+        res = fn()
         out[name] = round(nbytes / (time.perf_counter() - t0) / 1e9, 4)
+        if res is not None and name not in refs:
+            refs[name] = res
     rate("q8", lambda: oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args),
          wl.algorithmic_decode_bytes(scfg, sub.context_lens))
     if cfg.name in ("tiny", "llama8b", "edge"):          # also on one host core
@@ -934,12 +939,25 @@ def oracle_rates(w, n: int) -> dict:
 
     def append_decode():
         oracle.reshape_and_cache(nk, nv, kc, vc, nslots, num_kv_heads=Hk, head_size=D, block_size=B)
-        oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args)
+        return oracle.decode(q, kc, vc, sub.block_tables, sub.context_lens, **args)
     rate("append", append_decode, wl.algorithmic_decode_bytes(scfg, sub.context_lens) +
          wl.algorithmic_writer_bytes(Hk, D, nslots))
     out["sample"] = f"first {n} sequences ({int(sub.context_lens.sum())} context tokens), fp64 C oracle"
     out["cores"] = oracle.num_threads()
+    out["_refs"] = refs              # the oracle's outputs for these sequences (parity of the GPU lines)
     return out
+
+
+def parity_fields(args, variant: str, got) -> dict:
+    """|gpu - oracle| / (1e-5 + 1e-4 |oracle|) at its largest over the oracle
+    sample's sequences (the first rows of `got`); a value above 1 ends the
+    report with an error once the line is printed."""
+    want = args.oracle_rates["_refs"][variant]
+    g = got[:want.shape[0]].detach().cpu().numpy().astype(np.float64).reshape(want.shape)
+    ratio = float(np.max(np.abs(g - want) / (1e-5 + 1e-4 * np.abs(want))))
+    if not ratio <= 1.0:
+        args.parity_failures.append(variant)
+    return {"parity_max_err_over_bound": round(ratio, 4), "parity_sequences": int(want.shape[0])}
 
 
 def run_configs(args) -> None:
@@ -958,12 +976,14 @@ def run_configs(args) -> None:
     peaks = measured_peaks()
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     sink = torch.empty((), dtype=torch.int32, device=dev)
+    args.parity_failures = []
     for name in wl.CONFIGS:
         w = wl.build(name, with_append=False)
         cfg = w.cfg
         ora = oracle_rates(w, {"tiny": 2, "llama8b": 4, "long": 1, "large": 8, "edge": 8}[name])
         args.oracle_rates = ora
-        print(json.dumps({"kind": "cpu oracle sample", "workload": name, **ora}), flush=True)
+        print(json.dumps({"kind": "cpu oracle sample", "workload": name,
+                          **{k: v for k, v in ora.items() if k != "_refs"}}), flush=True)
         S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
 
         def u32(x):
@@ -1024,6 +1044,7 @@ def run_configs(args) -> None:
                 torch.cuda.synchronize()
                 ts.append(a.elapsed_time(b))
             ms = float(np.median(ts))
+            par = parity_fields(args, "q8" if R == 1 else f"rows{R}", out if R == 1 else outr)
             print(json.dumps({"kind": "decode per workload", "workload": name, "description": cfg.description,
                               "query_rows": R,
                               "kernel": {1: "cuda-core", 2: "tensor-core", 3: "tcgen05"}[kernel],
@@ -1032,11 +1053,13 @@ def run_configs(args) -> None:
                               "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
                               "pct_of_hbm_peak": round(100 * nbytes / ms / 1e6 / peaks["hbm_gbs"], 1),
                               "pct_of_nominal_hbm": round(100 * nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 1),
-                              "seqs_per_s": round(S / (ms * 1e-3), 1)}), flush=True)
+                              "seqs_per_s": round(S / (ms * 1e-3), 1), **par}), flush=True)
         if name in ("llama8b", "large"):
             run_append_lines(args, name, w, kc, vc, bt, cl, q, flush, sink, peaks)
         del kc, vc, q, out
         torch.cuda.empty_cache()
+    if args.parity_failures:
+        raise SystemExit(f"bench --configs: results outside the oracle tolerance: {args.parity_failures}")
 
 
 def main():
