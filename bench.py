@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -138,8 +139,8 @@ class ClockSampler:
             self._thread = threading.Thread(target=self._poll, daemon=True)
             self._thread.start()
         else:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self._smi_path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            fd, self._smi_path = tempfile.mkstemp(prefix="pa_q8_clocks_", suffix=".csv")
+            os.close(fd)
             self._smi = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=timestamp,clocks.sm,clocks.max.sm,"
                  "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "100"],
@@ -154,13 +155,15 @@ class ClockSampler:
             self._smi.terminate()
             self._smi.wait()
             src = "nvidia-smi"
-            for line in open(self._smi_path):
-                parts = [p.strip() for p in line.split(",")]
-                try:
-                    self.samples.append((0.0, int(float(parts[1])), int(parts[3], 16)))
-                    self.max_mhz = int(float(parts[2]))
-                except (ValueError, IndexError):
-                    pass
+            with open(self._smi_path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    try:
+                        self.samples.append((0.0, int(float(parts[1])), int(parts[3], 16)))
+                        self.max_mhz = int(float(parts[2]))
+                    except (ValueError, IndexError):
+                        pass
+            os.unlink(self._smi_path)
         else:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         busy = [s for s in self.samples if not (s[2] & 0x1)] or self.samples
