@@ -14,20 +14,25 @@ namespace {
 // cache).  CUDA cores, with the CUDA-core family's streams, softmax and merge.
 //
 // Tiles move with 2-D tensor copies over the cache seen as rows of D floats:
-// one box is 32 floats (128 B) of min(B, 32) rows, copied with the 128-byte
+// one box is 32 floats (128 B) of min(B, 16) rows, copied with the 128-byte
 // swizzle, so 16-byte chunk c of token row t lands at chunk c ^ (t % 8) of
-// that row's 128 bytes.  A chunk buffer holds [D/32 segments][32 tokens][32
-// floats]; lane = token reads of one chunk index by eight lanes then touch
-// eight different bank groups (the rows are 512 B apart at D = 128, which
-// without the swizzle would put all of them in one bank group).
-// Each warp owns chunks ts, ts + SLOTS, ...; the K and V halves of its buffer
-// have their own mbarrier, so the next chunk's keys are in flight during this
-// chunk's PV and its values during the next QK.
+// that row's 128 bytes.  A chunk of 16 tokens keeps a warp's K and V buffers
+// at 2 * 16 * D * 4 bytes, so 12 token-stream warps share an SM at head size
+// 128 (latency hiding for the FMA-bound GQA-8 case).  A buffer holds [D/32
+// segments][16 tokens][32 floats].  QK: lane = (token, half of the head
+// dims); eight lanes reading one chunk index touch eight bank groups thanks
+// to the swizzle, and one shuffle adds the two halves' partial dots.  PV:
+// lane = 4 head dims.  Each warp owns chunks ts, ts + SLOTS, ...; the K and V
+// halves of its buffer have their own mbarrier, so the next chunk's keys are
+// in flight during this chunk's PV and its values during the next QK.
 
+// Token-stream warps per CTA: a warp's K and V chunk buffers take 2 * 16 * D
+// * 4 bytes (16 KB at head size 128), so 12 of them fill about 200 KB.
 template <int D>
-__host__ __device__ constexpr int f32_slots() { return D == 64 ? 8 : (D == 128 ? 6 : 3); }
+__host__ __device__ constexpr int f32_slots() { return D == 256 ? 6 : 12; }
 
-constexpr uint32_t kF32SegBytes = kChunk * 128;        // one 32-float column of a chunk
+constexpr int kF32Chunk = 16;                           // tokens per chunk
+constexpr uint32_t kF32SegBytes = kF32Chunk * 128;      // one 32-float column of a chunk
 
 struct F32Params {
     Params p;
@@ -37,7 +42,7 @@ struct F32Params {
 
 // shared memory beside the buffers: q rows [NH][D], weights [slot][NH][32], row lags [NH]
 template <int D, int NH>
-__host__ __device__ constexpr uint32_t f32_extra() { return NH * D * 4 + f32_slots<D>() * 32 * NH * 4 + NH * 4; }
+__host__ __device__ constexpr uint32_t f32_extra() { return NH * D * 4 + f32_slots<D>() * kF32Chunk * NH * 4 + NH * 4; }
 
 struct F32Layout {
     uint32_t table, extra, ring, half_bytes, total;
@@ -52,26 +57,28 @@ __host__ __device__ inline F32Layout make_f32_layout(int D, int slots, int PT, i
     L.table = align_up(slots * 16, 16);
     L.extra = align_up(L.table + pieces * 4, 128);
     L.ring = align_up(L.extra + extra_bytes, 1024);
-    L.half_bytes = (uint32_t)kChunk * D * 4;
+    L.half_bytes = (uint32_t)kF32Chunk * D * 4;
     L.total = L.ring + 2u * slots * L.half_bytes + 1024u;
     return L;
 }
 
-// Copy the K or V half of chunk c: lane = (piece of min(B, 32) tokens,
-// 32-float column), one tensor copy each.  Pieces past the partition's end
-// or in an out-of-range block are not copied (their rows are never used as
-// values, or the block was flagged by the table walk).
+// Copy the K or V half of chunk c (16 tokens): lane = (piece of min(B, 16)
+// tokens, 32-float column), one tensor copy each.  Pieces past the
+// partition's end or in an out-of-range block are not copied (their rows are
+// never used as values, or the block was flagged by the table walk).  The
+// table holds one block per min(B, 32) tokens, so a piece lies in one entry.
 template <int D>
 __device__ __forceinline__ void issue_f32_half(const Params &P, const Work &w, const uint32_t *table,
                                                const CUtensorMap *tmap, int c, uint32_t dst, uint32_t bar,
                                                uint64_t policy) {
     constexpr int NSEG = D / 32;
     const int lane = threadIdx.x & 31;
+    const int log2f = min(P.log2B, 4);                      // box rows: min(B, 16)
     const int piece = lane / NSEG, seg = lane % NSEG;
-    const int t = c * kChunk + (piece << P.log2ptok);      // partition-relative token
+    const int t = c * kF32Chunk + (piece << log2f);         // partition-relative token
     bool go = false;
     int y = 0;
-    if (piece < (kChunk >> P.log2ptok) && t < w.len) {
+    if (piece < (kF32Chunk >> log2f) && t < w.len) {
         const uint32_t pb = table[t >> P.log2ptok];
         if (pb != kPadSlot) {
             const int off = (w.t_begin + t) & (P.B - 1);
@@ -79,14 +86,14 @@ __device__ __forceinline__ void issue_f32_half(const Params &P, const Work &w, c
             go = true;
         }
     }
-    const uint32_t bytes = go ? 128u << P.log2ptok : 0u;
+    const uint32_t bytes = go ? 128u << log2f : 0u;
     const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bytes);
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
     if (go) {
         fence_proxy_async_smem();
-        tma_load_2d(dst + seg * kF32SegBytes + ((uint32_t)piece << P.log2ptok) * 128u, tmap, seg * 32, y,
-                    bar, policy);
+        tma_load_2d(dst + seg * kF32SegBytes + ((uint32_t)piece << log2f) * 128u, tmap, seg * 32, y, bar,
+                    policy);
     }
 }
 
@@ -100,6 +107,7 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
     constexpr int LW = WORDS < 32 ? WORDS : 32;      // lanes per token row in PV
     constexpr int TG = 32 / LW;                      // token groups in PV (2 for D = 64)
     constexpr int NWL = WORDS / LW;                  // groups per lane in PV
+    constexpr int C = kF32Chunk;
 
     extern __shared__ __align__(128) uint8_t smem[];     // the buffers are aligned to 1024 at run time
     Work w;
@@ -117,9 +125,9 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
     const float *sV = reinterpret_cast<const float *>(smem + (vbuf - s0));
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
     float *sq = reinterpret_cast<float *>(smem + L.extra);                  // [NH][D]
-    float *myw = sq + NH * D + ts * 32 * NH;                                // [NH][32]
-    int *slag = reinterpret_cast<int *>(sq + NH * D + SLOTS * 32 * NH);     // [NH]
-    const int nchunks = (w.len + kChunk - 1) / kChunk;
+    float *myw = sq + NH * D + ts * C * NH;                                 // [NH][C]
+    int *slag = reinterpret_cast<int *>(sq + NH * D + SLOTS * C * NH);      // [NH]
+    const int nchunks = (w.len + C - 1) / C;
     const int my_n = ts < nchunks ? (nchunks - ts + SLOTS - 1) / SLOTS : 0;
     const uint64_t policy = l2_policy_evict_first();
 
@@ -154,28 +162,33 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
     }
 
     bool ok = true;
-    const int rsw = lane & 7;                        // swizzle phase of this lane's row in QK
+    // QK: lane = (token tl of the chunk, half dh of the head dims); the two
+    // halves' partial dots are summed with one shuffle, so both hold the
+    // logits and the softmax below stays warp-uniform
+    const int tl = lane & (C - 1), dh = lane >> 4;
+    const int rsw = tl & 7;                          // swizzle phase of this lane's row
     for (int i = 0; i < my_n; ++i) {
         const int c = ts + SLOTS * i;
-        const int t0 = c * kChunk;
+        const int t0 = c * C;
         if (!mbar_wait(kbar, i & 1)) {
             if (lane == 0) flag_error(P.status, kDevWaitTimeout);
             ok = false;
             break;
         }
         ++k_done;
-        // ---- logits, lane = token
-        const bool valid = t0 + lane < w.len;
-        const int ahead = w.c - w.t_begin - t0 - lane;         // tokens from this one to the context end
+        // ---- logits
+        const bool valid = t0 + tl < w.len;
+        const int ahead = w.c - w.t_begin - t0 - tl;           // tokens from this one to the context end
         float dot[NH];
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh) dot[hh] = 0.0f;
-        const float *krow = sK + lane * 32;
+        const float *krow = sK + tl * 32;
 #pragma unroll
-        for (int sg = 0; sg < NSEG; ++sg) {
+        for (int sh = 0; sh < NSEG / 2; ++sh) {
+            const int sg = dh * (NSEG / 2) + sh;
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 kv = *reinterpret_cast<const float4 *>(krow + sg * (kChunk * 32) + ((q4 ^ rsw) << 2));
+                const float4 kv = *reinterpret_cast<const float4 *>(krow + sg * (C * 32) + ((q4 ^ rsw) << 2));
 #pragma unroll
                 for (int hh = 0; hh < NH; ++hh) {
                     const float4 qv = sq4[hh * WORDS + sg * 8 + q4];
@@ -183,6 +196,8 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
                 }
             }
         }
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) dot[hh] += __shfl_xor_sync(0xFFFFFFFFu, dot[hh], 16);
         __syncwarp();
         if (i + 1 < my_n) {            // keys consumed: the next chunk's keys into the same half
             issue_f32_half<D>(P, w, table, &FP.tk, c + SLOTS, kbuf, kbar, policy);
@@ -194,9 +209,9 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
             const float z = seen ? dot[hh] * P.scale_log2 : -INFINITY;
             float cm = z;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+            for (int o = C / 2; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
             const float m_new = fmaxf(m[hh], cm);
-            if (m_new != m[hh]) {        // warp-uniform
+            if (m_new != m[hh]) {        // warp-uniform: both halves hold the same logits
                 const float alpha = (m[hh] == -INFINITY) ? 0.0f : fast_exp2(m[hh] - m_new);
                 lsum[hh] *= alpha;
 #pragma unroll
@@ -207,8 +222,8 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
                 m[hh] = m_new;
             }
             const float p = seen ? fast_exp2(z - m[hh]) : 0.0f;
-            lsum[hh] += p;
-            myw[hh * 32 + lane] = p;
+            lsum[hh] += p;                                    // each half counts its 16 tokens once
+            if (dh == 0) myw[hh * C + tl] = p;
         }
         __syncwarp();
         if (!mbar_wait(vbar, i & 1)) {
@@ -218,7 +233,7 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
         }
         ++v_done;
         // ---- weighted sum, lane = 4 head dims; only tokens inside the context
-        const int ntok = min(kChunk, w.len - t0);
+        const int ntok = min(C, w.len - t0);
         const int tg = lane / LW, lw = lane % LW;
 #pragma unroll 2
         for (int tt = tg; tt < ntok; tt += TG) {
@@ -227,12 +242,12 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
 #pragma unroll
             for (int u = 0; u < NWL; ++u) {
                 const int g4 = lw + 32 * u;                     // 16-byte group: column g4 / 8, chunk g4 % 8
-                v[u] = *reinterpret_cast<const float4 *>(vrow + (g4 >> 3) * (kChunk * 32) +
+                v[u] = *reinterpret_cast<const float4 *>(vrow + (g4 >> 3) * (C * 32) +
                                                          (((g4 & 7) ^ (tt & 7)) << 2));
             }
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh) {
-                const float wt = myw[hh * 32 + tt];
+                const float wt = myw[hh * C + tt];
 #pragma unroll
                 for (int u = 0; u < NWL; ++u) {
                     acc[hh][u][0] = fmaf(wt, v[u].x, acc[hh][u][0]);
@@ -261,9 +276,9 @@ decode_f32_kernel(const __grid_constant__ F32Params FP) {
     float *accs = ml + SLOTS * NH * 3;                          // [slot][NH][D]
 #pragma unroll
     for (int hh = 0; hh < NH; ++hh) {
-        float l = lsum[hh];
+        float l = lsum[hh];                 // each half holds the sums of all 16 token lanes
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+        for (int o = C / 2; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
 #pragma unroll
         for (int u = 0; u < NWL; ++u) {
 #pragma unroll
@@ -308,7 +323,7 @@ EncodeTiledFn tensor_map_encoder() {
 }
 
 // An f32 cache [num_blocks * Hk * B rows][D] as a 2-D tensor with boxes of
-// 32 floats x min(B, 32) rows and the 128-byte swizzle.
+// 32 floats x min(B, 16) rows and the 128-byte swizzle.
 bool encode_f32_cache_map(CUtensorMap *map, const void *cache, int64_t rows, int D, int ptok) {
     const EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return false;
@@ -333,7 +348,7 @@ cudaError_t launch_f32(const Params &P, cudaStream_t st) {
     std::memset(&FP, 0, sizeof FP);
     FP.p = P;
     const int64_t rows = P.num_blocks * P.Hk * P.B;
-    const int ptok = 1 << P.log2ptok;
+    const int ptok = 1 << (P.log2B < 4 ? P.log2B : 4);     // box rows: min(B, 16)
     if (!encode_f32_cache_map(&FP.tk, P.kc, rows, D, ptok) || !encode_f32_cache_map(&FP.tv, P.vc, rows, D, ptok))
         return cudaErrorNotSupported;
     switch (P.heads_per_cta) {
