@@ -44,6 +44,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-I", include, "-Xcompiler", "-fPIC",
                     "-Xcompiler", "-O2"]
     flags += os.environ.get("PA_Q8_NVCC_FLAGS", "").split()
+    # objects built with other flags (PA_Q8_NVCC_FLAGS) are stale whatever their times
+    stamp = os.path.join(BUILD, "flags.txt")
+    key = " ".join([cc] + flags)
+    try:
+        with open(stamp) as f:
+            force = force or f.read() != key
+    except OSError:
+        force = True
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -69,6 +77,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp, "w") as f:
+            f.write(key)
     return LIB
 
 

@@ -880,6 +880,7 @@ Params make_params(const DecodeArgs &a) {
     P.nk = a.new_key; P.nv = a.new_value;
     P.nk_stride = a.new_key_stride; P.nv_stride = a.new_value_stride;
     P.contiguous = a.contiguous;
+    P.per_sm = a.per_sm;
     P.kc_w = const_cast<uint32_t *>(a.key_cache);      // written only by the fused append
     P.vc_w = const_cast<uint32_t *>(a.value_cache);
     return P;
@@ -944,6 +945,17 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
     return (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
 }
 
+// CTAs of the chosen kernel resident per SM (registers and shared memory as
+// built): the partition planner sizes its waves and the one-wave test by it.
+int resident_per_sm(const DecodeArgs &a) {
+    const int hd = a.head_size;
+    if (hd == 256) return 1;
+    if (a.contiguous) return 3;
+    if (a.kernel == kF32) return 1;
+    if (a.kernel == kTcgen05 || a.kernel == kCudaCore) return 2;
+    return a.heads_per_cta > 8 ? 2 : 3;
+}
+
 }  // namespace
 
 bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int num_sms) {
@@ -975,19 +987,11 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     }
     a.head_groups = (r + a.heads_per_cta - 1) / a.heads_per_cta;
     const int64_t max_ctx = (int64_t)a.max_blocks_per_seq * a.block_size;
+    const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
+    int per_sm = resident_per_sm(a);
     int pt = requested_partition;
     if (pt <= 0) {
-        // CTAs resident per SM for this kernel configuration
-        const int hd = a.head_size;
-        const bool big_tile = hd == 256 || a.heads_per_cta > 8;
-        const int per_sm = a.contiguous          ? (hd == 256 ? 1 : 2)
-                           : a.kernel == kF32       ? 1
-                           : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
-                           : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
-                           : hd == 256              ? 1
-                                                   : (big_tile ? 2 : 3);
         const int64_t slots = (int64_t)per_sm * num_sms;
-        const int64_t units = (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups;
         if (units >= slots) {
             // Enough (sequence, kv head) work items: one partition per context
             // (up to 8192 tokens).  The grid runs the longest contexts first,
@@ -1009,17 +1013,19 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     const int64_t np = (max_ctx + pt - 1) / pt;
     if (np > 0x7FFFFFFF || np < 1) return false;
     a.num_partitions = (int)np;
-    {
-        const int hd = a.head_size;
-        const bool big_tile = hd == 256 || a.heads_per_cta > 8;
-        const int per_sm = a.contiguous          ? (hd == 256 ? 1 : 2)
-                           : a.kernel == kF32       ? 1
-                           : a.kernel == kTcgen05 ? (hd == 256 ? 1 : 2)
-                           : a.kernel == kCudaCore ? (hd == 256 ? 1 : 2)
-                           : hd == 256              ? 1
-                                                   : (big_tile ? 2 : 3);
-        a.one_wave = np == 1 && (int64_t)a.num_seqs * a.num_kv_heads * a.head_groups <= (int64_t)per_sm * num_sms;
+    if (a.contiguous && a.head_size == 128) {
+        // Two builds of the kernel: 3 CTAs per SM (168 registers) keep more
+        // loads in flight per SM; 2 per SM (no register limit below 255) run
+        // each CTA faster.  With four or more waves of 3 per SM expected
+        // (contexts taken at half their maximum) occupancy wins; with fewer,
+        // the longest CTAs set the time and the faster CTA wins (measured:
+        // 256-sequence lognormal batch 3; 64 x U[512, 4096] and 8 x
+        // U[32K, 128K] contexts 2).
+        const int64_t live = units * std::max<int64_t>(1, (max_ctx / 2 + pt - 1) / pt);
+        per_sm = live >= 4 * 3 * (int64_t)num_sms ? 3 : 2;
     }
+    a.per_sm = per_sm;
+    a.one_wave = np == 1 && units <= (int64_t)per_sm * num_sms;
     return true;
 }
 

@@ -52,6 +52,8 @@ struct Params {
     uint32_t *kc_w;         // the caches, written by the append
     uint32_t *vc_w;
     int contiguous;         // contiguous q8 cache (decode_cq_kernel)
+    int per_sm;             // CTAs per SM the plan sized its waves for (the contiguous
+                            // head-size-128 kernel is built for 2 and for 3)
 };
 
 // Launchers of the families in their own translation units (head sizes

@@ -88,9 +88,11 @@ struct CqTmaParams {
 constexpr uint32_t kCqTmaCodes = kChunk * 128u, kCqTmaScales = kChunk * 16u;
 constexpr uint32_t kCqTmaSlot = 2u * kCqTmaCodes + 2u * kCqTmaScales;      // 9216 = 9 x 1024
 
-// [barriers] [ring, 1024-aligned at run time: slot x ring] (+1024 slack)
+// [barriers] [ring, 1024-aligned at run time: slot x ring]: the ring starts
+// at most 1023 bytes past the barriers.  About 73 KB, so three CTAs can share
+// an SM (the build for three per SM is held to 168 registers for that).
 __host__ __device__ inline uint32_t cq_tma_smem_bytes() {
-    return 1024u + PA_Q8_TC_SLOTS * kCqRing * 8u + PA_Q8_TC_SLOTS * kCqRing * kCqTmaSlot + 1024u;
+    return align_up(PA_Q8_TC_SLOTS * kCqRing * 8u + 1023u + PA_Q8_TC_SLOTS * kCqRing * kCqTmaSlot, 128u);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z, uint32_t bar,
@@ -107,8 +109,9 @@ __device__ __forceinline__ uint32_t sw128(int r, int w) {
     return (uint32_t)(r * 128 + ((((w >> 2) ^ r) & 7) << 4) + (w & 3) * 4);
 }
 
-template <int D>
-__global__ void __launch_bounds__(PA_Q8_TC_SLOTS * 32, 2)
+// MINB: CTAs per SM the build is for (2 or 3; the plan picks one)
+template <int D, int MINB>
+__global__ void __launch_bounds__(PA_Q8_TC_SLOTS * 32, MINB)
 decode_cq_tma_kernel(const __grid_constant__ CqTmaParams CP) {
     static_assert(D == 128, "tensor-copy contiguous decode: head size 128");
     const Params &P = CP.p;
@@ -629,7 +632,9 @@ cudaError_t launch_cq_tma(const Params &P, cudaStream_t st) {
     if (!encode_cq_maps(&CP.kcodes, &CP.kscales, P.kc, P.S, P.Nb, P.Hk) ||
         !encode_cq_maps(&CP.vcodes, &CP.vscales, P.vc, P.S, P.Nb, P.Hk))
         return cudaErrorNotSupported;
-    return launch_attn_arg(decode_cq_tma_kernel<128>, P, CP, cq_tma_smem_bytes(), PA_Q8_TC_SLOTS * 32, st);
+    if (P.per_sm >= 3)
+        return launch_attn_arg(decode_cq_tma_kernel<128, 3>, P, CP, cq_tma_smem_bytes(), PA_Q8_TC_SLOTS * 32, st);
+    return launch_attn_arg(decode_cq_tma_kernel<128, 2>, P, CP, cq_tma_smem_bytes(), PA_Q8_TC_SLOTS * 32, st);
 }
 
 }  // namespace

@@ -59,6 +59,8 @@ struct DecodeArgs {
     int head_groups;       // CTAs per (seq, kv head, partition) along the group
     int one_wave;          // one partition per context and every CTA resident at once: no
                            // ordering and no combine counters, so no prep kernel
+    int per_sm;            // CTAs per SM the waves are sized for (selects the contiguous
+                           // kernel's register budget)
     // workspace: sequence order [S] (u64: clamped length << 32 | sequence,
     // longest context first); when
     // partitions > 1 also arrival counters [S][Hk * head_groups] (u32),

@@ -152,3 +152,26 @@ def test_llama8b_contexts_all_rows():
     got = _gpu(kc, vc, w.q, w.context_lens, Hk, max_t, w.scale)
     assert_close(got, want, "llama8b contiguous")
     assert device_status() == 0
+
+
+def test_many_sequences_three_per_sm_build():
+    """Enough (sequence, kv head) work for four or more waves of three CTAs
+    per SM: the plan takes the head-size-128 kernel's three-per-SM build
+    (the cases above, with few sequences, take the two-per-SM one)."""
+    import torch
+    import oracle
+    from tests.gpu_helpers import assert_close, device_status
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hk, H, D, max_t = 8, 16, 128, 128
+    S = (4 * 3 * sms + Hk - 1) // Hk + 16               # one partition each (max_t <= 8192)
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(0, max_t + 1, size=S)]
+    lens[:4] = [0, 1, max_t, 33]
+    kc, vc, q, *_ = _case(S, H, Hk, D, max_t, lens, seed=12)
+    cl = np.array(lens, dtype=np.uint32)
+    scale = float(np.float32(D ** -0.5))
+    want = oracle.cq_decode(q, kc, vc, cl, num_kv_heads=Hk, max_t=max_t, scale=scale)
+    got = _gpu(kc, vc, q, cl, Hk, max_t, scale)
+    assert_close(got, want, f"S {S}")
+    assert np.all(got[0] == 0.0)
+    assert device_status() == 0
