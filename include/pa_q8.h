@@ -10,6 +10,15 @@
  * void*; NULL = the legacy default stream) and no function synchronises,
  * except pa_q8_device_status which reads a flag back.
  *
+ * Programmatic dependent launch: the writers let the next kernel on the
+ * stream start once all their CTAs run, and a decode's first kernel (its
+ * ordering pass) is launched to take that chance.  That kernel reads only
+ * context_lens before the previous kernel has finished, and waits for it
+ * before anything else; every later step of the decode waits for it in turn.
+ * So context_lens must be final when the kernel before the decode starts,
+ * which stream order gives unless that kernel is itself one (of the caller's)
+ * that writes context_lens and allows early dependents.
+ *
  * Data layout (header comments of the "paged_attn_q8.comp" and
  * "reshape_and_cache_q8.comp" pages, hanzo-ml 0.11.92 / 0.11.93):
  *

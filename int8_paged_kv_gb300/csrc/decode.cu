@@ -778,6 +778,12 @@ decode_cc_kernel(Params P) {
 // holds only short ones.  (length, index) keys in shared memory: ranked by
 // counting for up to blockDim sequences, bitonic-sorted up to kPrepMaxSort;
 // beyond that the order is the identity.
+//
+// Launched as a programmatic dependent of the kernel before it (the library's
+// writers let it start once all their CTAs are running): it reads only the
+// context lengths, which that kernel does not write, and waits for it to
+// finish before writing the workspace.  The attention grid waits for this one,
+// so it sees the writer's cache words too.
 constexpr int kPrepThreads = 1024;
 constexpr int kPrepMaxSort = 8192;
 
@@ -787,8 +793,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
     extern __shared__ unsigned long long keys[];
     // the attention grid may launch now; it waits for this grid's writes
     grid_dependents_launch();
-    for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
     if (S > kPrepMaxSort) {
+        grid_dependency_wait();
+        for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
         for (int i = threadIdx.x; i < S; i += blockDim.x) {
             const int64_t c = min((int64_t)__ldg(context_lens + i), cap);
             order[i] = ((unsigned long long)c << 32) | (unsigned)i;
@@ -820,6 +827,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
             for (int j = part; j < S; j += G) rank += keys[j] < mine;
         }
         for (int o = G >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        grid_dependency_wait();
+        for (int64_t c = threadIdx.x; c < n_counters; c += blockDim.x) counters[c] = 0u;
         if (i < S && part == 0)
             order[rank] = ((unsigned long long)(cap - (int64_t)(mine >> 32)) << 32) | (unsigned)i;
         return;
@@ -840,6 +849,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
             __syncthreads();
         }
     }
+    grid_dependency_wait();
+    for (int64_t i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
     for (int i = threadIdx.x; i < S; i += blockDim.x)
         order[i] = ((unsigned long long)(cap - (int64_t)(keys[i] >> 32)) << 32) | (keys[i] & 0xFFFFFFFFull);
 }
@@ -933,9 +944,19 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
         const size_t smem = (size_t)n * sizeof(unsigned long long);
         cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prep_kernel<<<1, kPrepThreads, smem, st>>>(P.cl, P.S, (int64_t)P.Nb * P.B,
-                                                   const_cast<unsigned long long *>(P.order),
-                                                   P.counters, n_counters);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kPrepThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prep_kernel, P.cl, P.S, (int64_t)P.Nb * P.B,
+                               const_cast<unsigned long long *>(P.order), P.counters, n_counters);
+        if (e != cudaSuccess) return e;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

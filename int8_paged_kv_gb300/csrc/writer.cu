@@ -50,6 +50,9 @@ quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ va
                      const uint32_t *__restrict__ slot_mapping, int num_tokens,
                      int64_t key_stride, int64_t value_stride, int num_kv_heads,
                      int block_size, int log2_block, int64_t num_slots, uint32_t *status) {
+    // a decode launched next may start its prep (which reads only the
+    // context lengths until this grid has finished)
+    grid_dependents_launch();
     constexpr int WORDS = D / 4;
     constexpr int G = kLanesPerVector;
     constexpr int NW = WORDS / G;
@@ -136,6 +139,7 @@ cq_append_kernel(const float *__restrict__ key, const float *__restrict__ value,
                  uint32_t *__restrict__ key_cache, uint32_t *__restrict__ value_cache,
                  const uint32_t *__restrict__ slot_mapping, int num_tokens, int64_t key_stride,
                  int64_t value_stride, int kv_row, int64_t max_t, int64_t num_slots, uint32_t *status) {
+    grid_dependents_launch();
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
     if (tok >= num_tokens) return;
@@ -177,6 +181,7 @@ f32_scatter_kernel(const float *__restrict__ key, const float *__restrict__ valu
                    const uint32_t *__restrict__ slot_mapping, int num_tokens, int64_t key_stride,
                    int64_t value_stride, int num_kv_heads, int log2_block, int64_t num_slots,
                    uint32_t *status) {
+    grid_dependents_launch();
     const int lane = threadIdx.x & 31;
     const int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
     const int h = blockIdx.y;
