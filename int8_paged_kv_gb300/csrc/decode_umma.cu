@@ -260,6 +260,9 @@ decode_umma_kernel(Params P) {
     } else if (warp >= 4) {
         // ---- conversion (96 threads)
         const int ct = tid - 128;
+        static_assert(kUmmaConvThreads % kChunk == 0, "conversion threads: whole warps per token lane");
+        constexpr int kConvColStep = kUmmaConvThreads / kChunk;
+        const int tok = ct % kChunk, col0 = ct / kChunk;
         const F16Consts fk;
         for (int i = 0; i < nch; ++i) {
             const int b = i & 1, k = i % RING;
@@ -268,24 +271,33 @@ decode_umma_kernel(Params P) {
             if (!mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort)) break;
             if (i >= 2 && !mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)) break;   // K tile free
             uint8_t *dK = sK0 + b * K_BYTES;
-            for (int u = ct; u < kChunk * D / 8; u += kUmmaConvThreads) {   // lane = token: 8 bank groups
-                const int t = u % kChunk, c8 = u / kChunk;
-                uint32_t a0, a1, a2, a3;
-                codes4_to_f16x2(rawK[t * W + 2 * c8], a0, a1, fk);
-                codes4_to_f16x2(rawK[t * W + 2 * c8 + 1], a2, a3, fk);
-                *reinterpret_cast<uint4 *>(dK + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
+            // element u = ct + 96k of the [8-code column][token] walk: lane = token
+            // (8 bank groups); 96 is a multiple of 32, so this thread's token is
+            // fixed and its column steps by 3 (128 bytes each in the tile)
+            {
+                const uint32_t *src = rawK + tok * W;
+                uint8_t *dst = dK + kmaj_off(tok, 0, D);
+                for (int c8 = col0; c8 < D / 8; c8 += kConvColStep) {
+                    uint32_t a0, a1, a2, a3;
+                    codes4_to_f16x2(src[2 * c8], a0, a1, fk);
+                    codes4_to_f16x2(src[2 * c8 + 1], a2, a3, fk);
+                    *reinterpret_cast<uint4 *>(dst + 128 * c8) = make_uint4(a0, a1, a2, a3);
+                }
             }
             // V tile and scale table b free: PV(i-2) done, so softmax(i-2) is too
             if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
             if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
             else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
             uint8_t *dV = sV0 + b * V_BYTES;
-            for (int u = ct; u < kChunk * D / 8; u += kUmmaConvThreads) {   // as K: the PV B operand is MN-major
-                const int t = u % kChunk, c8 = u / kChunk;
-                uint32_t a0, a1, a2, a3;
-                codes4_to_f16x2(rawV[t * W + 2 * c8], a0, a1, fk);
-                codes4_to_f16x2(rawV[t * W + 2 * c8 + 1], a2, a3, fk);
-                *reinterpret_cast<uint4 *>(dV + kmaj_off(t, 8 * c8, D)) = make_uint4(a0, a1, a2, a3);
+            {                                                 // as K: the PV B operand is MN-major
+                const uint32_t *src = rawV + tok * W;
+                uint8_t *dst = dV + kmaj_off(tok, 0, D);
+                for (int c8 = col0; c8 < D / 8; c8 += kConvColStep) {
+                    uint32_t a0, a1, a2, a3;
+                    codes4_to_f16x2(src[2 * c8], a0, a1, fk);
+                    codes4_to_f16x2(src[2 * c8 + 1], a2, a3, fk);
+                    *reinterpret_cast<uint4 *>(dst + 128 * c8) = make_uint4(a0, a1, a2, a3);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(kBarConv, b));
