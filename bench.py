@@ -43,7 +43,14 @@ from int8_paged_kv_gb300 import workloads as wl  # noqa: E402
 WORKLOAD = "large"
 METRIC = "q8 paged decode: effective KV HBM GB/s (% of GB300 peak) and seqs/s"
 UNIT = "GB/s"
-L2_FLUSH_BYTES = 256 << 20          # read (not written) between steps: evicts L2 with clean lines
+L2_FLUSH_MIN_BYTES = 256 << 20      # read (not written) between steps: evicts L2 with clean lines
+def l2_flush_bytes(dev) -> int:
+    """Twice the device's L2 (as the driver reports it), at least 256 MiB."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 0)
+    return max(L2_FLUSH_MIN_BYTES, 2 * l2) // 4 * 4
+
+
 NOMINAL_HBM_GBS = 8000.0            # GB300 HBM3e, nominal ~8 TB/s (reported beside the measured copy peak)
 NVML_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                 0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
@@ -386,7 +393,7 @@ def run_ours(args) -> None:
     ws_bytes = pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq, kernel=args.kernel,
                                               partition_tokens=args.partition_tokens)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.ones(l2_flush_bytes(dev) // 4, dtype=torch.int32, device=dev)
     flush_sink = torch.empty((), dtype=torch.int32, device=dev)
 
     def flush_l2():
@@ -977,7 +984,7 @@ def run_configs(args) -> None:
     pkbuild.build()
     dev = torch.device("cuda", 0)
     peaks = measured_peaks()
-    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.ones(l2_flush_bytes(dev) // 4, dtype=torch.int32, device=dev)
     sink = torch.empty((), dtype=torch.int32, device=dev)
     args.parity_failures = []
     for name in wl.CONFIGS:
