@@ -126,3 +126,37 @@ def test_random_fused_append_against_oracle(c):
     assert np.array_equal(host_u32(kc), wk) and np.array_equal(host_u32(vc), wv), _ids(c)
     assert_close(got, want, _ids(c))
     assert device_status() == 0
+
+
+def _many_seq_contig_cases(n=6, seed=10):
+    """Head size 128 with (sequence, kv head) units for four or more waves of
+    three CTAs per SM at 152 SMs (1824): the three-per-SM contiguous build."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        Hk = int(rng.choice([1, 2, 4, 8]))
+        r = int(rng.choice([1, 2, 4, 8]))
+        max_t = int(rng.choice([64, 128, 200]))
+        S = -(-1900 // Hk) + int(rng.integers(0, 40))
+        lens = rng.integers(0, max_t + 1, size=S)
+        lens[:3] = [0, 1, max_t]
+        out.append(dict(i=i, Hk=Hk, H=Hk * r, S=S, max_t=max_t, lens=[int(x) for x in lens],
+                        pt=int(rng.choice([0, 128]))))
+    return out
+
+
+@pytest.mark.parametrize("c", _many_seq_contig_cases(),
+                         ids=lambda c: f"{c['i']}-H{c['H']}-Hk{c['Hk']}-S{c['S']}-T{c['max_t']}-pt{c['pt']}")
+def test_random_many_sequence_contiguous_against_oracle(c):
+    import oracle
+    from tests.gpu_helpers import assert_close, device_status
+    from tests.test_contig import _case, _gpu
+    D = 128
+    kc, vc, q, *_ = _case(c["S"], c["H"], c["Hk"], D, c["max_t"], c["lens"], seed=5000 + c["i"])
+    cl = np.array(c["lens"], dtype=np.uint32)
+    scale = float(np.float32(D ** -0.5))
+    want = oracle.cq_decode(q, kc, vc, cl, num_kv_heads=c["Hk"], max_t=c["max_t"], scale=scale)
+    got = _gpu(kc, vc, q, cl, c["Hk"], c["max_t"], scale, c["pt"])
+    assert_close(got, want, str({k: v for k, v in c.items() if k != "lens"}))
+    assert np.all(got[0] == 0.0)
+    assert device_status() == 0
