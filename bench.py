@@ -558,7 +558,7 @@ def run_ours(args) -> None:
                    "decode_kernel": kernel_name, "partition_tokens": plan["partition_tokens"],
                    "num_partitions": plan["num_partitions"], "attention_ctas": plan["num_ctas"],
                    "parallelism": f"{world} independent replica(s)" if world > 1 else "1 GPU",
-                   "l2": "256 MB buffer read between steps (outside the timed events), so every "
+                   "l2": f"{flush.numel() * 4 >> 20} MiB buffer read between steps (outside the timed events), so every "
                          "step starts with an L2 of clean foreign lines; the decode reads 1.6 GB of KV "
                          "per step"},
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
