@@ -29,10 +29,14 @@ namespace {
 //  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
 //    and O += P.V (M 128, N D, K 32), each as soon as its inputs are ready.
 // K, V, P and S are double buffered by chunk parity.  Signals per buffer
-// b = chunk & 1: conv[b] (96 conversion threads), s_free[b] / p_ready[b]
-// (the active softmax threads), qk[b] / pv[b] (tcgen05.commit).  A waiter
-// never falls two phases behind: the next phase of each barrier needs a step
-// that follows the wait.
+// b = chunk & 1: k_ready[b] (96 conversion threads: K tile and the token
+// scale table written), v_ready[b] (the same threads: V tile written),
+// s_free[b] / p_ready[b] (the active softmax threads), qk[b] / pv[b]
+// (tcgen05.commit).  QK and the softmax wait only for k_ready, so a chunk's
+// logits do not wait for its V tile, whose conversion waits for PV two chunks
+// back.  A waiter never falls two phases behind: the next phase of each
+// barrier needs a step that follows the wait (the issue warp observes
+// v_ready in chunk order and issues PV(j) only after it saw v_ready(j)).
 
 constexpr int kUmmaThreads = 256;
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
@@ -57,7 +61,8 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
 }
 
 // barrier slots (8 bytes each) after the ring's
-enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarConv = 4, kBarSFree = 6, kBarPReady = 8, kUmmaBars = 10 };
+enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarVReady = 4, kBarSFree = 6, kBarPReady = 8, kBarKReady = 10,
+               kUmmaBars = 12 };
 
 struct UmmaLayout {
     uint32_t misc, scales, table, ops, ring, slot_bytes, total;
@@ -125,7 +130,8 @@ decode_umma_kernel(Params P) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarQk, b), 1);
             mbar_init(bar(kBarPv, b), 1);
-            mbar_init(bar(kBarConv, b), kUmmaConvThreads);
+            mbar_init(bar(kBarKReady, b), kUmmaConvThreads);
+            mbar_init(bar(kBarVReady, b), kUmmaConvThreads);
             mbar_init(bar(kBarSFree, b), 32 * nquad);
             mbar_init(bar(kBarPReady, b), 32 * nquad);
         }
@@ -185,30 +191,36 @@ decode_umma_kernel(Params P) {
     int issued = 0;                  // chunks whose ring copy warp 7 started
 
     if (warp == 7) {
-        // ---- ring refills and MMA issue.  Lane 0 polls both inputs and
-        // issues whichever MMA is ready: QK(nq) once chunk nq is converted
-        // (and S buffer nq & 1 was read), PV(np) once P(np) is written.  PV
-        // never waits for a later chunk's conversion, so the V tile it frees
-        // is ready for that conversion as early as possible.  A barrier
-        // cannot run two phases ahead of the poll: its next phase needs an
-        // MMA this warp has not issued yet.
+        // ---- ring refills and MMA issue.  Lane 0 polls the inputs and issues
+        // whatever is ready: QK(nq) once chunk nq's K tile is converted (and S
+        // buffer nq & 1 was read), PV(np) once P(np) is written and V(np) is
+        // converted, and the refill of chunk nv's raw slot once V(nv) is
+        // converted (the conversion's last read of that slot).  v_ready is
+        // observed in chunk order (nv) and PV(j) needs j < nv, so no barrier
+        // runs two phases ahead of the poll: each one's next phase needs a step
+        // this warp has not taken yet.
         for (; issued < RING && issued < nch; ++issued)
             issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
-        int nq = 0, np = 0;                                   // next QK / PV to issue
+        int nq = 0, np = 0, nv = 0;                           // next QK / PV to issue, next V tile to see
         uint64_t idle_since = 0;
         uint32_t polls = 0;
         while (np < nch) {
             int act = 0;
             if (lane == 0) {
-                if (nq < nch && mbar_try_wait(bar(kBarConv, nq & 1), (nq >> 1) & 1) &&
+                if (nq < nch && mbar_try_wait(bar(kBarKReady, nq & 1), (nq >> 1) & 1) &&
                     (nq < 2 || mbar_try_wait(bar(kBarSFree, nq & 1), ((nq - 2) >> 1) & 1)))
                     act |= 1;
-                if (np < nq && mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1)) act |= 2;
+                if (nv < nch && mbar_try_wait(bar(kBarVReady, nv & 1), (nv >> 1) & 1)) act |= 8;
+                if (np < nq && np < nv && mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1)) act |= 2;
                 if (act == 0) {
-                    // nothing ready: suspend briefly on the older pending input, then
+                    // nothing ready: suspend briefly on the oldest pending input, then
                     // poll again; give up after the wait limit or on the CTA's abort
-                    if (np < nq) mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, kIssuePollNs);
-                    else mbar_try_wait_suspend(bar(kBarConv, nq & 1), (nq >> 1) & 1, kIssuePollNs);
+                    if (nv <= np && nv < nch)
+                        mbar_try_wait_suspend(bar(kBarVReady, nv & 1), (nv >> 1) & 1, kIssuePollNs);
+                    else if (np < nq)
+                        mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, kIssuePollNs);
+                    else
+                        mbar_try_wait_suspend(bar(kBarKReady, nq & 1), (nq >> 1) & 1, kIssuePollNs);
                     if (polls++ == 0) idle_since = global_timer_ns();
                     if ((polls & 15u) == 0) {
                         if (*abort) act = 4;
@@ -249,14 +261,15 @@ decode_umma_kernel(Params P) {
                 last_parity = (np >> 1) & 1;
             }
             if (act & 2) ++np;
-            if (act & 1) {
-                // chunk nq's raw slot is free (converted): refill it, after the MMAs are on their way
+            if (act & 1) ++nq;
+            if (act & 8) {
+                // chunk nv's raw slot is free (both tiles converted): refill it, after the MMAs are on their way
                 if (issued < nch) {
                     issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
                                    ring_bars + 8 * (issued % RING), policy);
                     ++issued;
                 }
-                ++nq;
+                ++nv;
             }
         }
         __syncwarp();
@@ -287,10 +300,14 @@ decode_umma_kernel(Params P) {
                     *reinterpret_cast<uint4 *>(dst + 128 * c8) = make_uint4(a0, a1, a2, a3);
                 }
             }
-            // V tile and scale table b free: PV(i-2) done, so softmax(i-2) is too
-            if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
+            // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)) break;
             if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
             else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarKReady, b));
+            // V tile b free: PV(i-2) done
+            if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
             uint8_t *dV = sV0 + b * V_BYTES;
             {                                                 // as K: the PV B operand is MN-major
                 const uint32_t *src = rawV + tok * W;
@@ -303,7 +320,7 @@ decode_umma_kernel(Params P) {
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(kBarConv, b));
+            mbar_arrive(bar(kBarVReady, b));
         }
     } else if (warp < nquad) {
         // ---- softmax (quadrant warp)
@@ -316,7 +333,7 @@ decode_umma_kernel(Params P) {
         for (int i = 0; ok && i < nch; ++i) {
             const int b = i & 1;
             ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
-            ok = ok && mbar_wait_abortable(bar(kBarConv, b), (i >> 1) & 1, abort);     // the scale table
+            ok = ok && mbar_wait_abortable(bar(kBarKReady, b), (i >> 1) & 1, abort);   // the scale table
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             tc_fence_after();
             float sv[32], z[16];
