@@ -26,8 +26,12 @@ namespace {
 //    the other families) become f16 K and V tiles [32 tokens][D] in the
 //    same core-matrix layout (K-major for QK's B, MN-major for PV's B) and
 //    the token scales a small table.
-//  - warp 7: refills the ring; its lane 0 issues S = Q.K^T (M 128, N 32, K D)
-//    and O += P.V (M 128, N D, K 32), each as soon as its inputs are ready.
+//  - warp 7: its lane 0 issues S = Q.K^T (M 128, N 32, K D) and O += P.V
+//    (M 128, N D, K 32), each as soon as its inputs are ready.
+//  - warp 8: refills the raw ring, chunk c into the slot of chunk c - ring
+//    once the conversion has read that slot (slot_free[slot]).  A refill
+//    costs about as much as issuing both MMAs of a chunk, so it has a warp of
+//    its own.
 // K, V, P and S are double buffered by chunk parity.  Signals per buffer
 // b = chunk & 1: k_ready[b] (96 conversion threads: K tile and the token
 // scale table written), v_ready[b] (the same threads: V tile written),
@@ -35,10 +39,11 @@ namespace {
 // (tcgen05.commit).  QK and the softmax wait only for k_ready, so a chunk's
 // logits do not wait for its V tile, whose conversion waits for PV two chunks
 // back.  A waiter never falls two phases behind: the next phase of each
-// barrier needs a step that follows the wait (the issue warp observes
-// v_ready in chunk order and issues PV(j) only after it saw v_ready(j)).
+// barrier needs a step that follows the wait (v_ready(j + 2) needs PV(j),
+// issued after the issue warp saw v_ready(j); slot_free for chunk c + ring
+// needs the refill issued after the wait for chunk c).
 
-constexpr int kUmmaThreads = 256;
+constexpr int kUmmaThreads = 288;
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
 constexpr uint32_t kUmmaBMnMajor = 1u << 16;
 constexpr int kUmmaConvThreads = 96;
@@ -50,7 +55,7 @@ template <int D>
 __host__ __device__ constexpr int umma_ring() { return 3; }
 template <int D>
 __host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 64 ? 128u : (D == 128 ? 256u : 512u); }
-// resident CTAs per SM: TMEM (512 columns) and registers (2 x 256 threads x 128)
+// resident CTAs per SM: TMEM (512 columns) and registers (2 x 288 threads)
 template <int D>
 __host__ __device__ constexpr int umma_ctas_per_sm() { return D == 256 ? 1 : 2; }
 
@@ -62,7 +67,7 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
 
 // barrier slots (8 bytes each) after the ring's
 enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarVReady = 4, kBarSFree = 6, kBarPReady = 8, kBarKReady = 10,
-               kUmmaBars = 12 };
+               kBarSlotFree = 12, kUmmaBars = 16 };     // slot_free: one per raw ring slot (ring <= 4)
 
 struct UmmaLayout {
     uint32_t misc, scales, table, ops, ring, slot_bytes, total;
@@ -95,6 +100,7 @@ template <int D>
 __global__ void __launch_bounds__(kUmmaThreads, umma_ctas_per_sm<D>())
 decode_umma_kernel(Params P) {
     constexpr int RING = umma_ring<D>();
+    static_assert(RING <= kUmmaBars - kBarSlotFree, "one slot_free barrier per raw ring slot");
     constexpr int W = D / 4 + 1;
     constexpr uint32_t TCOLS = umma_tmem_cols<D>();
     constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
@@ -126,7 +132,10 @@ decode_umma_kernel(Params P) {
 
     if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
     if (tid == 0) {
-        for (int k = 0; k < RING; ++k) mbar_init(ring_bars + 8 * k, 1);
+        for (int k = 0; k < RING; ++k) {
+            mbar_init(ring_bars + 8 * k, 1);
+            mbar_init(bar(kBarSlotFree, k), kUmmaConvThreads);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarQk, b), 1);
             mbar_init(bar(kBarPv, b), 1);
@@ -188,20 +197,25 @@ decode_umma_kernel(Params P) {
     int E = 12;
     int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
     uint32_t last_parity = 0;
-    int issued = 0;                  // chunks whose ring copy warp 7 started
+    int issued = 0;                  // chunks whose ring copy warp 8 started
 
-    if (warp == 7) {
-        // ---- ring refills and MMA issue.  Lane 0 polls the inputs and issues
-        // whatever is ready: QK(nq) once chunk nq's K tile is converted (and S
-        // buffer nq & 1 was read), PV(np) once P(np) is written and V(np) is
-        // converted, and the refill of chunk nv's raw slot once V(nv) is
-        // converted (the conversion's last read of that slot).  v_ready is
-        // observed in chunk order (nv) and PV(j) needs j < nv, so no barrier
-        // runs two phases ahead of the poll: each one's next phase needs a step
-        // this warp has not taken yet.
-        for (; issued < RING && issued < nch; ++issued)
-            issue_chunk<D>(P, w, table, issued, ring + issued * L.slot_bytes, ring_bars + 8 * issued, policy);
-        int nq = 0, np = 0, nv = 0;                           // next QK / PV to issue, next V tile to see
+    if (warp == 8) {
+        // ---- ring refills: the first RING chunks at once, then chunk c into
+        // the slot of chunk c - RING once the conversion has read it
+        for (; issued < nch; ++issued) {
+            const int k = issued % RING;
+            const bool ok = issued < RING ||
+                            mbar_wait_abortable(bar(kBarSlotFree, k), ((issued - RING) / RING) & 1, abort);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;          // issue_chunk is warp-collective
+            issue_chunk<D>(P, w, table, issued, ring + k * L.slot_bytes, ring_bars + 8 * k, policy);
+        }
+    } else if (warp == 7) {
+        // ---- MMA issue.  Lane 0 polls the inputs and issues whichever MMA is
+        // ready: QK(nq) once chunk nq's K tile is converted (and S buffer
+        // nq & 1 was read), PV(np) once P(np) is written and V(np) is
+        // converted.  No barrier runs two phases ahead of the poll: each one's
+        // next phase needs an MMA this warp has not issued yet.
+        int nq = 0, np = 0;                                   // next QK / PV to issue
         uint64_t idle_since = 0;
         uint32_t polls = 0;
         while (np < nch) {
@@ -210,17 +224,20 @@ decode_umma_kernel(Params P) {
                 if (nq < nch && mbar_try_wait(bar(kBarKReady, nq & 1), (nq >> 1) & 1) &&
                     (nq < 2 || mbar_try_wait(bar(kBarSFree, nq & 1), ((nq - 2) >> 1) & 1)))
                     act |= 1;
-                if (nv < nch && mbar_try_wait(bar(kBarVReady, nv & 1), (nv >> 1) & 1)) act |= 8;
-                if (np < nq && np < nv && mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1)) act |= 2;
+                bool p_ok = false;
+                if (np < nq) {
+                    p_ok = mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1);
+                    if (p_ok && mbar_try_wait(bar(kBarVReady, np & 1), (np >> 1) & 1)) act |= 2;
+                }
                 if (act == 0) {
                     // nothing ready: suspend briefly on the oldest pending input, then
                     // poll again; give up after the wait limit or on the CTA's abort
-                    if (nv <= np && nv < nch)
-                        mbar_try_wait_suspend(bar(kBarVReady, nv & 1), (nv >> 1) & 1, kIssuePollNs);
-                    else if (np < nq)
-                        mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, kIssuePollNs);
-                    else
+                    if (np < nq) {
+                        if (p_ok) mbar_try_wait_suspend(bar(kBarVReady, np & 1), (np >> 1) & 1, kIssuePollNs);
+                        else mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, kIssuePollNs);
+                    } else {
                         mbar_try_wait_suspend(bar(kBarKReady, nq & 1), (nq >> 1) & 1, kIssuePollNs);
+                    }
                     if (polls++ == 0) idle_since = global_timer_ns();
                     if ((polls & 15u) == 0) {
                         if (*abort) act = 4;
@@ -262,15 +279,6 @@ decode_umma_kernel(Params P) {
             }
             if (act & 2) ++np;
             if (act & 1) ++nq;
-            if (act & 8) {
-                // chunk nv's raw slot is free (both tiles converted): refill it, after the MMAs are on their way
-                if (issued < nch) {
-                    issue_chunk<D>(P, w, table, issued, ring + (issued % RING) * L.slot_bytes,
-                                   ring_bars + 8 * (issued % RING), policy);
-                    ++issued;
-                }
-                ++nv;
-            }
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -321,6 +329,7 @@ decode_umma_kernel(Params P) {
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(kBarVReady, b));
+            mbar_arrive(bar(kBarSlotFree, k));                // raw slot k read for the last time
         }
     } else if (warp < nquad) {
         // ---- softmax (quadrant warp)
@@ -459,6 +468,8 @@ decode_umma_kernel(Params P) {
     if (failed && warp == 7 && lane == 0) {
         // stop only after the newest MMA (and so every earlier one) completed
         if (last_commit >= 0) mbar_wait(bars + 8 * last_commit, last_parity);
+    }
+    if (failed && warp == 8 && lane == 0) {
         for (int c = max(0, issued - RING); c < issued; ++c)     // and the ring copies in flight
             mbar_wait(ring_bars + 8 * (c % RING), (c / RING) & 1);
     }
