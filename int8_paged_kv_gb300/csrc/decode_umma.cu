@@ -43,10 +43,18 @@ namespace {
 // issued after the issue warp saw v_ready(j); slot_free for chunk c + ring
 // needs the refill issued after the wait for chunk c).
 
-constexpr int kUmmaThreads = 288;
+// conversion warps (4 measured slower than 3: large R = 8 0.96 against 0.93 ms)
+#ifndef PA_Q8_UMMA_CONV_WARPS
+#define PA_Q8_UMMA_CONV_WARPS 3
+#endif
+// warps 0-3 softmax, then the conversion warps, the issue warp, the refill warp
+constexpr int kUmmaConvWarps = PA_Q8_UMMA_CONV_WARPS;
+constexpr int kUmmaIssueWarp = 4 + kUmmaConvWarps;
+constexpr int kUmmaRefillWarp = kUmmaIssueWarp + 1;
+constexpr int kUmmaThreads = 32 * (kUmmaRefillWarp + 1);
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
 constexpr uint32_t kUmmaBMnMajor = 1u << 16;
-constexpr int kUmmaConvThreads = 96;
+constexpr int kUmmaConvThreads = 32 * kUmmaConvWarps;
 // longest suspension of the issue warp on one pending input before it polls
 // the other again (64 and 32 ns measured the same)
 constexpr uint32_t kIssuePollNs = 256;
@@ -199,7 +207,7 @@ decode_umma_kernel(Params P) {
     uint32_t last_parity = 0;
     int issued = 0;                  // chunks whose ring copy warp 8 started
 
-    if (warp == 8) {
+    if (warp == kUmmaRefillWarp) {
         // ---- ring refills: the first RING chunks at once, then chunk c into
         // the slot of chunk c - RING once the conversion has read it
         for (; issued < nch; ++issued) {
@@ -209,7 +217,7 @@ decode_umma_kernel(Params P) {
             if (!__all_sync(0xFFFFFFFFu, ok)) break;          // issue_chunk is warp-collective
             issue_chunk<D>(P, w, table, issued, ring + k * L.slot_bytes, ring_bars + 8 * k, policy);
         }
-    } else if (warp == 7) {
+    } else if (warp == kUmmaIssueWarp) {
         // ---- MMA issue.  Lane 0 polls the inputs and issues whichever MMA is
         // ready: QK(nq) once chunk nq's K tile is converted (and S buffer
         // nq & 1 was read), PV(np) once P(np) is written and V(np) is
@@ -282,7 +290,7 @@ decode_umma_kernel(Params P) {
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ---- conversion (96 threads)
+        // ---- conversion (kUmmaConvThreads threads)
         const int ct = tid - 128;
         static_assert(kUmmaConvThreads % kChunk == 0, "conversion threads: whole warps per token lane");
         constexpr int kConvColStep = kUmmaConvThreads / kChunk;
@@ -295,9 +303,10 @@ decode_umma_kernel(Params P) {
             if (!mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort)) break;
             if (i >= 2 && !mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)) break;   // K tile free
             uint8_t *dK = sK0 + b * K_BYTES;
-            // element u = ct + 96k of the [8-code column][token] walk: lane = token
-            // (8 bank groups); 96 is a multiple of 32, so this thread's token is
-            // fixed and its column steps by 3 (128 bytes each in the tile)
+            // element u = ct + kUmmaConvThreads * k of the [8-code column][token]
+            // walk: lane = token (8 bank groups); the thread count is a multiple
+            // of 32, so this thread's token is fixed and its column steps by
+            // kConvColStep (128 bytes each in the tile)
             {
                 const uint32_t *src = rawK + tok * W;
                 uint8_t *dst = dK + kmaj_off(tok, 0, D);
@@ -465,11 +474,11 @@ decode_umma_kernel(Params P) {
     }
     __syncthreads();
     const bool failed = *abort != 0u;
-    if (failed && warp == 7 && lane == 0) {
+    if (failed && warp == kUmmaIssueWarp && lane == 0) {
         // stop only after the newest MMA (and so every earlier one) completed
         if (last_commit >= 0) mbar_wait(bars + 8 * last_commit, last_parity);
     }
-    if (failed && warp == 8 && lane == 0) {
+    if (failed && warp == kUmmaRefillWarp && lane == 0) {
         for (int c = max(0, issued - RING); c < issued; ++c)     // and the ring copies in flight
             mbar_wait(ring_bars + 8 * (c % RING), (c / RING) & 1);
     }
