@@ -35,6 +35,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _flags_changed(stamp: str, key: str) -> bool:
+    """True unless `stamp` records exactly this compiler command (`key`):
+    objects built with other flags are stale whatever their times."""
+    try:
+        with open(stamp) as f:
+            return f.read() != key
+    except OSError:
+        return True
+
+
+def _record_flags(stamp: str, key: str) -> None:
+    with open(stamp, "w") as f:
+        f.write(key)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
@@ -47,11 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     # objects built with other flags (PA_Q8_NVCC_FLAGS) are stale whatever their times
     stamp = os.path.join(BUILD, "flags.txt")
     key = " ".join([cc] + flags)
-    try:
-        with open(stamp) as f:
-            force = force or f.read() != key
-    except OSError:
-        force = True
+    force = force or _flags_changed(stamp, key)
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -77,8 +88,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
-        with open(stamp, "w") as f:
-            f.write(key)
+        _record_flags(stamp, key)
     return LIB
 
 

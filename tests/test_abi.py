@@ -104,3 +104,18 @@ def test_contiguous_cache_shape_checks_without_a_device(L):
                            None, 0, None, None) == -1
     assert pk.pa_q8c_decode_workspace_size(4, 8, 2, 128, 4096) > 0
     assert pk.pa_q8c_decode_workspace_size(4, 8, 2, 64, 4096) == 0
+
+
+def test_build_recompiles_when_its_flags_change(tmp_path):
+    """The in-tree build records the compiler command it linked with; a later
+    build with other flags (PA_Q8_NVCC_FLAGS) must treat every object as stale
+    even though the objects are newer than their sources."""
+    from int8_paged_kv_gb300 import build
+    stamp = str(tmp_path / "flags.txt")
+    key = "nvcc -gencode arch=compute_103a,code=sm_103a -O3"
+    assert build._flags_changed(stamp, key)                       # never built here
+    build._record_flags(stamp, key)
+    assert not build._flags_changed(stamp, key)
+    assert build._flags_changed(stamp, key + " -DPA_Q8_CQ_MINB=2")   # flags added
+    build._record_flags(stamp, key + " -DX=1")
+    assert build._flags_changed(stamp, key)                       # flags removed again
