@@ -116,6 +116,6 @@ def test_build_recompiles_when_its_flags_change(tmp_path):
     assert build._flags_changed(stamp, key)                       # never built here
     build._record_flags(stamp, key)
     assert not build._flags_changed(stamp, key)
-    assert build._flags_changed(stamp, key + " -DPA_Q8_CQ_MINB=2")   # flags added
+    assert build._flags_changed(stamp, key + " -DPA_Q8_TC_WIDE=0")    # flags added
     build._record_flags(stamp, key + " -DX=1")
     assert build._flags_changed(stamp, key)                       # flags removed again
