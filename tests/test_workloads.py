@@ -155,3 +155,28 @@ def test_algorithmic_bytes_by_hand():
     assert wl.algorithmic_decode_bytes(cfg, c, cache="f32") == (37 + 100) * 2 * 2 * 256 + qo + bt + 8
     slots = np.array([5, PAD, 7], dtype=np.uint32)
     assert wl.algorithmic_writer_bytes(2, 64, slots) == 2 * (2 * 64 * 4 * 2 + 2 * 68 * 2) + 3 * 4
+
+
+def test_subset_keeps_the_first_sequences_with_a_compact_pool(structure):
+    """subset(w, n): the first n sequences' contexts and queries, their blocks
+    renumbered 0 .. pool-1 in pool order, and every writer row still landing at
+    the same (sequence, position)."""
+    w = structure["llama8b"]
+    B = w.cfg.block_size
+    n = 5
+    sub = wl.subset(w, n)
+    assert sub.cfg.num_seqs == n
+    assert np.array_equal(sub.context_lens, w.context_lens[:n])
+    assert np.array_equal(sub.q, w.q[:n])
+    used_old = w.block_tables[:n][w.block_tables[:n] != UNUSED]
+    used_new = sub.block_tables[sub.block_tables != UNUSED]
+    assert sub.num_blocks == used_old.size == used_new.size
+    assert sorted(used_new.tolist()) == list(range(sub.num_blocks))
+    # the renumbering keeps the pool order of the blocks
+    order_old = np.argsort(used_old, kind="stable")
+    assert np.all(np.diff(used_new[order_old].astype(np.int64)) > 0)
+    for s in range(n):
+        idx = np.flatnonzero(sub.row_seq == s)
+        t = np.arange(idx.size)
+        want = sub.block_tables[s, t // B].astype(np.int64) * B + t % B
+        assert np.array_equal(sub.slot_mapping[idx].astype(np.int64), want), s
