@@ -331,6 +331,100 @@ def job_gbps(world: int, bytes_per_step: int, ms_per_step: float) -> float:
     return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
+# ------------------------------------------------- the other four workloads
+
+# sequences the oracle checks per workload (the first n): every sequence of
+# tiny, a share of the others (long: one 32K-131K context of 32 heads)
+PARITY_SEQS = {"tiny": 2, "llama8b": 4, "long": 1, "large": 8, "edge": 8}
+
+
+def oracle_rows(w, n: int) -> np.ndarray:
+    """The fp64 oracle's outputs for the first n sequences of a workload: their
+    rows written into oracle-owned caches by the oracle writer, then decoded."""
+    import oracle
+    cfg = w.cfg
+    sub = wl.subset(w, n)
+    n = int(sub.context_lens.size)
+    k, v, sm = wl.sequence_rows(sub, range(n))
+    kc, vc = wl.empty_cache(sub), wl.empty_cache(sub)
+    oracle.reshape_and_cache(k, v, kc, vc, sm, num_kv_heads=cfg.num_kv_heads, head_size=cfg.head_size,
+                             block_size=cfg.block_size)
+    return oracle.decode(np.ascontiguousarray(sub.q[:n]), kc, vc, sub.block_tables, sub.context_lens,
+                         num_kv_heads=cfg.num_kv_heads, block_size=cfg.block_size, scale=sub.scale)
+
+
+def time_workload_decodes(args, dev, peaks, flush_l2, names, with_parity: bool) -> dict:
+    """pa_q8_decode on each named workload (automatic plan), timed like the
+    bench step: L2 flushed between calls outside the events, CUDA events on the
+    launching stream, median of args.steps calls after max(3, warmup) untimed
+    ones.  With the oracle leg on, the first PARITY_SEQS[name] sequences'
+    output rows are checked against the oracle (|gpu - oracle| <= 1e-5 +
+    1e-4 |oracle|)."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name in names:
+        w = wl.build(name, with_append=False)
+        cfg = w.cfg
+        S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+
+        def u32(x):
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int32)).to(dev)
+
+        kc = torch.empty((w.num_blocks, Hk, B, D // 4 + 1), dtype=torch.int32, device=dev)
+        vc = torch.empty_like(kc)
+        step = 1 << 18
+        for i in range(0, w.key.shape[0], step):
+            pk.pa_q8_reshape_and_cache(torch.from_numpy(w.key[i:i + step].reshape(-1, Hk * D)).to(dev),
+                                       torch.from_numpy(w.value[i:i + step].reshape(-1, Hk * D)).to(dev),
+                                       kc, vc, u32(w.slot_mapping[i:i + step]), num_kv_heads=Hk, head_size=D,
+                                       block_size=B)
+        w.key = w.value = None
+        q = torch.from_numpy(w.q).to(dev)
+        bt, cl = u32(w.block_tables), u32(w.context_lens)
+        out = torch.empty_like(q)
+        plan = pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq)
+        ws = torch.empty(max(16, pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq)),
+                         dtype=torch.uint8, device=dev)
+
+        def run():
+            pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale, workspace=ws)
+        for _ in range(max(3, args.warmup)):
+            flush_l2()
+            run()
+        a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush_l2()
+            a[i].record(stream)
+            run()
+            b[i].record(stream)
+        torch.cuda.synchronize()
+        ms = float(statistics.median(x.elapsed_time(y) for x, y in zip(a, b)))
+        nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens)
+        gbps = nbytes / ms / 1e6
+        entry = {"ms": round(ms, 4), "gbps": round(gbps, 1),
+                 "pct_of_hbm_peak": round(100 * gbps / peaks["hbm_gbs"], 2),
+                 "pct_of_nominal_hbm": round(100 * gbps / NOMINAL_HBM_GBS, 2),
+                 "seqs_per_s": round(S / (ms * 1e-3), 1), "algorithmic_bytes": int(nbytes),
+                 "partition_tokens": plan["partition_tokens"], "attention_ctas": plan["num_ctas"],
+                 "device_status": pk.pa_q8_device_status(clear=True)}
+        if with_parity:
+            want = oracle_rows(w, PARITY_SEQS[name])
+            got = out[:want.shape[0]].cpu().numpy().astype(np.float64)
+            ratio = float(np.max(np.abs(got - want) / (1e-5 + 1e-4 * np.abs(want))))
+            entry["parity"] = {"sequences": int(want.shape[0]), "rows": int(want.shape[0] * H),
+                               "max_err_over_bound": round(ratio, 4),
+                               "ok": bool(ratio <= 1.0 and entry["device_status"] == 0)}
+        res[name] = entry
+        del kc, vc, q, out, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args) -> None:
@@ -439,10 +533,20 @@ def run_ours(args) -> None:
     dends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     wstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
+    sampler.start()
+    # sustained, untimed load (back-to-back steps with the L2 flush) so clocks
+    # and power settle, and a clock sampler sees the GPU busy, before timing
+    sustained_steps, t_sus = 0, time.perf_counter()
+    while time.perf_counter() - t_sus < args.sustain_seconds:
+        for _ in range(64):
+            flush_l2()
+            step()
+        torch.cuda.synchronize()
+        sustained_steps += 64
+    t_sus = time.perf_counter() - t_sus
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler.start()
     for i in range(args.steps):
         flush_l2()                                      # outside the timed events
         starts[i].record(stream)
@@ -451,6 +555,7 @@ def run_ours(args) -> None:
         ends[i].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    clocks["window"] = "the sustained warm-up and the timed steps"
     if world > 1:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -460,8 +565,10 @@ def run_ours(args) -> None:
     status = pk.pa_q8_device_status(clear=True)
     ms_per_step = total_ms / args.steps
     value = job_gbps(world, bytes_w + bytes_d, ms_per_step)
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    dec_gbs = bytes_d / (dec_avg_ms * 1e-3) / 1e9
+    # per-kernel figures: medians over the timed steps
+    dec_med_ms = float(statistics.median(dec_ms))
+    dec_gbs = bytes_d / (dec_med_ms * 1e-3) / 1e9
+    wr_med_ms = float(statistics.median(wr_ms))
 
     # ---- end to end: host (pinned) inputs copied in, output copied back, every step
     e2e = None
@@ -547,6 +654,24 @@ def run_ours(args) -> None:
         samp = ob.sample(seconds=args.cpu_seconds)
         cpu = cpu_line_fields(samp, bytes_w, bytes_d)
 
+    # the other four workloads' decodes, each timed on its own (rank 0 only)
+    configs = {}
+    if not args.seqs and not args.no_configs:
+        configs = time_workload_decodes(args, dev, peaks, flush_l2, ["tiny", "llama8b", "long", "edge"],
+                                        with_parity=ob is not None)
+    large_entry = {"ms": round(dec_med_ms, 4), "gbps": round(dec_gbs, 1),
+                   "pct_of_hbm_peak": round(100 * dec_gbs / peaks["hbm_gbs"], 2),
+                   "pct_of_nominal_hbm": round(100 * dec_gbs / NOMINAL_HBM_GBS, 2),
+                   "seqs_per_s": round(S / (dec_med_ms * 1e-3), 1), "algorithmic_bytes": int(bytes_d),
+                   "partition_tokens": plan["partition_tokens"], "attention_ctas": plan["num_ctas"],
+                   "device_status": status}
+    if parity is not None:
+        large_entry["parity"] = {"sequences": len(parity["sequences"]), "rows": parity["decode_rows"],
+                                 "max_err_over_bound": parity["max_err_over_bound"], "ok": parity["ok"]}
+    if configs:
+        configs = {"tiny": configs["tiny"], "llama8b": configs["llama8b"], "long": configs["long"],
+                   "large": large_entry, "edge": configs["edge"]}
+
     traffic = recorded_traffic()
     kernel_name = {1: "CUDA-core (f32 FMA)", 2: "tensor-core (mma.sync f16 hi/lo)"}[plan["kernel"]]
     line = {
@@ -561,18 +686,23 @@ def run_ours(args) -> None:
                    "l2": f"{flush.numel() * 4 >> 20} MiB buffer read between steps (outside the timed events), so every "
                          "step starts with an L2 of clean foreign lines; the decode reads 1.6 GB of KV "
                          "per step"},
+        "ms_per_step_median": round(float(statistics.median(step_ms)), 4),
         "pct_of_hbm_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "seqs_per_s": round(world * S / (ms_per_step * 1e-3), 1),
-        "decode": {"ms": round(dec_avg_ms, 4), "gbps": round(dec_gbs, 1),
+        "timing": ("value and ms_per_step: the K timed steps' total (max over ranks) / K; decode, writer, "
+                   "roofline and configs: medians of per-call CUDA events"),
+        "decode": {"ms": round(dec_med_ms, 4), "gbps": round(dec_gbs, 1),
                    "pct_of_hbm_peak": round(100 * dec_gbs / peaks["hbm_gbs"], 2),
                    "pct_of_nominal_hbm": round(100 * dec_gbs / NOMINAL_HBM_GBS, 2),
-                   "seqs_per_s": round(S / (dec_avg_ms * 1e-3), 1),
+                   "seqs_per_s": round(S / (dec_med_ms * 1e-3), 1),
                    "algorithmic_bytes": int(bytes_d)},
-        "writer": {"ms": round(sum(wr_ms) / len(wr_ms), 4),
-                   "gbps": round(bytes_w / (sum(wr_ms) / len(wr_ms) * 1e-3) / 1e9, 1),
-                   "tokens_per_s": round(rows_w / (sum(wr_ms) / len(wr_ms) * 1e-3), 1),
+        "writer": {"ms": round(wr_med_ms, 4),
+                   "gbps": round(bytes_w / (wr_med_ms * 1e-3) / 1e9, 1),
+                   "tokens_per_s": round(rows_w / (wr_med_ms * 1e-3), 1),
                    "algorithmic_bytes": int(bytes_w)},
+        "configs": configs or None,
+        "sustained_warmup": {"seconds": round(t_sus, 2), "steps": sustained_steps},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
                      "traffic": (round(traffic["bytes_per_launch"]) if traffic else None),
@@ -1092,6 +1222,10 @@ def main():
     ap.add_argument("--e2e-streams", type=int, default=2, help="copy streams of the end-to-end step")
     ap.add_argument("--e2e-chunks", type=int, default=4, help="chunks the appended rows are copied in")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other four workloads' decode timings in the bench line")
+    ap.add_argument("--sustain-seconds", type=float, default=1.5,
+                    help="untimed back-to-back steps before the timed ones (clock sampler running)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.0,
                     help="oracle seconds per reference step (0: fit the run into ~2.5 minutes)")

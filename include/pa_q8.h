@@ -3,9 +3,17 @@
  *
  * C ABI of libpa_q8.so.  Plain pointers and sizes only; every pointer named
  * "device" is a CUDA device address the caller allocated and owns.  The
- * library keeps no per-call state and allocates no device memory: scratch
- * (the split-context partials) lives in a workspace the caller passes in
- * (or, for pa_q8_decode_noalloc, in a fixed buffer compiled into it).
+ * library keeps no per-call state and makes no allocation call: scratch (the
+ * split-context partials) lives in a workspace the caller passes in, or, for
+ * pa_q8_decode_noalloc, in a fixed buffer compiled into the library.  That
+ * buffer (PA_Q8_NOALLOC_SCRATCH_BYTES, 64 MiB) sits in the same device module
+ * as the library's status word, so every device on which any entry point has
+ * run holds it until the process exits, whether or not pa_q8_decode_noalloc
+ * is called there.  The library looks up the device addresses of those two
+ * symbols once per device and caches them: after cudaDeviceReset (or any
+ * other teardown of a device's primary context) the cached addresses are
+ * stale, so the library must not be called again on that device in the same
+ * process.
  * All work is queued on the caller's CUDA stream (a cudaStream_t passed as
  * void*; NULL = the legacy default stream) and no function synchronises,
  * except pa_q8_device_status which reads a flag back.

@@ -1,14 +1,15 @@
-"""pa_q8_decode_noalloc, called through the C ABI, against pa_q8_decode.
+"""pa_q8_decode_noalloc, called through the C ABI, against the fp64 oracle
+and against pa_q8_decode.
 
 Some callers cannot give the library device memory for scratch -- a plugin
 inside another runtime that owns every device allocation, or a serving loop
 that may not call an allocator -- so pa_q8_decode_noalloc keeps the
 split-context partials in a fixed buffer compiled into the library.  This
 test checks, on two calls in a row with different inputs (the second one
-split into partitions), that its output matches the workspace-taking entry
-point within the decode tolerance (|a - b| <= 1e-5 + 1e-4 |b|), that a shape
-whose scratch would not fit the buffer is refused, and that nothing was
-flagged on the device.  The file is
+split into partitions), that its output is within the decode tolerance
+(|gpu - oracle| <= 1e-5 + 1e-4 |oracle|) of the oracle's and of the
+workspace-taking entry point's, that a shape whose scratch would not fit the
+buffer is refused, and that nothing was flagged on the device.  The file is
 named to be collected last.
 """
 import ctypes
@@ -53,30 +54,44 @@ def _cache_from_rows(pk, key, value, slots, nblocks, Hk, D, B, dev):
     return kc, vc
 
 
-def test_noalloc_matches_decode_on_two_calls(lib):
+def test_noalloc_matches_oracle_and_decode_on_two_calls(lib):
     """Call 1: the 64-sequence workload (one partition per context: the
     buffer holds the sequence order).  Call 2: three ~20k-token contexts
     (split into partitions: the buffer also holds their partials, over
-    whatever call 1 left there).  Each output matches pa_q8_decode's on the
-    same inputs."""
+    whatever call 1 left there).  Each output matches the oracle's (on caches
+    the oracle writer built from the same rows) and pa_q8_decode's."""
     import torch
     import int8_paged_kv_gb300 as pk
+    import oracle
     from int8_paged_kv_gb300 import workloads as wl
+    from tests.gpu_helpers import assert_close, host_u32
 
+    oracle.build()
     dev = torch.device("cuda")
     stream = torch.cuda.current_stream().cuda_stream
 
     def u32(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(dev)
 
+    def caches(w, key, value):
+        """Device caches from the GPU writer and host caches from the oracle
+        writer, from the same f32 rows (checked equal word for word)."""
+        cfg = w.cfg
+        Hk, D, B = cfg.num_kv_heads, cfg.head_size, cfg.block_size
+        kc, vc = _cache_from_rows(pk, torch.from_numpy(key).to(dev), torch.from_numpy(value).to(dev),
+                                  u32(w.slot_mapping), w.num_blocks, Hk, D, B, dev)
+        W = D // 4 + 1
+        ok_ = np.full((w.num_blocks, Hk, B, W), 0xFFFFFFFF, dtype=np.uint32)
+        ov_ = ok_.copy()
+        oracle.reshape_and_cache(key, value, ok_, ov_, w.slot_mapping, num_kv_heads=Hk, head_size=D,
+                                 block_size=B)
+        assert np.array_equal(host_u32(kc), ok_) and np.array_equal(host_u32(vc), ov_)
+        return kc, vc, ok_, ov_
+
     cases = []
     w = wl.build("llama8b")
-    cfg = w.cfg
-    kc, vc = _cache_from_rows(pk, torch.from_numpy(w.key).to(dev), torch.from_numpy(w.value).to(dev),
-                              u32(w.slot_mapping), w.num_blocks, cfg.num_kv_heads, cfg.head_size,
-                              cfg.block_size, dev)
+    cases.append((w, *caches(w, w.key, w.value)))
     w.key = w.value = None
-    cases.append((w, kc, vc))
 
     rng = np.random.default_rng(7)
     S, H, Hk, D, B = 3, 8, 2, 128, 16
@@ -93,24 +108,24 @@ def test_noalloc_matches_decode_on_two_calls(lib):
         slots.append(bt[s_, t // B].astype(np.int64) * B + t % B)
     slots = np.concatenate(slots).astype(np.uint32)
     T = slots.size
-    gen = torch.Generator(device=dev).manual_seed(7)
-    key = torch.randn(T, Hk, D, device=dev, generator=gen)
-    value = torch.randn(T, Hk, D, device=dev, generator=gen)
-    kc2, vc2 = _cache_from_rows(pk, key, value, u32(slots), sum(nblk), Hk, D, B, dev)
+    key = rng.standard_normal((T, Hk, D)).astype(np.float32)
+    value = rng.standard_normal((T, Hk, D)).astype(np.float32)
     cfg2 = wl.Config("three-long", 98, S, H, Hk, D, B, Nb * B)
     w2 = wl.Workload(cfg=cfg2, context_lens=lens, block_tables=bt, num_blocks=sum(nblk),
                      q=rng.standard_normal((S, H, D)).astype(np.float32),
                      scale=float(np.float32(D ** -0.5)), key=None, value=None, slot_mapping=slots,
                      row_seq=None)
-    cases.append((w2, kc2, vc2))
+    cases.append((w2, *caches(w2, key, value)))
 
     needs = [pk.pa_q8_decode_workspace_size(c.cfg.num_seqs, c.cfg.num_heads, c.cfg.num_kv_heads,
                                             c.cfg.head_size, c.cfg.block_size, c.cfg.max_blocks_per_seq)
-             for c, _, _ in cases]
+             for c, *_ in cases]
     assert 0 < needs[0] < needs[1] <= 64 << 20      # call 2 also stores split-context partials
 
-    for call, (wk, kck, vck) in enumerate(cases):
+    for call, (wk, kck, vck, ok_, ov_) in enumerate(cases):
         c = wk.cfg
+        want = oracle.decode(wk.q, ok_, ov_, wk.block_tables, wk.context_lens, num_kv_heads=c.num_kv_heads,
+                             block_size=c.block_size, scale=wk.scale)
         q = torch.from_numpy(wk.q).to(dev)
         bt_d, cl_d = u32(wk.block_tables), u32(wk.context_lens)
         ref = torch.full_like(q, float("nan"))
@@ -122,8 +137,9 @@ def test_noalloc_matches_decode_on_two_calls(lib):
         torch.cuda.synchronize()
         a = got.cpu().numpy().astype(np.float64)
         b = ref.cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(a))
-        assert np.all(np.abs(a - b) <= 1e-5 + 1e-4 * np.abs(b)), f"call {call}"
+        assert_close(a, want, f"call {call}: noalloc against the oracle")
+        assert_close(b, want, f"call {call}: pa_q8_decode against the oracle")
+        assert np.all(np.abs(a - b) <= 1e-5 + 1e-4 * np.abs(b)), f"call {call}: noalloc against pa_q8_decode"
     assert pk.pa_q8_device_status(clear=True) == 0
 
 
