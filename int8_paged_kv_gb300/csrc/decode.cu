@@ -109,9 +109,9 @@ decode_tc_kernel(Params P) {
     const bool row_ok = gq < nh_tile;
     const int vh = w.h0 + 8 * ht + gq;                      // this thread's virtual head
     // q is loaded before the block table so the two round trips overlap
-    // (head size 256 reads q below, into shared memory)
-    float4 qraw[kQInSmem ? 1 : NKS];
-    if constexpr (!kQInSmem) {
+    // (head size 256 then keeps its fragments in shared memory)
+    float4 qraw[NKS];
+    {
         const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks)
@@ -139,12 +139,7 @@ decode_tc_kernel(Params P) {
     uint4 *qf = reinterpret_cast<uint4 *>(smem + L.extra);           // [HT][NKS][32]
     float qk2;
     {
-        const float4 *qv = reinterpret_cast<const float4 *>(
-            P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
-        auto qload = [&](int ks) -> float4 {
-            if constexpr (kQInSmem) return row_ok ? __ldg(qv + kword<D>(cq, ks)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            else return qraw[ks];
-        };
+        auto qload = [&](int ks) -> float4 { return qraw[ks]; };
         float mx = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
@@ -887,7 +882,7 @@ Params make_params(const DecodeArgs &a) {
     P.R = a.num_rows;
     P.rv = P.R * P.r;
     P.heads_per_cta = a.heads_per_cta; P.head_groups = a.head_groups;
-    P.order = a.order; P.counters = a.counters; P.pml = a.partial_ml; P.pacc = a.partial_acc; P.status = a.status;
+    P.order = a.order; P.counters = a.counters; P.part = a.partials; P.status = a.status;
     P.nk = a.new_key; P.nv = a.new_value;
     P.nk_stride = a.new_key_stride; P.nv_stride = a.new_value_stride;
     P.contiguous = a.contiguous;
@@ -1059,8 +1054,7 @@ size_t plan_workspace_bytes(const DecodeArgs &a) {
     if (a.num_partitions <= 1) return order;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
     const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions;
-    return order + round256(groups * sizeof(uint32_t)) + round256(rows * 2 * sizeof(float)) +
-           rows * a.head_size * sizeof(float);
+    return order + round256(groups * sizeof(uint32_t)) + rows * (a.head_size + 4) * sizeof(float);
 }
 
 void plan_workspace_layout(DecodeArgs &a, void *workspace) {
@@ -1069,12 +1063,9 @@ void plan_workspace_layout(DecodeArgs &a, void *workspace) {
     p += round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-    const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions;
     a.counters = reinterpret_cast<uint32_t *>(p);
     p += round256(groups * sizeof(uint32_t));
-    a.partial_ml = reinterpret_cast<float *>(p);
-    p += round256(rows * 2 * sizeof(float));
-    a.partial_acc = reinterpret_cast<float *>(p);
+    a.partials = reinterpret_cast<float *>(p);
 }
 
 int64_t plan_num_ctas(const DecodeArgs &a) {

@@ -32,8 +32,8 @@ struct Params {
     int log2ptok;           // piece = min(block_size, 32) tokens
     int64_t num_blocks;
     float scale_log2;       // scale * log2(e)
-    int PT;                 // tokens per partition
-    int NP;                 // partitions per sequence (grid x)
+    int PT;                 // most tokens a partition holds
+    int NP;                 // most partitions a sequence is split into (grid x)
     int r;                  // num_heads / num_kv_heads
     int R;                  // query rows per sequence (1 = single-query decode)
     int rv;                 // R * r: (row, head) "virtual heads" per kv head
@@ -42,8 +42,7 @@ struct Params {
     const unsigned long long *order;  // [S]: (clamped length << 32 | sequence) of grid z,
                                       // longest context first
     uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
-    float *pml;             // [S][R][H][NP][2]
-    float *pacc;            // [S][R][H][NP][D]
+    float *part;            // [S][R][H][NP][D + 4]: A, then m, l (and two spare words)
     uint32_t *status;
     // fused append of the newest R tokens (nk == nullptr: none)
     const float *nk;
@@ -111,9 +110,17 @@ struct Work {
     int c;          // clamped context length
     int t_begin;    // first logical token of the partition
     int len;        // tokens in the partition
+    int np;         // partitions of this sequence
     bool single;    // the partition is the whole context
 };
 
+// Which (sequence, partition, kv head group) this CTA serves.  A context of
+// c tokens is cut into np = ceil(c / PT) partitions of PT tokens, the last
+// one taking the rest: each sequence gets its own partition count from its
+// own length (as the split-T decode of "attention.rs", attention_b, sizes each
+// row's workgroups from its visible length), so only contexts longer than PT
+// are split.  CTAs with p >= np have nothing to stream and return false; so
+// does partition 0 of an empty context, whose rows write_zero_rows writes.
 __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
     w.p = blockIdx.x;
     w.g = blockIdx.y / P.head_groups;
@@ -132,9 +139,10 @@ __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
         const int64_t craw = __ldg(P.cl + w.s);
         w.c = (int)(craw < cap ? craw : cap);
     }
+    w.np = max(1, (w.c + P.PT - 1) / P.PT);
     w.t_begin = w.p * P.PT;
     w.len = min(w.c - w.t_begin, P.PT);
-    w.single = w.c <= P.PT;
+    w.single = w.np == 1;
     return w.len > 0;
 }
 
@@ -151,7 +159,7 @@ __device__ __forceinline__ int64_t qrow(const Params &P, const Work &w, int vh) 
 // t_len = base_pos + b + 1).
 __device__ __forceinline__ int row_len(const Params &P, const Work &w, int vh) {
     const int cb = P.R == 1 ? w.c : w.c - (P.R - 1 - vh / P.r);
-    return max(0, min(cb - w.t_begin, P.PT));
+    return max(0, min(cb - w.t_begin, w.len));
 }
 
 // Fused append: quantise the sequence's newest R tokens (positions c-R ..
@@ -167,7 +175,7 @@ __device__ void append_tokens(const Params &P, const Work &w) {
     constexpr int WORDS = D / 4;
     constexpr int NW = (WORDS + 31) / 32;          // words per lane (head size 64: lanes 0..15)
     const int first = w.c - P.R;                    // position of new row 0 (may be < 0)
-    const int t_lo = max(first, w.t_begin), t_hi = min(w.c, w.t_begin + P.PT);
+    const int t_lo = max(first, w.t_begin), t_hi = min(w.c, w.t_begin + w.len);
     const int nvec = 2 * max(0, t_hi - t_lo);       // (token, K or V) vectors
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int v = warp; v < nvec; v += (int)(blockDim.x >> 5)) {
@@ -315,80 +323,161 @@ __device__ void drain(const Params &P, uint32_t bars, int ring, int consumed, in
 //
 // Merge the per-warp online-softmax states of the CTA (m in log2 units, l,
 // acc scaled by 2^(E - 139)) and write the output rows, or this
-// partition's partial (M, L, A) for the combine kernel.
+// partition's partial (M, L, A) for the combine.
+//
 // Log-sum-exp merge of all np partitions of this CTA's heads (run by the
 // last CTA of a (sequence, head group) to finish):
 // out = sum_p A_p 2^(M_p - M*) / sum_p L_p 2^(M_p - M*), M* = max M_p.
-// The partials of other CTAs are read through L2 (__ldcg).  scratch holds
-// (M*, 1/L) per head.
+// A head's np partial records (A_p, M_p, L_p; D + 4 floats each) are
+// contiguous in the workspace and were written by other CTAs (or this one).
+// `scratch` is the start of shared memory this CTA no longer needs, up to the
+// end of its dynamic allocation.  As many heads' records as fit come in with
+// one bulk copy per head, so a batch of heads costs one memory round trip;
+// the weights 2^(M_p - M*) then go into each record's spare word.  A head
+// whose records alone do not fit is read with vector loads instead.
+// Not inlined: it runs once, in the last CTA of a split sequence, and keeps
+// its registers out of the streaming loop's budget.
 template <int D>
-__device__ void combine_rows(const Params &P, const Work &w, int np, float *scratch) {
+__device__ __noinline__ void combine_rows(const Params &P, const Work &w, int np, uint8_t *scratch) {
+    constexpr int DP = D + 4;            // floats per partial record
+    constexpr int D4 = D / 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
-    for (int hh = warp; hh < w.nh; hh += nwarps) {
-        const int64_t row0 = qrow(P, w, w.h0 + hh) * P.NP;
-        // up to 32 partitions: each lane's (m, l) is read once
-        const float2 ml0 = lane < np ? __ldcg(reinterpret_cast<const float2 *>(P.pml + (row0 + lane) * 2))
-                                     : make_float2(-INFINITY, 0.0f);
-        float M = ml0.x;
-        for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(P.pml + (row0 + p) * 2));
+    const int nh = w.nh;
+    extern __shared__ __align__(16) uint8_t combine_dsm[];
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    const uintptr_t end = reinterpret_cast<uintptr_t>(combine_dsm) + dyn;
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(scratch) + 15) & ~(uintptr_t)15;
+    float *iL = reinterpret_cast<float *>(base + 16);                  // after the barrier: [nh] 1/L
+    const uintptr_t buf = (reinterpret_cast<uintptr_t>(iL + nh) + 127) & ~(uintptr_t)127;
+    const size_t head_bytes = (size_t)np * DP * 4;
+    const size_t fit = buf + head_bytes <= end ? (end - buf) / head_bytes : 0;
+    const int hb = fit < (size_t)nh ? (int)fit : nh;                   // heads per batch
+    auto record = [&](int h) { return P.part + qrow(P, w, w.h0 + h) * P.NP * DP; };
+
+    if (hb > 0) {
+        const uint32_t bar = smem_addr(reinterpret_cast<void *>(base));
+        const uint64_t policy = l2_policy_evict_first();
+        if (threadIdx.x == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        float *rows = reinterpret_cast<float *>(buf);                  // [hb][np][DP]
+        for (int h0 = 0, ph = 0; h0 < nh; h0 += hb, ph ^= 1) {
+            const int n = min(hb, nh - h0);
+            if (h0 > 0) __syncthreads();                               // the previous batch is consumed
+            if (warp == 0) {
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * head_bytes));
+                __syncwarp();
+                // other CTAs' generic stores, seen through the arrival counter,
+                // before this thread's bulk (async proxy) reads of them; and
+                // this CTA's earlier generic use of the buffer before the
+                // copies overwrite it
+                fence_proxy_async_global();
+                fence_proxy_async_smem();
+                for (int h = lane; h < n; h += 32)
+                    bulk_copy_g2s(smem_addr(rows + (size_t)h * np * DP), record(h0 + h), (uint32_t)head_bytes, bar,
+                                  policy);
+            }
+            if (!mbar_wait(bar, (uint32_t)ph)) {
+                flag_error(P.status, kDevWaitTimeout);
+                return;
+            }
+            // M* and 1/L per head (a warp per head, lanes over partitions); each
+            // partition's weight goes into its record's spare word
+            for (int h = warp; h < n; h += nwarps) {
+                float *rh = rows + (size_t)h * np * DP;
+                float M = -INFINITY;
+                for (int p = lane; p < np; p += 32) M = fmaxf(M, rh[p * DP + D]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+                if (M == -INFINITY) M = 0.0f;       // a query row that sees no token: weights 0, row 0
+                float L = 0.0f;
+                for (int p = lane; p < np; p += 32) {
+                    const float e = fast_exp2(rh[p * DP + D] - M);
+                    L += rh[p * DP + D + 1] * e;
+                    rh[p * DP + D + 2] = e;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+                if (lane == 0) iL[h0 + h] = L > 0.0f ? 1.0f / L : 0.0f;
+            }
+            __syncthreads();
+            // out[h][d] = (1/L) sum_p A_p[h][d] 2^(M_p - M*), summed over p in order
+            for (int i = threadIdx.x; i < n * D4; i += blockDim.x) {
+                const int hl = i / D4, d4 = i - hl * D4;
+                const float *rh = rows + (size_t)hl * np * DP;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p = 0; p < np; ++p) {
+                    const float4 v = reinterpret_cast<const float4 *>(rh + p * DP)[d4];
+                    const float x = rh[p * DP + D + 2];
+                    a.x = fmaf(v.x, x, a.x);
+                    a.y = fmaf(v.y, x, a.y);
+                    a.z = fmaf(v.z, x, a.z);
+                    a.w = fmaf(v.w, x, a.w);
+                }
+                const float il = iL[h0 + hl];
+                reinterpret_cast<float4 *>(P.out + qrow(P, w, w.h0 + h0 + hl) * D)[d4] =
+                    make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
+            }
+        }
+        return;
+    }
+    // Records too large for shared memory: M* and 1/L per head from the (m, l)
+    // words, then the weighted sums with eight partitions' vector loads in
+    // flight per thread, each weight recomputed from its m.
+    float *Ms = iL + nh;
+    for (int h = warp; h < nh; h += nwarps) {
+        const float *rh = record(h);
+        float M = -INFINITY;
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(rh + (size_t)p * DP + D));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        if (M == -INFINITY) M = 0.0f;       // a query row that sees no token: weights 0, row 0
-        float L = lane < np ? ml0.y * fast_exp2(ml0.x - M) : 0.0f;
-        for (int p = lane + 32; p < np; p += 32)
-            L += __ldcg(P.pml + (row0 + p) * 2 + 1) * fast_exp2(__ldcg(P.pml + (row0 + p) * 2) - M);
+        if (M == -INFINITY) M = 0.0f;
+        float L = 0.0f;
+        for (int p = lane; p < np; p += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(rh + (size_t)p * DP + D));
+            L += ml.y * fast_exp2(ml.x - M);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
         if (lane == 0) {
-            scratch[2 * hh] = M;
-            scratch[2 * hh + 1] = L > 0.0f ? 1.0f / L : 0.0f;
+            Ms[h] = M;
+            iL[h] = L > 0.0f ? 1.0f / L : 0.0f;
         }
     }
     __syncthreads();
-    // four output elements per thread at a time, eight partitions deep, so
-    // their loads overlap; the sum still runs over p in order
-    constexpr int U = 4, PU = 8;
-    const int n_out = w.nh * D;
-    for (int i0 = threadIdx.x; i0 < n_out; i0 += U * blockDim.x) {
-        float a[U], M[U];
-        int64_t prow[U];
-        int dd[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = min(i0 + u * (int)blockDim.x, n_out - 1);
-            const int hh = i / D;
-            dd[u] = i % D;
-            prow[u] = qrow(P, w, w.h0 + hh) * P.NP;
-            M[u] = scratch[2 * hh];
-            a[u] = 0.0f;
-        }
+    constexpr int PU = 8;
+    for (int i = threadIdx.x; i < nh * D4; i += blockDim.x) {
+        const int h = i / D4, d4 = i - h * D4;
+        const float *rh = record(h);
+        const float M = Ms[h];
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p0 = 0; p0 < np; p0 += PU) {
-            float v[U][PU], m[U][PU];
+            float4 v[PU];
+            float m[PU];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int j = 0; j < PU; ++j) {
+                const int p = min(p0 + j, np - 1);
+                v[j] = __ldcg(reinterpret_cast<const float4 *>(rh + (size_t)p * DP) + d4);
+                m[j] = __ldcg(rh + (size_t)p * DP + D);
+            }
 #pragma unroll
-                for (int j = 0; j < PU; ++j) {
-                    const int p = min(p0 + j, np - 1);
-                    v[u][j] = __ldcg(P.pacc + (prow[u] + p) * D + dd[u]);
-                    m[u][j] = __ldcg(P.pml + (prow[u] + p) * 2);
+            for (int j = 0; j < PU; ++j) {
+                if (p0 + j < np) {
+                    const float x = fast_exp2(m[j] - M);
+                    a.x = fmaf(v[j].x, x, a.x);
+                    a.y = fmaf(v[j].y, x, a.y);
+                    a.z = fmaf(v[j].z, x, a.z);
+                    a.w = fmaf(v[j].w, x, a.w);
                 }
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-#pragma unroll
-                for (int j = 0; j < PU; ++j)
-                    if (p0 + j < np) a[u] = fmaf(v[u][j], fast_exp2(m[u][j] - M[u]), a[u]);
-            }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * (int)blockDim.x;
-            if (i < n_out) {
-                const int hh = i / D;
-                P.out[qrow(P, w, w.h0 + hh) * D + dd[u]] = a[u] * scratch[2 * hh + 1];
-            }
-        }
+        const float il = iL[h];
+        reinterpret_cast<float4 *>(P.out + qrow(P, w, w.h0 + h) * D)[d4] =
+            make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
     }
 }
 
@@ -427,11 +516,11 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
             // a query row that sees no token (L = 0) gets a zero row
             P.out[qr * D + d] = f[n_slots + 1] > 0.0f ? A / f[n_slots + 1] : 0.0f;
         } else {
-            const int64_t row = qr * P.NP + w.p;
-            P.pacc[row * D + d] = A;
+            float *rec = P.part + (qr * P.NP + w.p) * (D + 4);
+            rec[d] = A;
             if (d == 0) {
-                P.pml[row * 2] = f[n_slots];
-                P.pml[row * 2 + 1] = f[n_slots + 1];
+                rec[D] = f[n_slots];
+                rec[D + 1] = f[n_slots + 1];
             }
         }
     }
@@ -440,7 +529,7 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
     // merges every partition (threadfence / counter handshake).
     __threadfence();
     __syncthreads();
-    const int np = (w.c + P.PT - 1) / P.PT;
+    const int np = w.np;
     int *last = reinterpret_cast<int *>(fac);
     if (threadIdx.x == 0) {
         const uint32_t prev = atomicAdd(P.counters + (int64_t)w.s * gridDim.y + blockIdx.y, 1u);
@@ -451,7 +540,8 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    combine_rows<D>(P, w, np, fac);
+    // the merge's own scratch (ml, accs) is no longer needed
+    combine_rows<D>(P, w, np, reinterpret_cast<uint8_t *>(const_cast<float *>(ml)));
 }
 
 // The attention grid is launched as a programmatic dependent of the prep

@@ -62,13 +62,13 @@ struct DecodeArgs {
     int per_sm;            // CTAs per SM the waves are sized for (selects the contiguous
                            // kernel's register budget)
     // workspace: sequence order [S] (u64: clamped length << 32 | sequence,
-    // longest context first); when
-    // partitions > 1 also arrival counters [S][Hk * head_groups] (u32),
-    // m,l [S][H][P][2] and acc [S][H][P][D] (f32)
+    // longest context first); when partitions > 1 also arrival counters
+    // [S][Hk * head_groups] (u32) and one partial record per (sequence, query
+    // row, head, partition): [S][R][H][P][head_size + 4] f32, the weighted sum
+    // A followed by m, l and two spare words
     unsigned long long *order;
     uint32_t *counters;
-    float *partial_ml;
-    float *partial_acc;
+    float *partials;
     uint32_t *status;
     // fused append (new_key == nullptr: none): rows [num_seqs][num_rows] of
     // num_kv_heads * head_size floats, row (s, b) at new_key + (s * num_rows +

@@ -223,3 +223,58 @@ def test_many_sequences_take_every_ordering_path(S):
         for pt in (0, 128):
             assert_close(gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt), want,
                          f"S {S} kernel {kernel} pt {pt}")
+
+
+MIXED_LENS = [0, 1, 31, 33, 5000, 20000, 700, 4096, 4097, 12345, 129, 64, 9000, 2, 16384, 333]
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("pt", [0, 256, 1024, 4096])
+def test_mixed_per_sequence_splits_against_oracle(kernel, pt):
+    """Contexts from empty to 20000 tokens in one batch, so some sequences are
+    split into many equal partitions (the 20000-token one into 79 at 256,
+    more than the 32 the combine keeps in shared memory), some into two and
+    most not at all."""
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode, oracle_decode
+    lens = MIXED_LENS
+    w, ok_, ov_, kc, vc = _random_case(len(lens), 8, 2, 128, 16, lens, seed=32)
+    want = oracle_decode(w, ok_, ov_)
+    got = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+    assert_close(got, want, f"kernel {kernel} pt {pt}")
+    assert np.all(got[0] == 0.0)
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("R", [2, 5])
+def test_mixed_per_sequence_splits_multi_row(R):
+    """The same batch with R causal query rows per sequence on every family
+    (tcgen05 takes R * r > 32 pairs)."""
+    from tests.gpu_helpers import (assert_close, device_status, gpu_decode_rows, oracle_decode_rows,
+                                   random_case)
+    lens = MIXED_LENS
+    w, ok_, ov_, kc, vc = random_case(len(lens), 16, 2, 128, 16, lens, seed=33)
+    q = np.random.default_rng(R).standard_normal((len(lens), R, 16, 128)).astype(np.float32)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    for kernel in (0, CC, TC, 3):
+        for pt in (0, 512):
+            got = gpu_decode_rows(w, kc, vc, q, kernel=kernel, partition_tokens=pt)
+            assert_close(got, want, f"R {R} kernel {kernel} pt {pt}")
+    assert device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("D", [128, 256])
+def test_combine_of_many_partitions(kernel, D):
+    """A 40000-token context split at 1024 tokens (40 partial records per
+    head: the combine fetches a few heads' records per batch into shared
+    memory) and at 128 tokens (313 records per head: more than shared memory
+    holds, so the combine reads them with vector loads)."""
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode, oracle_decode
+    lens = [40000, 3000, 0, 1]
+    w, ok_, ov_, kc, vc = _random_case(len(lens), 8, 2, D, 32, lens, seed=41 + D)
+    want = oracle_decode(w, ok_, ov_)
+    for pt in (1024, 128):
+        got = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+        assert_close(got, want, f"D {D} kernel {kernel} pt {pt}")
+        assert np.all(got[2] == 0.0)
+    assert device_status() == 0
