@@ -29,6 +29,12 @@
 // warp leaves only after the copies it issued have landed.
 #include "decode_common.cuh"
 
+// Partition length, in quarters of the table's capacity, when the sequences
+// fill less than two waves of resident CTAs (4: no cut)
+#ifndef PA_Q8_TAIL_CUT_X4
+#define PA_Q8_TAIL_CUT_X4 3
+#endif
+
 namespace pa_q8 {
 namespace {
 
@@ -1011,8 +1017,12 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
         if (units >= slots) {
             // Enough (sequence, kv head) work items: one partition per context
             // (up to 8192 tokens).  The grid runs the longest contexts first,
-            // so the tail holds short ones.
-            pt = (int)std::min<int64_t>((max_ctx + 127) / 128 * 128, 8192);
+            // so the tail holds short ones.  Within two waves, the longest
+            // contexts alone would set that tail: those in the top quarter of
+            // the table's capacity are cut in two (measured on 64 x U[512,
+            // 4096] contexts: 3072-token partitions 65-66 us against 68 us)
+            const int64_t cut = units < 2 * slots ? (max_ctx * PA_Q8_TAIL_CUT_X4 + 3) / 4 : max_ctx;
+            pt = (int)std::min<int64_t>((cut + 127) / 128 * 128, 8192);
         } else {
             // Few, long contexts: split so that the expected work (contexts
             // taken at half their maximum) fills about two waves of resident

@@ -335,10 +335,8 @@ __device__ void drain(const Params &P, uint32_t bars, int ring, int consumed, in
 // one bulk copy per head, so a batch of heads costs one memory round trip;
 // the weights 2^(M_p - M*) then go into each record's spare word.  A head
 // whose records alone do not fit is read with vector loads instead.
-// Not inlined: it runs once, in the last CTA of a split sequence, and keeps
-// its registers out of the streaming loop's budget.
 template <int D>
-__device__ __noinline__ void combine_rows(const Params &P, const Work &w, int np, uint8_t *scratch) {
+__device__ __forceinline__ void combine_rows(const Params &P, const Work &w, int np, uint8_t *scratch) {
     constexpr int DP = D + 4;            // floats per partial record
     constexpr int D4 = D / 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -481,7 +479,16 @@ __device__ __noinline__ void combine_rows(const Params &P, const Work &w, int np
     }
 }
 
+// combine_rows as a call of its own, for kernels whose register budget is
+// tight (the tcgen05 family: 96 per thread): it runs once per split sequence,
+// and keeping it out of line keeps its registers out of the streaming loop's
+// allocation.  The other families inline it (measured slightly faster).
 template <int D>
+__device__ __noinline__ void combine_rows_outlined(const Params &P, const Work &w, int np, uint8_t *scratch) {
+    combine_rows<D>(P, w, np, scratch);
+}
+
+template <int D, bool kOutlineCombine = false>
 __device__ void merge_and_store(const Params &P, const Work &w, const float *ml, const float *accs,
                                 int n_slots, int heads_stride, float *fac) {
     // ml: [slot][head][3] = (m, l, E); accs: [slot][head][D]; fac: scratch
@@ -541,7 +548,9 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
     if (!is_last) return;
     __threadfence();
     // the merge's own scratch (ml, accs) is no longer needed
-    combine_rows<D>(P, w, np, reinterpret_cast<uint8_t *>(const_cast<float *>(ml)));
+    uint8_t *scratch = reinterpret_cast<uint8_t *>(const_cast<float *>(ml));
+    if constexpr (kOutlineCombine) combine_rows_outlined<D>(P, w, np, scratch);
+    else combine_rows<D>(P, w, np, scratch);
 }
 
 // The attention grid is launched as a programmatic dependent of the prep

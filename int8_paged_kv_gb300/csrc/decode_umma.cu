@@ -494,7 +494,7 @@ decode_umma_kernel(Params P) {
     }
     float *ml = reinterpret_cast<float *>(sQ);
     float *accs = ml + kUmmaHeads * 3;
-    merge_and_store<D>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
+    merge_and_store<D, true>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
 }
 
 template <int D>
