@@ -6,9 +6,12 @@
 // halves away from zero; 4 codes per u32 (code l in byte l); then the f32
 // bits of amax/127 (1.0 for amax = 0); slot 0xFFFFFFFF skips the row.
 //
-// GB300 mapping: one warp per (token, pair of kv heads), eight lanes per
-// K or V vector, so the per-vector reductions and divisions of four vectors
-// share instructions; loads are 16-byte vectors issued before the slot read.
+// GB300 mapping: a warp per (token, pair of kv heads), eight lanes per K or
+// V vector, so the per-vector reductions and divisions of four vectors share
+// instructions.  Large appends of 16-byte aligned rows run as one wave of
+// CTAs whose warps walk a series of tokens, reading each token's slot ahead of
+// its rows (PAD rows are never read); other appends take one token per warp,
+// its 16-byte row loads issued before the slot read.
 // Every f32 operation is an explicit round-to-nearest intrinsic, so nothing
 // is contracted or approximated and the words match an IEEE reference bit
 // for bit.
@@ -22,6 +25,17 @@ namespace pa_q8 {
 namespace {
 
 constexpr int kWriterWarps = 8;
+// The walking writer (one wave of CTAs, each warp a series of tokens) takes
+// appends of at least kWalkTokensPerWarp tokens per warp of that wave
+#ifndef PA_Q8_WRITER_WALK
+#define PA_Q8_WRITER_WALK 1
+#endif
+constexpr int kWalkTokensPerWarp = 2;
+// tokens whose rows a walking warp has in flight
+#ifndef PA_Q8_WRITER_WALK_DEPTH
+#define PA_Q8_WRITER_WALK_DEPTH 1
+#endif
+constexpr int kWalkDepth = PA_Q8_WRITER_WALK_DEPTH;
 
 template <bool kVec>
 __device__ __forceinline__ float4 load4(const float *p) {
@@ -99,6 +113,96 @@ quant_scatter_kernel(const float *__restrict__ key, const float *__restrict__ va
     if (j == 0) cache[dst + WORDS] = __float_as_uint(scale);
 }
 
+// The same arithmetic with every warp walking a strided series of tokens for
+// one pair of kv heads (16-byte aligned rows only), as one wave of CTAs.  A
+// token's slot is read DEPTH + 1 tokens ahead and its rows DEPTH tokens
+// ahead, so a PAD row is never read and no slot round trip sits in front of
+// the row loads: while a warp quantises token i, the rows of the next DEPTH
+// tokens and the slot of the one after are in flight.  One token ahead
+// measured as fast as the one-token warps (30.6 against 30.7 us for the
+// 16384-row append) with 5% fewer bytes read; two and three ahead were slower
+// (31.6, 31.0 us: more registers, fewer CTAs per SM).
+template <int D, int DEPTH>
+__global__ void __launch_bounds__(kWriterWarps * 32)
+quant_scatter_walk_kernel(const float *__restrict__ key, const float *__restrict__ value,
+                          uint32_t *__restrict__ key_cache, uint32_t *__restrict__ value_cache,
+                          const uint32_t *__restrict__ slot_mapping, int num_tokens,
+                          int64_t key_stride, int64_t value_stride, int num_kv_heads,
+                          int block_size, int log2_block, int64_t num_slots, uint32_t *status) {
+    grid_dependents_launch();
+    constexpr int WORDS = D / 4;
+    constexpr int G = kLanesPerVector;
+    constexpr int NW = WORDS / G;
+    const int lane = threadIdx.x & 31;
+    const int stride = (int)gridDim.x * kWriterWarps;
+    int tok = blockIdx.x * kWriterWarps + (threadIdx.x >> 5);
+    const int v = lane / G, j = lane % G;
+    const bool is_v = v & 1;
+    const int h = 2 * blockIdx.y + (v >> 1);
+    const bool live = h < num_kv_heads;
+    const float *base = is_v ? value + (int64_t)h * D : key + (int64_t)h * D;
+    const int64_t row_stride = is_v ? value_stride : key_stride;
+    uint32_t *cache = is_v ? value_cache : key_cache;
+    auto slot_at = [&](int t) { return t < num_tokens ? __ldg(slot_mapping + t) : kPadSlot; };
+    auto load_rows = [&](int t, uint32_t slot, float4 (&x)[NW]) {
+        const bool want = live && t < num_tokens && slot != kPadSlot;
+        const float *src = base + (int64_t)t * row_stride;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            x[i] = want ? load4<true>(src + 4 * (j + G * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    // rows of the next DEPTH tokens in flight (x[0] the current one), slots of
+    // one more token ahead
+    uint32_t sl[DEPTH + 1];
+    float4 x[DEPTH][NW];
+#pragma unroll
+    for (int d = 0; d <= DEPTH; ++d) sl[d] = slot_at(tok + d * stride);
+#pragma unroll
+    for (int d = 0; d < DEPTH; ++d) load_rows(tok + d * stride, sl[d], x[d]);
+    for (; tok < num_tokens; tok += stride) {
+        const uint32_t slot = sl[0];
+        float4 cur[NW];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) cur[i] = x[0][i];
+        // shift the window: rows of token tok + DEPTH * stride, slot one further
+#pragma unroll
+        for (int d = 0; d + 1 < DEPTH; ++d) {
+#pragma unroll
+            for (int i = 0; i < NW; ++i) x[d][i] = x[d + 1][i];
+        }
+#pragma unroll
+        for (int d = 0; d < DEPTH; ++d) sl[d] = sl[d + 1];
+        load_rows(tok + DEPTH * stride, sl[DEPTH - 1], x[DEPTH - 1]);
+        sl[DEPTH] = slot_at(tok + (DEPTH + 1) * stride);
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(cur[i].x), fabsf(cur[i].y)), fmaxf(fabsf(cur[i].z), fabsf(cur[i].w))));
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float inv = m > 0.0f ? __fdiv_rn(127.0f, m) : 0.0f;
+        const float scale = m > 0.0f ? __fdiv_rn(m, 127.0f) : 1.0f;
+        if (slot != kPadSlot && live) {
+            if ((int64_t)slot >= num_slots) {
+                if (j == 0) flag_error(status, kDevBadSlot);
+            } else {
+                uint32_t blk, off;
+                if (log2_block >= 0) {
+                    blk = slot >> log2_block;
+                    off = slot & ((1u << log2_block) - 1u);
+                } else {
+                    blk = slot / (uint32_t)block_size;
+                    off = slot - blk * (uint32_t)block_size;
+                }
+                const int64_t dst = (((int64_t)blk * num_kv_heads + h) * block_size + off) * (WORDS + 1);
+#pragma unroll
+                for (int i = 0; i < NW; ++i) cache[dst + j + G * i] = pack_word(cur[i], inv);
+                if (j == 0) cache[dst + WORDS] = __float_as_uint(scale);
+            }
+        }
+    }
+}
+
 template <int D>
 cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
     const int64_t head_pairs = (a.num_kv_heads + 1) / 2;
@@ -112,7 +216,20 @@ cudaError_t launch_d(const WriterArgs &a, cudaStream_t stream) {
         log2_block = 0;
         while ((1 << log2_block) < a.block_size) ++log2_block;
     }
-    if (vec) {
+    int sms = 0, dev = 0, per_sm = 0;
+    if (PA_Q8_WRITER_WALK && vec && cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_scatter_walk_kernel<D, kWalkDepth>,
+                                                      kWriterWarps * 32, 0) ==
+            cudaSuccess &&
+        per_sm > 0 && grid.x > (unsigned)(kWalkTokensPerWarp * per_sm * sms / head_pairs)) {
+        // enough tokens for every warp to walk several: one wave of CTAs
+        const dim3 wgrid((unsigned)((per_sm * sms + head_pairs - 1) / head_pairs), (unsigned)head_pairs);
+        quant_scatter_walk_kernel<D, kWalkDepth><<<wgrid, kWriterWarps * 32, 0, stream>>>(
+            a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens,
+            a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, log2_block, num_slots, a.status);
+    } else if (vec) {
+        cudaGetLastError();
         quant_scatter_kernel<D, true><<<grid, kWriterWarps * 32, 0, stream>>>(
             a.key, a.value, a.key_cache, a.value_cache, a.slot_mapping, (int)a.num_tokens,
             a.key_stride, a.value_stride, a.num_kv_heads, a.block_size, log2_block, num_slots, a.status);
