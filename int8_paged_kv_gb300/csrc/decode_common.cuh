@@ -85,6 +85,11 @@ constexpr int kUmmaAutoPairs = 32;
 #ifndef PA_Q8_TC_RING_256
 #define PA_Q8_TC_RING_256 2
 #endif
+// Head size 256, one-tile (8-head) tensor-core CTAs: CTAs per SM the
+// register budget targets (shared memory holds one at ring depth 2)
+#ifndef PA_Q8_TC_MINB_256
+#define PA_Q8_TC_MINB_256 1
+#endif
 // Virtual heads per one-tile tensor-core CTA (decode_tc_kernel) at head
 // sizes 64 / 128.  Several such CTAs per kv head each read the K/V (the
 // second read mostly from L2) and convert its codes again.
@@ -223,6 +228,17 @@ __device__ void write_zero_rows(const Params &P, const Work &w) {
 }
 
 __host__ __device__ constexpr uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Bytes of the CTA merge's scratch (merge_and_store): per-slot (m, l, E)
+// and accumulators of every head, then the per-head factors.  The kernels
+// carve it out of their chunk ring once the streams are drained, so it must
+// fit there (checked at compile time per kernel).
+__host__ __device__ constexpr uint32_t merge_scratch_bytes(int D, int slots, int heads) {
+    return (uint32_t)(slots * heads * (3 + D) + heads * (slots + 2)) * 4u;
+}
+__host__ __device__ constexpr uint32_t ring_bytes(int D, int streams, int ring) {
+    return (uint32_t)streams * ring * ((2u * kChunk * (D / 4 + 1) * 4 + 127) / 128 * 128);
+}
 
 // Shared-memory layout (bytes from the dynamic base).
 struct Layout {
