@@ -61,8 +61,9 @@ constexpr uint32_t kIssuePollNs = 256;
 
 template <int D>
 __host__ __device__ constexpr int umma_ring() { return 3; }
+// TMEM columns: S twice (64), O (D), the Q tile (D / 2: two f16 per column)
 template <int D>
-__host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 64 ? 128u : (D == 128 ? 256u : 512u); }
+__host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 256 ? 512u : 256u; }
 // resident CTAs per SM: TMEM (512 columns) and registers (2 x 288 threads)
 template <int D>
 __host__ __device__ constexpr int umma_ctas_per_sm() { return D == 256 ? 1 : 2; }
@@ -170,8 +171,16 @@ decode_umma_kernel(Params P) {
     const int half = lo_part ? 16 : 0;
     const int len_row = row_ok ? row_len(P, w, vh) : 0;
     const int row = 32 * (warp & 3) + lane, row_hi = 32 * (warp & 3) + (lane & 15), row_lo = row_hi + 16;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();                                  // barriers initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + L.misc);
+    const uint32_t tO = tmem + 64;
+    const uint32_t tQ = tO + D;                       // the Q tile: D / 2 columns
     float qk2 = 0.0f;
-    if (warp < 4) {      // Q row: q * 2^-eq as hi (or lo) f16, K-major
+    if (warp < 4) {
+        // Q row: q * 2^-eq as hi (or lo) f16, two per column of this thread's TMEM lane
         const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
         float mx = 0.0f;
         for (int c = 0; c < D / 4; ++c) {
@@ -181,24 +190,28 @@ decode_umma_kernel(Params P) {
         const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
         const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
         qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
-        for (int c = 0; c < D / 8; ++c) {
-            const float4 a = row_ok ? __ldg(qv + 2 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 b = row_ok ? __ldg(qv + 2 * c + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-            uint32_t h[4], l[4];
-            split_f16x2(a.x * down, a.y * down, h[0], l[0]);
-            split_f16x2(a.z * down, a.w * down, h[1], l[1]);
-            split_f16x2(b.x * down, b.y * down, h[2], l[2]);
-            split_f16x2(b.z * down, b.w * down, h[3], l[3]);
-            *reinterpret_cast<uint4 *>(sQ + kmaj_off(row, 8 * c, D)) =
-                lo_part ? make_uint4(l[0], l[1], l[2], l[3]) : make_uint4(h[0], h[1], h[2], h[3]);
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            float words[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {                 // words c0 + j .. + 3: elements 2(c0 + j) .. + 7
+                const int e4 = (2 * (c0 + j)) / 4;
+                const float4 a = row_ok ? __ldg(qv + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 b = row_ok ? __ldg(qv + e4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t h[4], l[4];
+                split_f16x2(a.x * down, a.y * down, h[0], l[0]);
+                split_f16x2(a.z * down, a.w * down, h[1], l[1]);
+                split_f16x2(b.x * down, b.y * down, h[2], l[2]);
+                split_f16x2(b.z * down, b.w * down, h[3], l[3]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) words[j + u] = __uint_as_float(lo_part ? l[u] : h[u]);
+            }
+            tmem_st32(tQ + lane_base + c0, words);
         }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();                                  // the Q tile is in TMEM
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + L.misc);
-    const uint32_t tO = tmem + 64;
 
     // softmax state (warps 0-3) and the issuer's commit record (warp 7, lane 0)
     float m = -INFINITY, lsum = 0.0f;
@@ -266,8 +279,7 @@ decode_umma_kernel(Params P) {
                 const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    umma_f16(tS, umma_smem_desc(aQ + ks * 256, 128, D * 16),
-                             umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
+                    umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
                 umma_commit(bar(kBarQk, b));
                 last_commit = kBarQk + b;
                 last_parity = (nq >> 1) & 1;
