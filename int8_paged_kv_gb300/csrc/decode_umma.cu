@@ -14,8 +14,9 @@ namespace {
 // partition.  TMEM lane quadrant q holds M rows 32q .. 32q+31: rows 32q + j
 // (j < 16) the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq like
 // the mma.sync kernel), rows 32q + 16 + j its lo part, so a logit's two
-// halves are one shuffle apart.  TMEM holds S twice (columns 0-31, 32-63) and
-// O (D columns).
+// halves are one shuffle apart.  TMEM holds S twice (columns 0-31, 32-63), O
+// (D columns) and the Q tile itself (D / 2 columns, two f16 per column of a
+// row's lane), which QK takes as its A operand from tensor memory.
 //
 // Warp roles, linked only by mbarriers (every wait bounded and abortable):
 //  - warps 0-3, softmax: warp q owns quadrant q (idle when it holds no head).
