@@ -504,6 +504,29 @@ __device__ __noinline__ void combine_rows_outlined(const Params &P, const Work &
     combine_rows<D>(P, w, np, scratch);
 }
 
+// Split context, after this CTA stored its partial records: the last CTA of
+// the (sequence, head group) to arrive merges every partition (threadfence /
+// counter handshake).  Called by every thread of the CTA; scratch is shared
+// memory free up to the end of the dynamic allocation.
+template <int D, bool kOutlineCombine = false>
+__device__ void arrive_and_combine(const Params &P, const Work &w, uint8_t *scratch) {
+    __threadfence();
+    __syncthreads();
+    const int np = w.np;
+    int *last = reinterpret_cast<int *>(scratch);
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(P.counters + (int64_t)w.s * gridDim.y + blockIdx.y, 1u);
+        *last = (prev == (uint32_t)(np - 1));
+    }
+    __syncthreads();
+    const bool is_last = *last != 0;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    if constexpr (kOutlineCombine) combine_rows_outlined<D>(P, w, np, scratch);
+    else combine_rows<D>(P, w, np, scratch);
+}
+
 template <int D, bool kOutlineCombine = false>
 __device__ void merge_and_store(const Params &P, const Work &w, const float *ml, const float *accs,
                                 int n_slots, int heads_stride, float *fac) {
@@ -548,25 +571,8 @@ __device__ void merge_and_store(const Params &P, const Work &w, const float *ml,
         }
     }
     if (w.single) return;
-    // Split context: the last CTA of this (sequence, head group) to arrive
-    // merges every partition (threadfence / counter handshake).
-    __threadfence();
-    __syncthreads();
-    const int np = w.np;
-    int *last = reinterpret_cast<int *>(fac);
-    if (threadIdx.x == 0) {
-        const uint32_t prev = atomicAdd(P.counters + (int64_t)w.s * gridDim.y + blockIdx.y, 1u);
-        *last = (prev == (uint32_t)(np - 1));
-    }
-    __syncthreads();
-    const bool is_last = *last != 0;
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
     // the merge's own scratch (ml, accs) is no longer needed
-    uint8_t *scratch = reinterpret_cast<uint8_t *>(const_cast<float *>(ml));
-    if constexpr (kOutlineCombine) combine_rows_outlined<D>(P, w, np, scratch);
-    else combine_rows<D>(P, w, np, scratch);
+    arrive_and_combine<D, kOutlineCombine>(P, w, reinterpret_cast<uint8_t *>(const_cast<float *>(ml)));
 }
 
 // The attention grid is launched as a programmatic dependent of the prep

@@ -11,38 +11,51 @@ namespace {
 // Many virtual heads per kv head (multi-row decode: R query rows x r heads)
 // make the contraction GEMM-shaped, so it runs on the 5th-generation tensor
 // cores: one CTA serves up to 64 virtual heads of one kv head for one
-// partition.  TMEM lane quadrant q holds M rows 32q .. 32q+31: rows 32q + j
-// (j < 16) the hi f16 part of virtual head 16q + j's q (scaled by 2^-eq like
-// the mma.sync kernel), rows 32q + 16 + j its lo part, so a logit's two
-// halves are one shuffle apart.  TMEM holds S twice (columns 0-31, 32-63), O
-// (D columns) and the Q tile itself (D / 2 columns, two f16 per column of a
-// row's lane), which QK takes as its A operand from tensor memory.
+// partition.
+//
+// Precision: K and V codes are exact in f16; q and the weights P are not, so
+// each is split into an f16 hi part and the f16 residual (lo), about 22
+// significant bits together (q scaled by 2^-eq per row first, like the
+// mma.sync kernel).  The two parts are separate rows of the M = 128 MMAs:
+// TMEM lane quadrant q holds rows 32q + j (j < 16: the hi part of virtual
+// head 16q + j) and 32q + 16 + j (its lo part), for the Q tile (the A
+// operand of S = Q.K^T, read from tensor memory: D / 2 columns, two f16 per
+// column), for S (two chunk buffers of 32 columns) and for O (D columns),
+// and the P tile in shared memory has the same rows.  A logit is the sum of
+// its two rows, an output row the sum of its two O rows.
+//
+// Each softmax thread owns one virtual head and 16 of a chunk's 32 tokens:
+// two 16x32bx2 loads (lane bases 32q and 32q + 16) give thread t the hi and
+// the lo row of head 16q + t % 16 at tokens 16 (t / 16) .. + 15, so a logit
+// is one paired add, with no exchange between threads.
 //
 // Warp roles, linked only by mbarriers (every wait bounded and abortable):
-//  - warps 0-3, softmax: warp q owns quadrant q (idle when it holds no head).
-//    Per chunk: S row -> online softmax (hi/lo partner threads take 16 tokens
-//    each; lazy rescale of O rows in TMEM) -> P tile rows (w = p * v_scale *
-//    2^(131 - E), split hi/lo like the mma.sync kernel).
+//  - warps 0-3, softmax: first the Q tile (row max -> 2^-eq -> hi/lo into
+//    tensor memory, while the ring fills), then per chunk: S half-rows ->
+//    online softmax with a lazy reference max (O rows rescaled in TMEM only
+//    when it moves past 2^kLazy, or the weight scale changes) -> P half-rows
+//    as hi and lo f16.  The per-logit arithmetic runs on f32 pairs.
 //  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
 //    the other families) become f16 K and V tiles [32 tokens][D] in the
-//    same core-matrix layout (K-major for QK's B, MN-major for PV's B) and
-//    the token scales a small table.
-//  - warp 7: its lane 0 issues S = Q.K^T (M 128, N 32, K D) and O += P.V
-//    (M 128, N D, K 32), each as soon as its inputs are ready.
+//    core-matrix layout (K-major for QK's B, MN-major for PV's B), and the
+//    chunk's scale table: the K scales, the V scales times the weight scale
+//    2^(131 - E) (E the largest V-scale exponent of the partition so far),
+//    and E; tokens past the partition get scale 0.
+//  - warp 7: its lane 0 issues S = Q.K^T and O += P.V, each as soon as its
+//    inputs are ready.
 //  - warp 8: refills the raw ring, chunk c into the slot of chunk c - ring
-//    once the conversion has read that slot (slot_free[slot]).  A refill
-//    costs about as much as issuing both MMAs of a chunk, so it has a warp of
-//    its own.
+//    once the conversion has read that slot (slot_free[slot]).
 // K, V, P and S are double buffered by chunk parity.  Signals per buffer
-// b = chunk & 1: k_ready[b] (96 conversion threads: K tile and the token
-// scale table written), v_ready[b] (the same threads: V tile written),
-// s_free[b] / p_ready[b] (the active softmax threads), qk[b] / pv[b]
-// (tcgen05.commit).  QK and the softmax wait only for k_ready, so a chunk's
-// logits do not wait for its V tile, whose conversion waits for PV two chunks
-// back.  A waiter never falls two phases behind: the next phase of each
-// barrier needs a step that follows the wait (v_ready(j + 2) needs PV(j),
-// issued after the issue warp saw v_ready(j); slot_free for chunk c + ring
-// needs the refill issued after the wait for chunk c).
+// b = chunk & 1: k_ready[b] (96 conversion threads: K tile and scale table
+// written), v_ready[b] (the same threads: V tile written), s_free[b] /
+// p_ready[b] (the active softmax threads), qk[b] / pv[b] (tcgen05.commit),
+// and q_ready once (the 128 softmax threads: Q tile stored).  QK and the
+// softmax wait only for k_ready, so a chunk's logits do not wait for its V
+// tile, whose conversion waits for PV two chunks back.  A waiter never falls
+// two phases behind: the next phase of each barrier needs a step that
+// follows the wait (v_ready(j + 2) needs PV(j), issued after the issue warp
+// saw v_ready(j); slot_free for chunk c + ring needs the refill issued after
+// the wait for chunk c).
 
 // conversion warps (4 measured slower than 3: large R = 8 0.96 against 0.93 ms)
 #ifndef PA_Q8_UMMA_CONV_WARPS
@@ -59,10 +72,11 @@ constexpr int kUmmaConvThreads = 32 * kUmmaConvWarps;
 // longest suspension of the issue warp on one pending input before it polls
 // the other again (64 and 32 ns measured the same)
 constexpr uint32_t kIssuePollNs = 256;
+static_assert(kUmmaHeads == 64, "64 virtual heads: hi and lo rows of one M = 128 tile");
 
 template <int D>
 __host__ __device__ constexpr int umma_ring() { return 3; }
-// TMEM columns: S twice (64), O (D), the Q tile (D / 2: two f16 per column)
+// TMEM columns: S twice (64), O (D), the Q tile (D / 2)
 template <int D>
 __host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 256 ? 512u : 256u; }
 // resident CTAs per SM: TMEM (512 columns) and registers (2 x 288 threads)
@@ -77,16 +91,16 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
 
 // barrier slots (8 bytes each) after the ring's
 enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarVReady = 4, kBarSFree = 6, kBarPReady = 8, kBarKReady = 10,
-               kBarSlotFree = 12, kUmmaBars = 16 };     // slot_free: one per raw ring slot (ring <= 4)
+               kBarQReady = 12, kBarSlotFree = 13, kUmmaBars = 17 };   // slot_free: one per raw ring slot (ring <= 4)
 
 struct UmmaLayout {
     uint32_t misc, scales, table, ops, ring, slot_bytes, total;
 };
 
-// [barriers: ring, kUmmaBars] [TMEM address, abort flag] [token scales 2 x
-// (K, V) x 32] [table] [operand tiles Q, K x2, V x2, P x2] [raw chunk ring].
-// Total at least a 1/(n+1) share of the shared memory, so no more CTAs share
-// an SM than its TMEM serves.
+// [barriers: ring, kUmmaBars] [TMEM address, abort flag] [scale tables: K
+// 2 x 32, weighted V 2 x 32, E 2] [block table] [operand tiles K x2, V x2,
+// P x2] [raw chunk ring].  Total at least a 1/(n+1) share of the
+// shared memory, so no more CTAs share an SM than its TMEM serves.
 template <int D>
 __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
     constexpr int RING = umma_ring<D>();
@@ -95,9 +109,9 @@ __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
     const int pieces = (PT + ptok - 1) / ptok + 1;
     L.misc = (RING + kUmmaBars) * 8;
     L.scales = align_up(L.misc + 8, 16);
-    L.table = L.scales + 2 * 2 * kChunk * 4;
+    L.table = L.scales + align_up(2 * 2 * kChunk * 4 + 2 * 4, 16);
     L.ops = align_up(L.table + pieces * 4, 128);
-    const uint32_t ops_bytes = 128u * D * 2 + 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * 32 * 2);
+    const uint32_t ops_bytes = 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * kChunk * 2);
     L.ring = align_up(L.ops + ops_bytes, 128);
     L.slot_bytes = align_up(2u * kChunk * (D / 4 + 1) * 4, 128);
     L.total = L.ring + RING * L.slot_bytes;
@@ -113,7 +127,8 @@ decode_umma_kernel(Params P) {
     static_assert(RING <= kUmmaBars - kBarSlotFree, "one slot_free barrier per raw ring slot");
     constexpr int W = D / 4 + 1;
     constexpr uint32_t TCOLS = umma_tmem_cols<D>();
-    constexpr uint32_t Q_BYTES = 128u * D * 2, K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
+    static_assert(64 + D + D / 2 <= (int)TCOLS, "S twice, O and the Q tile in the allocation");
+    constexpr uint32_t K_BYTES = 32u * D * 2, V_BYTES = (uint32_t)D * 32 * 2;
     constexpr uint32_t P_BYTES = 128u * kChunk * 2;
     constexpr uint32_t IDESC_QK = umma_idesc_f16(128, 32), IDESC_PV = umma_idesc_f16(128, D) | kUmmaBMnMajor;
 
@@ -130,14 +145,15 @@ decode_umma_kernel(Params P) {
     auto bar = [&](int kind, int b) { return bars + 8 * (kind + b); };
     const uint32_t tmem_slot = s0 + L.misc;
     volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + L.misc + 4);
-    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [2][32]
-    float *vsc = ksc + 2 * kChunk;                                       // [2][32]
+    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [2][32] K scales x scale x log2(e)
+    float *vwc = ksc + 2 * kChunk;                                       // [2][32] V scales x 2^(131 - E)
+    int *ecc = reinterpret_cast<int *>(vwc + 2 * kChunk);                // [2] E
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
-    uint8_t *sQ = smem + L.ops, *sK0 = sQ + Q_BYTES, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
-    const uint32_t aQ = s0 + L.ops, aK0 = aQ + Q_BYTES, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
+    uint8_t *sK0 = smem + L.ops, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
+    const uint32_t aK0 = s0 + L.ops, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
     const uint32_t ring = s0 + L.ring;
     const uint64_t policy = l2_policy_evict_first();
-    const int nquad = min(4, (w.nh + 15) / 16);         // quadrants that hold a real head
+    const int nquad = min(4, (w.nh + 15) / 16);         // softmax warps that hold a real head
     const int nch = (w.len + kChunk - 1) / kChunk;
 
     if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
@@ -154,6 +170,7 @@ decode_umma_kernel(Params P) {
             mbar_init(bar(kBarSFree, b), 32 * nquad);
             mbar_init(bar(kBarPReady, b), 32 * nquad);
         }
+        mbar_init(bar(kBarQReady, 0), 128);
         *abort = 0u;
         fence_mbar_init();
     }
@@ -161,17 +178,8 @@ decode_umma_kernel(Params P) {
     // async proxy) before the barrier that precedes the first bulk copy
     if (P.nk) append_tokens<D>(P, w);
     load_table(P, w, const_cast<uint32_t *>(table));
-    for (int i = tid; i < 2 * 128 * kChunk / 8; i += kUmmaThreads)    // P rows of heads that do not exist stay 0
+    for (int i = tid; i < 2 * (int)P_BYTES / 16; i += kUmmaThreads)    // P rows of heads that do not exist stay 0
         reinterpret_cast<uint4 *>(sP0)[i] = make_uint4(0u, 0u, 0u, 0u);
-
-    // softmax threads: this thread's M row (virtual head hl, hi or lo part)
-    const int hl = 16 * (warp & 3) + (lane & 15);
-    const bool row_ok = warp < 4 && hl < w.nh;
-    const int vh = w.h0 + hl;
-    const bool lo_part = lane >= 16;
-    const int half = lo_part ? 16 : 0;
-    const int len_row = row_ok ? row_len(P, w, vh) : 0;
-    const int row = 32 * (warp & 3) + lane, row_hi = 32 * (warp & 3) + (lane & 15), row_lo = row_hi + 16;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();                                  // barriers initialised, TMEM allocated
@@ -179,43 +187,19 @@ decode_umma_kernel(Params P) {
     const uint32_t tmem = *reinterpret_cast<const volatile uint32_t *>(smem + L.misc);
     const uint32_t tO = tmem + 64;
     const uint32_t tQ = tO + D;                       // the Q tile: D / 2 columns
-    float qk2 = 0.0f;
-    if (warp < 4) {
-        // Q row: q * 2^-eq as hi (or lo) f16, two per column of this thread's TMEM lane
-        const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
-        float mx = 0.0f;
-        for (int c = 0; c < D / 4; ++c) {
-            const float4 v = row_ok ? __ldg(qv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-        const int eq = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
-        const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
-        qk2 = P.scale_log2 * __uint_as_float((uint32_t)(127 + min(eq, 127)) << 23);
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-            float words[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {                 // words c0 + j .. + 3: elements 2(c0 + j) .. + 7
-                const int e4 = (2 * (c0 + j)) / 4;
-                const float4 a = row_ok ? __ldg(qv + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float4 b = row_ok ? __ldg(qv + e4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                uint32_t h[4], l[4];
-                split_f16x2(a.x * down, a.y * down, h[0], l[0]);
-                split_f16x2(a.z * down, a.w * down, h[1], l[1]);
-                split_f16x2(b.x * down, b.y * down, h[2], l[2]);
-                split_f16x2(b.z * down, b.w * down, h[3], l[3]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) words[j + u] = __uint_as_float(lo_part ? l[u] : h[u]);
-            }
-            tmem_st32(tQ + lane_base + c0, words);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();                                  // the Q tile is in TMEM
-    tc_fence_after();
+
+    // softmax threads: virtual head hl (M row) and token half of each chunk
+    const int hl = 16 * (warp & 3) + (lane & 15);
+    const int half = lane >> 4;
+    const bool row_ok = warp < 4 && hl < w.nh;
+    const int vh = w.h0 + hl;
+    const int len_row = row_ok ? row_len(P, w, vh) : 0;
+    const uint32_t lane_hi = (uint32_t)(32 * (warp & 3)) << 16;        // the quadrant's hi rows
+    const uint32_t lane_lo = (uint32_t)(32 * (warp & 3) + 16) << 16;   // and its lo rows
 
     // softmax state (warps 0-3) and the issuer's commit record (warp 7, lane 0)
-    float m = -INFINITY, lsum = 0.0f;
+    float m = -INFINITY, qk2 = 1.0f;   // qk2: the row's 2^eq
+    float2 lsum = make_float2(0.0f, 0.0f);
     int E = 12;
     int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
     uint32_t last_parity = 0;
@@ -240,6 +224,7 @@ decode_umma_kernel(Params P) {
         int nq = 0, np = 0;                                   // next QK / PV to issue
         uint64_t idle_since = 0;
         uint32_t polls = 0;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQReady, 0), 0, abort))) np = nch;
         while (np < nch) {
             int act = 0;
             if (lane == 0) {
@@ -274,13 +259,13 @@ decode_umma_kernel(Params P) {
             }
             act = __shfl_sync(0xFFFFFFFFu, act, 0);
             if (act & 4) break;
-            if (lane == 0 && (act & 1)) {                        // S = Q . K(nq)^T
+            if (lane == 0 && (act & 1)) {                        // S = Q . K(nq)^T, Q from TMEM
                 tc_fence_after();
                 const int b = nq & 1;
                 const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, D * 16), IDESC_QK, ks > 0);
+                    umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, 16 * D), IDESC_QK, ks > 0);
                 umma_commit(bar(kBarQk, b));
                 last_commit = kBarQk + b;
                 last_parity = (nq >> 1) & 1;
@@ -290,10 +275,12 @@ decode_umma_kernel(Params P) {
                 const int bj = np & 1;
                 const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
                 // V tile: token rows of D dims = the MN-major B layout, 8-token
-                // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart
-                umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, D * 16, 128), IDESC_PV, np > 0);
-                umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 2 * D * 16, D * 16, 128),
-                         IDESC_PV, true);
+                // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart;
+                // k-steps 0, 1: tokens 0-15, 16-31
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks)
+                    umma_f16(tO, umma_smem_desc(aP + ks * 256, 128, 512),
+                             umma_smem_desc(aV + ks * 2 * D * 16, D * 16, 128), IDESC_PV, np > 0 || ks > 0);
                 umma_commit(bar(kBarPv, bj));
                 last_commit = kBarPv + bj;
                 last_parity = (np >> 1) & 1;
@@ -306,15 +293,19 @@ decode_umma_kernel(Params P) {
         // ---- conversion (kUmmaConvThreads threads)
         const int ct = tid - 128;
         static_assert(kUmmaConvThreads % kChunk == 0, "conversion threads: whole warps per token lane");
+        static_assert(kUmmaConvThreads >= 2 * kChunk, "one thread per K scale and per V scale");
         constexpr int kConvColStep = kUmmaConvThreads / kChunk;
         const int tok = ct % kChunk, col0 = ct / kChunk;
         const F16Consts fk;
+        int Ew = 12;                                           // weight-scale exponent (warp 5)
         for (int i = 0; i < nch; ++i) {
             const int b = i & 1, k = i % RING;
             const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
             const uint32_t *rawV = rawK + kChunk * W;
-            if (!mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort)) break;
-            if (i >= 2 && !mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)) break;   // K tile free
+            // every wait's outcome is made warp-uniform: warp 5 reduces over its lanes
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort))) break;
+            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)))
+                break;                                        // K tile free
             uint8_t *dK = sK0 + b * K_BYTES;
             // element u = ct + kUmmaConvThreads * k of the [8-code column][token]
             // walk: lane = token (8 bank groups); the thread count is a multiple
@@ -331,13 +322,24 @@ decode_umma_kernel(Params P) {
                 }
             }
             // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
-            if (i >= 2 && !mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)) break;
-            if (ct < kChunk) ksc[b * kChunk + ct] = __uint_as_float(rawK[ct * W + D / 4]);
-            else if (ct < 2 * kChunk) vsc[b * kChunk + ct - kChunk] = __uint_as_float(rawV[(ct - kChunk) * W + D / 4]);
+            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)))
+                break;
+            const int tk = i * kChunk;                          // partition-relative first token
+            if (ct < kChunk) {                                  // K scale x scale x log2(e)
+                ksc[b * kChunk + ct] = tk + ct < w.len ? __uint_as_float(rawK[ct * W + D / 4]) * P.scale_log2 : 0.0f;
+            } else if (ct < 2 * kChunk) {                       // one whole warp: the V scales
+                const int t = ct - kChunk;
+                const float vs = tk + t < w.len ? __uint_as_float(rawV[t * W + D / 4]) : 0.0f;
+                const int ev = (int)(__float_as_uint(fmaxf(vs, 0.0f)) >> 23);
+                Ew = max(Ew, (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)ev));
+                vwc[b * kChunk + t] = vs * __uint_as_float((uint32_t)(kVScaleBias + 127 - Ew) << 23);
+                if (t == 0) ecc[b] = Ew;
+            }
             fence_proxy_async_smem();
             mbar_arrive(bar(kBarKReady, b));
             // V tile b free: PV(i-2) done
-            if (i >= 2 && !mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)) break;
+            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
+                break;
             uint8_t *dV = sV0 + b * V_BYTES;
             {                                                 // as K: the PV B operand is MN-major
                 const uint32_t *src = rawV + tok * W;
@@ -353,138 +355,207 @@ decode_umma_kernel(Params P) {
             mbar_arrive(bar(kBarVReady, b));
             mbar_arrive(bar(kBarSlotFree, k));                // raw slot k read for the last time
         }
-    } else if (warp < nquad) {
-        // ---- softmax (quadrant warp)
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        float wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
-        // chunks below every row's length in this warp need no masking (0 when a
-        // lane holds no head: that warp always masks)
-        const int len_full = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)(row_ok ? len_row : 0));
-        bool ok = true;
-        for (int i = 0; ok && i < nch; ++i) {
-            const int b = i & 1;
-            ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
-            ok = ok && mbar_wait_abortable(bar(kBarKReady, b), (i >> 1) & 1, abort);   // the scale table
-            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-            tc_fence_after();
-            float sv[32], z[16];
-            tmem_ld32(tmem + 32 * b + lane_off, sv);      // TMEM addresses are warp-uniform
+    } else {
+        // ---- softmax warps: the Q tile first (all four warps; rows of heads
+        // that do not exist are written as zeros).  Thread t covers, in each
+        // 64-element block k of its head's q, elements 64k + 32 (t / 16) ..
+        // + 31: TMEM words 32k + 16 (t / 16) .. + 15 of the head's hi row and
+        // of its lo row (16x32bx2 stores at lane bases 32q and 32q + 16).
+        {
+            constexpr int NBLK = D / 64;                  // 64-element blocks (head size 64: one)
+            const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D) +
+                               8 * half;
+            // all of this thread's D / 2 elements in flight at once for the row
+            // maximum, then block by block again (from L1) for the split
+            float mx = 0.0f;
+            {
+                float4 v[8 * NBLK];
+#pragma unroll
+                for (int k = 0; k < NBLK; ++k)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[8 * k + u] = row_ok ? __ldg(qv + 16 * k + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 8 * NBLK; ++c)
+                    mx = max3f(mx, fmaxf(fabsf(v[c].x), fabsf(v[c].y)), fmaxf(fabsf(v[c].z), fabsf(v[c].w)));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+            // q scaled by 2^-eq, eq the row's largest exponent kept within the
+            // normal range, so the f16 parts keep their bits; logits are
+            // (q 2^-eq . k) (k scale x scale x log2 e) x 2^eq
+            const int eq = mx > 0.0f ? max(-126, min(126, (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127)) : 0;
+            const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
+            qk2 = __uint_as_float((uint32_t)(127 + eq) << 23);                    // 2^eq > 0
+#pragma unroll 1
+            for (int k = 0; k < NBLK; ++k) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = row_ok ? __ldg(qv + 16 * k + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float hw[16], lw[16];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 a = v[u];
+                    uint32_t h0, l0, h1, l1;
+                    split_f16x2_fma(a.x * down, a.y * down, h0, l0);
+                    split_f16x2_fma(a.z * down, a.w * down, h1, l1);
+                    hw[2 * u] = __uint_as_float(h0); hw[2 * u + 1] = __uint_as_float(h1);
+                    lw[2 * u] = __uint_as_float(l0); lw[2 * u + 1] = __uint_as_float(l1);
+                }
+                tmem_st16x2(tQ + lane_hi + 32 * k, hw);
+                tmem_st16x2(tQ + lane_lo + 32 * k, lw);
+            }
             tc_fence_before();
-            mbar_arrive(bar(kBarSFree, b));
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {                // own half + the partner's row at those tokens
-                const float mine = lo_part ? sv[16 + j] : sv[j], send = lo_part ? sv[j] : sv[16 + j];
-                z[j] = mine + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-            }
-            // this thread's 16 token scales, as 16-byte vectors
-            float ks[16], vs[16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 a = reinterpret_cast<const float4 *>(ksc + b * kChunk + half)[q4];
-                const float4 c = reinterpret_cast<const float4 *>(vsc + b * kChunk + half)[q4];
-                ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
-                vs[4 * q4] = c.x; vs[4 * q4 + 1] = c.y; vs[4 * q4 + 2] = c.z; vs[4 * q4 + 3] = c.w;
-            }
-            const int t0 = i * kChunk + half;
-            float cmax = -INFINITY, vmax = 0.0f;
-            if ((i + 1) * kChunk <= len_full) {                 // warp-uniform: every row sees the whole chunk
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    z[j] = z[j] * ks[j] * qk2;
-                    cmax = fmaxf(cmax, z[j]);
-                    vmax = fmaxf(vmax, vs[j]);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const bool valid = t0 + j < len_row;
-                    z[j] = valid ? z[j] * ks[j] * qk2 : -INFINITY;
-                    vs[j] = valid ? vs[j] : 0.0f;
-                    cmax = fmaxf(cmax, z[j]);
-                    vmax = fmaxf(vmax, vs[j]);
-                }
-            }
-            cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 16));
-            const int Ec = (int)(__float_as_uint(vmax) >> 23);
-            const bool need = cmax > m + (float)kLazy || Ec > E;
-            float fa = 1.0f;
-            if (need) {
-                const float m_new = fmaxf(m, cmax);
-                const int E_new = max(E, Ec);
-                const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
-                const float ea = (E - E_new < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - E_new) << 23);
-                fa = alpha * ea;
-                lsum *= alpha;
-                m = m_new;
-                E = E_new;
-                wscale = __uint_as_float((uint32_t)(kVScaleBias + 127 - E) << 23);
-            }
-            if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {      // O rows once PV(i-1) is done
-                ok = mbar_wait_abortable(bar(kBarPv, (i - 1) & 1), ((i - 1) >> 1) & 1, abort);
+            mbar_arrive(bar(kBarQReady, 0));
+        }
+        if (warp < nquad) {
+            // ---- softmax (this warp's 16 virtual heads)
+            // chunks below every row's length in this warp need no masking (0 when a
+            // lane holds no head: that warp always masks)
+            const int len_full = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)(row_ok ? len_row : 0));
+            bool ok = true;
+            for (int i = 0; ok && i < nch; ++i) {
+                const int b = i & 1;
+                ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
+                ok = ok && mbar_wait_abortable(bar(kBarKReady, b), (i >> 1) & 1, abort);   // the scale table
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 tc_fence_after();
+                float zh[16], zl[16];                            // this head's hi and lo rows, 16 tokens
+                tmem_ld16x2(tmem + 32 * b + lane_hi, zh);
+                tmem_ld16x2(tmem + 32 * b + lane_lo, zl);
+                tc_fence_before();
+                mbar_arrive(bar(kBarSFree, b));
+                float ks[16], vw[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 a = reinterpret_cast<const float4 *>(ksc + b * kChunk + 16 * half)[q4];
+                    const float4 c = reinterpret_cast<const float4 *>(vwc + b * kChunk + 16 * half)[q4];
+                    ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
+                    vw[4 * q4] = c.x; vw[4 * q4 + 1] = c.y; vw[4 * q4 + 2] = c.z; vw[4 * q4 + 3] = c.w;
+                }
+                const int Ei = ecc[b];
+                float2 t2[8];                                    // z x k scale x scale x log2 e; -inf where masked
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    t2[u] = mul_f2(add_f2(make_float2(zh[2 * u], zh[2 * u + 1]), make_float2(zl[2 * u], zl[2 * u + 1])),
+                                   make_float2(ks[2 * u], ks[2 * u + 1]));
+                if ((i + 1) * kChunk > len_full) {               // warp-uniform: some row ends in this chunk
+                    const int t0 = i * kChunk + 16 * half;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (t0 + 2 * u >= len_row) t2[u].x = -INFINITY;
+                        if (t0 + 2 * u + 1 >= len_row) t2[u].y = -INFINITY;
+                    }
+                }
+                float cmax = max3f(t2[0].x, t2[0].y, t2[1].x);
+                cmax = max3f(cmax, t2[1].y, t2[2].x);
+                cmax = max3f(cmax, t2[2].y, t2[3].x);
+                cmax = max3f(cmax, t2[3].y, t2[4].x);
+                cmax = max3f(cmax, t2[4].y, t2[5].x);
+                cmax = max3f(cmax, t2[5].y, t2[6].x);
+                cmax = max3f(cmax, t2[6].y, t2[7].x);
+                cmax = fmaxf(cmax, t2[7].y);
+                cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));   // the head's other 16 tokens
+                const float cm = cmax * qk2;                     // qk2 = 2^eq > 0: the max of the logits
+                // the same decision in both threads of a head (same cm, m, E)
+                const bool need = cm > m + (float)kLazy || Ei > E;
+                float fa = 1.0f;
+                if (need) {
+                    const float m_new = fmaxf(m, cm);
+                    const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+                    const float ea = (E - Ei < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - Ei) << 23);
+                    fa = alpha * ea;
+                    lsum.x *= alpha;
+                    lsum.y *= alpha;
+                    m = m_new;
+                    E = Ei;
+                }
+                if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {      // O rows once PV(i-1) is done
+                    ok = mbar_wait_abortable(bar(kBarPv, (i - 1) & 1), ((i - 1) >> 1) & 1, abort);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tO + lane_off + 32 * c, o);
+                    for (int c = 0; c < D / 16; ++c) {                // hi rows, then lo rows
+                        const uint32_t a = tO + (c & 1 ? lane_lo : lane_hi) + 32 * (c >> 1);
+                        float o[16];
+                        tmem_ld16x2(a, o);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= fa;
-                    tmem_st32(tO + lane_off + 32 * c, o);
+                        for (int j = 0; j < 16; ++j) o[j] *= fa;
+                        tmem_st16x2(a, o);
+                    }
                 }
-            }
-            if (i >= 2) {                                       // P tile b free: PV(i-2) done
-                ok = mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort);
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-            }
-            const float m_ref = m == -INFINITY ? 0.0f : m;
-            uint8_t *dP = sP0 + b * P_BYTES;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {                 // tokens half + 8c .. +7, both rows of the head
-                uint32_t ph[4], pl[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 8 * c + 2 * e;
-                    const float p0 = fast_exp2(z[j] - m_ref), p1 = fast_exp2(z[j + 1] - m_ref);
-                    lsum += p0 + p1;
-                    split_f16x2(p0 * vs[j] * wscale, p1 * vs[j + 1] * wscale, ph[e], pl[e]);
+                if (i >= 2) {                                       // P tile b free: PV(i-2) done
+                    ok = mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 }
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_hi, half + 8 * c, kChunk)) =
+                const float m_ref = m == -INFINITY ? 0.0f : m;
+                const float2 q2 = make_float2(qk2, qk2), nm2 = make_float2(-m_ref, -m_ref);
+                uint32_t ph[8], pl[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float2 a = fma_f2(t2[u], q2, nm2);        // masked tokens: 2^-inf = 0
+                    const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                    lsum = add_f2(lsum, p);
+                    const float2 pw = mul_f2(p, make_float2(vw[2 * u], vw[2 * u + 1]));
+                    split_f16x2_fma(pw.x, pw.y, ph[u], pl[u]);
+                }
+                // P rows of this head: hi (32q + j) and lo (32q + 16 + j), tokens 16 half ..
+                uint8_t *dP = sP0 + b * P_BYTES;
+                const int row_h = 32 * (warp & 3) + (lane & 15), row_l = row_h + 16;
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_h, 16 * half, kChunk)) =
                     make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_lo, half + 8 * c, kChunk)) =
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_h, 16 * half + 8, kChunk)) =
+                    make_uint4(ph[4], ph[5], ph[6], ph[7]);
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_l, 16 * half, kChunk)) =
                     make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_l, 16 * half + 8, kChunk)) =
+                    make_uint4(pl[4], pl[5], pl[6], pl[7]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(kBarPReady, b));
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(kBarPReady, b));
-        }
-        // the last PV, then this warp's O rows (hi + lo) into the merge scratch
-        if (ok && nch > 0) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) & 1), ((nch - 1) >> 1) & 1, abort);
-        if (__all_sync(0xFFFFFFFFu, ok)) {
-            tc_fence_after();
-            float *ml = reinterpret_cast<float *>(sQ);                  // [64][3]   (operand tiles are free)
-            float *accs = ml + kUmmaHeads * 3;                          // [64][D]
-            // every PV has completed: no MMA reads the Q tile any more
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(tO + lane_off + 32 * c, o);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] += __shfl_xor_sync(0xFFFFFFFFu, o[j], 16);
-                if (!lo_part) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) accs[hl * D + 32 * c + j] = o[j];
+            // the last PV, then this thread's half of its head's output row (hi +
+            // lo rows of O), normalised (one partition) or as the partition's
+            // record (m, l and the unnormalised row in the V scales' units)
+            if (ok) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) & 1), ((nch - 1) >> 1) & 1, abort);
+            if (__all_sync(0xFFFFFFFFu, ok)) {
+                tc_fence_after();
+                const float l_half = lsum.x + lsum.y;
+                const float l_row = l_half + __shfl_xor_sync(0xFFFFFFFFu, l_half, 16);
+                const float fE = m == -INFINITY ? 0.0f : ldexpf(1.0f, E - kVScaleBias);   // O = 2^(131-E) sum p v
+                float f = fE;
+                float *dst = nullptr;
+                if (row_ok) {
+                    const int64_t qr = qrow(P, w, vh);
+                    if (w.single) {
+                        // a query row that sees no token (l = 0) gets a zero row
+                        f = l_row > 0.0f ? fE / l_row : 0.0f;
+                        dst = P.out + qr * D;
+                    } else {
+                        dst = P.part + (qr * P.NP + w.p) * (D + 4);
+                        if (half == 0) {
+                            dst[D] = m;
+                            dst[D + 1] = l_row;
+                        }
+                    }
                 }
+                for (int c = 0; c < D / 32; ++c) {
+                    float oh[16], ol[16];
+                    tmem_ld16x2(tO + lane_hi + 32 * c, oh);
+                    tmem_ld16x2(tO + lane_lo + 32 * c, ol);
+                    if (dst) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * c + 16 * half);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_float4((oh[4 * j] + ol[4 * j]) * f, (oh[4 * j + 1] + ol[4 * j + 1]) * f,
+                                                (oh[4 * j + 2] + ol[4 * j + 2]) * f, (oh[4 * j + 3] + ol[4 * j + 3]) * f);
+                    }
+                }
+            } else {
+                *abort = 1u;
             }
-            const float l_row = lsum + __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
-            if (!lo_part) {
-                ml[hl * 3] = m;
-                ml[hl * 3 + 1] = l_row;
-                ml[hl * 3 + 2] = (float)E;
-            }
-        } else {
-            *abort = 1u;
         }
     }
+    tc_fence_before();
     __syncthreads();
     const bool failed = *abort != 0u;
     if (failed && warp == kUmmaIssueWarp && lane == 0) {
@@ -505,9 +576,9 @@ decode_umma_kernel(Params P) {
         if (tid == 0) flag_error(P.status, kDevWaitTimeout);
         return;
     }
-    float *ml = reinterpret_cast<float *>(sQ);
-    float *accs = ml + kUmmaHeads * 3;
-    merge_and_store<D, true>(P, w, ml, accs, 1, kUmmaHeads, accs + kUmmaHeads * D);
+    // split context: the records are out; the last CTA of the group merges
+    // them, with the operand tiles and the (drained) ring as scratch
+    if (!w.single) arrive_and_combine<D, true>(P, w, sK0);
 }
 
 template <int D>

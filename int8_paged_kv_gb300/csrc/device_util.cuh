@@ -248,6 +248,87 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32]) {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 consecutive 32-bit columns of 16 TMEM lanes, split across the warp
+// (shape 16x32bx2, half-split offset 16): threads t < 16 read lane
+// base + t at columns addr .. addr + 15, threads t >= 16 read lane
+// base + t - 16 at columns addr + 16 .. addr + 31.  An M = 64 accumulator
+// keeps its rows in lanes 0-15 of each warp's 32, so this gives the two
+// halves of a row's 32 columns to threads t and t + 16.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t addr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// The store of the same shape; waits until the columns are written.
+__device__ __forceinline__ void tmem_st16x2(uint32_t addr, const float (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(addr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                    "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                    "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+                    "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                    "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+                    "r"(__float_as_uint(v[15]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------- paired f32 arithmetic
+// One instruction for two f32 lanes (round to nearest even, no flush), the
+// same results as two scalar operations.
+
+__device__ __forceinline__ unsigned long long f2_bits(float2 a) {
+    return (unsigned long long)__float_as_uint(a.x) | ((unsigned long long)__float_as_uint(a.y) << 32);
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long b) {
+    return make_float2(__uint_as_float((uint32_t)b), __uint_as_float((uint32_t)(b >> 32)));
+}
+__device__ __forceinline__ float2 mul_f2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return bits_f2(d);
+}
+__device__ __forceinline__ float2 fma_f2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return bits_f2(d);
+}
+__device__ __forceinline__ float2 add_f2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return bits_f2(d);
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a, b) as f16x2 hi = rn(a, b) and lo = rn(a - hi.x, b - hi.y): the
+// residual of each lane is one f32 fma with an f16 operand (hi * -1 + x,
+// exact: hi is x rounded to f16), so the pair costs four instructions.
+__device__ __forceinline__ void split_f16x2_fma(float a, float b, uint32_t &hi, uint32_t &lo) {
+    asm("{\n\t.reg .b16 h0, h1, m1;\n\t.reg .f32 r0, r1;\n\t"
+        "cvt.rn.f16x2.f32 %0, %3, %2;\n\t"
+        "mov.b32 {h0, h1}, %0;\n\t"
+        "mov.b16 m1, 0xBC00;\n\t"
+        "fma.rn.f32.f16 r0, h0, m1, %2;\n\t"
+        "fma.rn.f32.f16 r1, h1, m1, %3;\n\t"
+        "cvt.rn.f16x2.f32 %1, r1, r0;\n\t}"
+        : "=r"(hi), "=r"(lo)
+        : "f"(a), "f"(b));
+}
+
 // ----------------------------------------------- programmatic dependent launch
 
 // Block until the grid this one depends on (launched before it on the
