@@ -35,19 +35,21 @@ namespace {
 //    online softmax with a lazy reference max (O rows rescaled in TMEM only
 //    when it moves past 2^kLazy, or the weight scale changes) -> P half-rows
 //    as hi and lo f16.  The per-logit arithmetic runs on f32 pairs.
-//  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
+//  - warps 4-7, conversion: per chunk the raw codes (bulk-copied ring, as in
 //    the other families) become f16 K and V tiles [32 tokens][D] in the
-//    core-matrix layout (K-major for QK's B, MN-major for PV's B), and the
-//    chunk's scale table: the K scales, the V scales times the weight scale
-//    2^(131 - E) (E the largest V-scale exponent of the partition so far),
-//    and E; tokens past the partition get scale 0.
-//  - warp 7: its lane 0 issues S = Q.K^T and O += P.V, each as soon as its
+//    core-matrix layout (K-major for QK's B, MN-major for PV's B).  Warps 4-5
+//    convert K and write the chunk's scale table: the K scales, the V scales
+//    times the weight scale 2^(131 - E) (E the largest V-scale exponent of
+//    the partition so far), and E; tokens past the partition get scale 0.
+//    Warps 6-7 convert V.  So a K tile never waits behind the V tile of the
+//    chunk before, whose buffer frees only when PV two chunks back is done.
+//  - warp 8: its lane 0 issues S = Q.K^T and O += P.V, each as soon as its
 //    inputs are ready.
-//  - warp 8: refills the raw ring, chunk c into the slot of chunk c - ring
+//  - warp 9: refills the raw ring, chunk c into the slot of chunk c - ring
 //    once the conversion has read that slot (slot_free[slot]).
 // K, V, P and S are double buffered by chunk parity.  Signals per buffer
-// b = chunk & 1: k_ready[b] (96 conversion threads: K tile and scale table
-// written), v_ready[b] (the same threads: V tile written), s_free[b] /
+// b = chunk & 1: k_ready[b] (warps 4-5: K tile and scale table written),
+// v_ready[b] (warps 6-7: V tile written), s_free[b] /
 // p_ready[b] (the active softmax threads), qk[b] / pv[b] (tcgen05.commit),
 // and q_ready once (the 128 softmax threads: Q tile stored).  QK and the
 // softmax wait only for k_ready, so a chunk's logits do not wait for its V
@@ -57,9 +59,10 @@ namespace {
 // saw v_ready(j); slot_free for chunk c + ring needs the refill issued after
 // the wait for chunk c).
 
-// conversion warps (4 measured slower than 3: large R = 8 0.96 against 0.93 ms)
+// conversion warps: half convert K tiles (and write the scale tables), half V
+// tiles, each half at its own pace
 #ifndef PA_Q8_UMMA_CONV_WARPS
-#define PA_Q8_UMMA_CONV_WARPS 3
+#define PA_Q8_UMMA_CONV_WARPS 4
 #endif
 // warps 0-3 softmax, then the conversion warps, the issue warp, the refill warp
 constexpr int kUmmaConvWarps = PA_Q8_UMMA_CONV_WARPS;
@@ -69,6 +72,8 @@ constexpr int kUmmaThreads = 32 * (kUmmaRefillWarp + 1);
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
 constexpr uint32_t kUmmaBMnMajor = 1u << 16;
 constexpr int kUmmaConvThreads = 32 * kUmmaConvWarps;
+constexpr int kUmmaHalfConv = kUmmaConvThreads / 2;      // threads per K or V conversion group
+static_assert(kUmmaConvWarps % 2 == 0, "as many K as V conversion warps");
 // longest suspension of the issue warp on one pending input before it polls
 // the other again (64 and 32 ns measured the same)
 constexpr uint32_t kIssuePollNs = 256;
@@ -165,8 +170,8 @@ decode_umma_kernel(Params P) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarQk, b), 1);
             mbar_init(bar(kBarPv, b), 1);
-            mbar_init(bar(kBarKReady, b), kUmmaConvThreads);
-            mbar_init(bar(kBarVReady, b), kUmmaConvThreads);
+            mbar_init(bar(kBarKReady, b), kUmmaHalfConv);
+            mbar_init(bar(kBarVReady, b), kUmmaHalfConv);
             mbar_init(bar(kBarSFree, b), 32 * nquad);
             mbar_init(bar(kBarPReady, b), 32 * nquad);
         }
@@ -290,70 +295,73 @@ decode_umma_kernel(Params P) {
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ---- conversion (kUmmaConvThreads threads)
-        const int ct = tid - 128;
-        static_assert(kUmmaConvThreads % kChunk == 0, "conversion threads: whole warps per token lane");
-        static_assert(kUmmaConvThreads >= 2 * kChunk, "one thread per K scale and per V scale");
-        constexpr int kConvColStep = kUmmaConvThreads / kChunk;
-        const int tok = ct % kChunk, col0 = ct / kChunk;
+        // ---- conversion: K group (warps 4 .. ) and V group.  A tile is 32
+        // tokens x D / 8 columns of 8 codes; thread g of a group takes token
+        // g % 32 (lane = token: conflict-free reads of the 33-word rows and
+        // 128-byte runs of core-matrix rows) and columns g / 32 + kGW k.
+        const bool kgroup = tid - 128 < kUmmaHalfConv;
+        const int g = (tid - 128) % kUmmaHalfConv;
+        constexpr int kGW = kUmmaHalfConv / 32;                // warps per group
+        constexpr int kCols = D / 8 / kGW;                      // columns per thread and tile
+        static_assert(kCols * kGW * 8 == D, "whole columns per conversion warp");
+        static_assert(kUmmaHalfConv >= 2 * kChunk, "one K-group thread per K scale and per V scale");
+        const int tok = g % kChunk, col0 = g / kChunk;
         const F16Consts fk;
-        int Ew = 12;                                           // weight-scale exponent (warp 5)
+        auto convert_tile = [&](const uint32_t *raw, uint8_t *tile) {
+            const uint32_t *src = raw + tok * W;
+            uint8_t *dst = tile + kmaj_off(tok, 0, D);
+            uint32_t wd[2 * kCols];
+#pragma unroll
+            for (int k = 0; k < kCols; ++k) {
+                const int c8 = col0 + kGW * k;
+                wd[2 * k] = src[2 * c8];
+                wd[2 * k + 1] = src[2 * c8 + 1];
+            }
+#pragma unroll
+            for (int k = 0; k < kCols; ++k) {
+                uint32_t a0, a1, a2, a3;
+                codes4_to_f16x2(wd[2 * k], a0, a1, fk);
+                codes4_to_f16x2(wd[2 * k + 1], a2, a3, fk);
+                *reinterpret_cast<uint4 *>(dst + 128 * (col0 + kGW * k)) = make_uint4(a0, a1, a2, a3);
+            }
+        };
+        int Ew = 12;                                           // weight-scale exponent (K group's second warp)
         for (int i = 0; i < nch; ++i) {
             const int b = i & 1, k = i % RING;
             const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
             const uint32_t *rawV = rawK + kChunk * W;
-            // every wait's outcome is made warp-uniform: warp 5 reduces over its lanes
+            // every wait's outcome is made warp-uniform: a K-group warp reduces over its lanes
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort))) break;
-            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)))
-                break;                                        // K tile free
-            uint8_t *dK = sK0 + b * K_BYTES;
-            // element u = ct + kUmmaConvThreads * k of the [8-code column][token]
-            // walk: lane = token (8 bank groups); the thread count is a multiple
-            // of 32, so this thread's token is fixed and its column steps by
-            // kConvColStep (128 bytes each in the tile)
-            {
-                const uint32_t *src = rawK + tok * W;
-                uint8_t *dst = dK + kmaj_off(tok, 0, D);
-                for (int c8 = col0; c8 < D / 8; c8 += kConvColStep) {
-                    uint32_t a0, a1, a2, a3;
-                    codes4_to_f16x2(src[2 * c8], a0, a1, fk);
-                    codes4_to_f16x2(src[2 * c8 + 1], a2, a3, fk);
-                    *reinterpret_cast<uint4 *>(dst + 128 * c8) = make_uint4(a0, a1, a2, a3);
+            if (kgroup) {
+                if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)))
+                    break;                                    // K tile free
+                convert_tile(rawK, sK0 + b * K_BYTES);
+                // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
+                if (i >= 2 &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)))
+                    break;
+                const int tk = i * kChunk;                      // partition-relative first token
+                if (g < kChunk) {                               // K scale x scale x log2(e)
+                    ksc[b * kChunk + g] = tk + g < w.len ? __uint_as_float(rawK[g * W + D / 4]) * P.scale_log2 : 0.0f;
+                } else if (g < 2 * kChunk) {                    // one whole warp: the V scales
+                    const int t = g - kChunk;
+                    const float vs = tk + t < w.len ? __uint_as_float(rawV[t * W + D / 4]) : 0.0f;
+                    const int ev = (int)(__float_as_uint(fmaxf(vs, 0.0f)) >> 23);
+                    Ew = max(Ew, (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)ev));
+                    vwc[b * kChunk + t] = vs * __uint_as_float((uint32_t)(kVScaleBias + 127 - Ew) << 23);
+                    if (t == 0) ecc[b] = Ew;
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarKReady, b));
+            } else {
+                // V tile b free: PV(i-2) done
+                if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
+                    break;
+                convert_tile(rawV, sV0 + b * V_BYTES);          // as K: the PV B operand is MN-major
+                fence_proxy_async_smem();
+                mbar_arrive(bar(kBarVReady, b));
             }
-            // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
-            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)))
-                break;
-            const int tk = i * kChunk;                          // partition-relative first token
-            if (ct < kChunk) {                                  // K scale x scale x log2(e)
-                ksc[b * kChunk + ct] = tk + ct < w.len ? __uint_as_float(rawK[ct * W + D / 4]) * P.scale_log2 : 0.0f;
-            } else if (ct < 2 * kChunk) {                       // one whole warp: the V scales
-                const int t = ct - kChunk;
-                const float vs = tk + t < w.len ? __uint_as_float(rawV[t * W + D / 4]) : 0.0f;
-                const int ev = (int)(__float_as_uint(fmaxf(vs, 0.0f)) >> 23);
-                Ew = max(Ew, (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)ev));
-                vwc[b * kChunk + t] = vs * __uint_as_float((uint32_t)(kVScaleBias + 127 - Ew) << 23);
-                if (t == 0) ecc[b] = Ew;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarKReady, b));
-            // V tile b free: PV(i-2) done
-            if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
-                break;
-            uint8_t *dV = sV0 + b * V_BYTES;
-            {                                                 // as K: the PV B operand is MN-major
-                const uint32_t *src = rawV + tok * W;
-                uint8_t *dst = dV + kmaj_off(tok, 0, D);
-                for (int c8 = col0; c8 < D / 8; c8 += kConvColStep) {
-                    uint32_t a0, a1, a2, a3;
-                    codes4_to_f16x2(src[2 * c8], a0, a1, fk);
-                    codes4_to_f16x2(src[2 * c8 + 1], a2, a3, fk);
-                    *reinterpret_cast<uint4 *>(dst + 128 * c8) = make_uint4(a0, a1, a2, a3);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kBarVReady, b));
-            mbar_arrive(bar(kBarSlotFree, k));                // raw slot k read for the last time
+            mbar_arrive(bar(kBarSlotFree, k));                // raw slot k read for the last time (by this group)
         }
     } else {
         // ---- softmax warps: the Q tile first (all four warps; rows of heads
