@@ -1,6 +1,8 @@
 // Multi-row decode on 5th-generation tensor cores: decode_umma_kernel
 // (tcgen05.mma, f32 accumulators in TMEM, warp-specialised conversion,
 // softmax and issue roles).
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace pa_q8 {
@@ -35,21 +37,23 @@ namespace {
 //    online softmax with a lazy reference max (O rows rescaled in TMEM only
 //    when it moves past 2^kLazy, or the weight scale changes) -> P half-rows
 //    as hi and lo f16.  The per-logit arithmetic runs on f32 pairs.
-//  - warps 4-7, conversion: per chunk the raw codes (bulk-copied ring, as in
+//  - warps 4-6, conversion: per chunk the raw codes (bulk-copied ring, as in
 //    the other families) become f16 K and V tiles [32 tokens][D] in the
 //    core-matrix layout (K-major for QK's B, MN-major for PV's B).  Warps 4-5
 //    convert K and write the chunk's scale table: the K scales, the V scales
 //    times the weight scale 2^(131 - E) (E the largest V-scale exponent of
 //    the partition so far), and E; tokens past the partition get scale 0.
-//    Warps 6-7 convert V.  So a K tile never waits behind the V tile of the
+//    Warp 6 converts V.  So a K tile never waits behind the V tile of the
 //    chunk before, whose buffer frees only when PV two chunks back is done.
-//  - warp 8: its lane 0 issues S = Q.K^T and O += P.V, each as soon as its
-//    inputs are ready.
+//  - warps 7 and 8: lane 0 of warp 8 issues S = Q.K^T, lane 0 of warp 7
+//    O += P.V, each as soon as its inputs are ready.  A thread's MMAs run
+//    one after another (about 25 ns each at these shapes), so the two
+//    streams from two threads overlap.
 //  - warp 9: refills the raw ring, chunk c into the slot of chunk c - ring
 //    once the conversion has read that slot (slot_free[slot]).
 // K, V, P and S are double buffered by chunk parity.  Signals per buffer
 // b = chunk & 1: k_ready[b] (warps 4-5: K tile and scale table written),
-// v_ready[b] (warps 6-7: V tile written), s_free[b] /
+// v_ready[b] (warp 6: V tile written), s_free[b] /
 // p_ready[b] (the active softmax threads), qk[b] / pv[b] (tcgen05.commit),
 // and q_ready once (the 128 softmax threads: Q tile stored).  QK and the
 // softmax wait only for k_ready, so a chunk's logits do not wait for its V
@@ -59,24 +63,21 @@ namespace {
 // saw v_ready(j); slot_free for chunk c + ring needs the refill issued after
 // the wait for chunk c).
 
-// conversion warps: half convert K tiles (and write the scale tables), half V
-// tiles, each half at its own pace
-#ifndef PA_Q8_UMMA_CONV_WARPS
-#define PA_Q8_UMMA_CONV_WARPS 4
-#endif
-// warps 0-3 softmax, then the conversion warps, the issue warp, the refill warp
-constexpr int kUmmaConvWarps = PA_Q8_UMMA_CONV_WARPS;
-constexpr int kUmmaIssueWarp = 4 + kUmmaConvWarps;
-constexpr int kUmmaRefillWarp = kUmmaIssueWarp + 1;
+// Warp roles: 0-3 softmax, 4-5 K conversion (and the scale tables), 6 V
+// conversion, 7 PV issue, 8 QK issue, 9 ring refill.  Ten warps: two CTAs
+// per SM then put at most five warps on an SM sub-partition, which leaves
+// 96 registers a thread.
+constexpr int kUmmaKConvWarps = 2;                        // one for the K scales, one for the V scales
+constexpr int kUmmaVConvWarps = 1;
+constexpr int kUmmaKConvThreads = 32 * kUmmaKConvWarps;
+constexpr int kUmmaVConvThreads = 32 * kUmmaVConvWarps;
+constexpr int kUmmaConvThreads = kUmmaKConvThreads + kUmmaVConvThreads;
+constexpr int kUmmaPvWarp = 4 + kUmmaKConvWarps + kUmmaVConvWarps;
+constexpr int kUmmaQkWarp = kUmmaPvWarp + 1;
+constexpr int kUmmaRefillWarp = kUmmaQkWarp + 1;
 constexpr int kUmmaThreads = 32 * (kUmmaRefillWarp + 1);
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
 constexpr uint32_t kUmmaBMnMajor = 1u << 16;
-constexpr int kUmmaConvThreads = 32 * kUmmaConvWarps;
-constexpr int kUmmaHalfConv = kUmmaConvThreads / 2;      // threads per K or V conversion group
-static_assert(kUmmaConvWarps % 2 == 0, "as many K as V conversion warps");
-// longest suspension of the issue warp on one pending input before it polls
-// the other again (64 and 32 ns measured the same)
-constexpr uint32_t kIssuePollNs = 256;
 static_assert(kUmmaHeads == 64, "64 virtual heads: hi and lo rows of one M = 128 tile");
 
 template <int D>
@@ -170,8 +171,8 @@ decode_umma_kernel(Params P) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(kBarQk, b), 1);
             mbar_init(bar(kBarPv, b), 1);
-            mbar_init(bar(kBarKReady, b), kUmmaHalfConv);
-            mbar_init(bar(kBarVReady, b), kUmmaHalfConv);
+            mbar_init(bar(kBarKReady, b), kUmmaKConvThreads);
+            mbar_init(bar(kBarVReady, b), kUmmaVConvThreads);
             mbar_init(bar(kBarSFree, b), 32 * nquad);
             mbar_init(bar(kBarPReady, b), 32 * nquad);
         }
@@ -208,7 +209,7 @@ decode_umma_kernel(Params P) {
     int E = 12;
     int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
     uint32_t last_parity = 0;
-    int issued = 0;                  // chunks whose ring copy warp 8 started
+    int issued = 0;                  // chunks whose ring copy the refill warp started
 
     if (warp == kUmmaRefillWarp) {
         // ---- ring refills: the first RING chunks at once, then chunk c into
@@ -220,112 +221,94 @@ decode_umma_kernel(Params P) {
             if (!__all_sync(0xFFFFFFFFu, ok)) break;          // issue_chunk is warp-collective
             issue_chunk<D>(P, w, table, issued, ring + k * L.slot_bytes, ring_bars + 8 * k, policy);
         }
-    } else if (warp == kUmmaIssueWarp) {
-        // ---- MMA issue.  Lane 0 polls the inputs and issues whichever MMA is
-        // ready: QK(nq) once chunk nq's K tile is converted (and S buffer
-        // nq & 1 was read), PV(np) once P(np) is written and V(np) is
-        // converted.  No barrier runs two phases ahead of the poll: each one's
-        // next phase needs an MMA this warp has not issued yet.
-        int nq = 0, np = 0;                                   // next QK / PV to issue
-        uint64_t idle_since = 0;
-        uint32_t polls = 0;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQReady, 0), 0, abort))) np = nch;
-        while (np < nch) {
-            int act = 0;
+    } else if (warp == kUmmaQkWarp || warp == kUmmaPvWarp) {
+        // ---- MMA issue, one warp per stream (a thread's MMAs run one after
+        // the other, so QK and PV from two threads overlap).  Lane 0 waits for
+        // the inputs and issues:
+        //  QK(c) once chunk c's K tile is converted and S buffer c & 1 was read
+        //  PV(c) once P(c) is written and V(c) is converted.
+        // No barrier runs two phases ahead of a wait: each one's next phase
+        // needs an MMA of this stream that is not issued yet.
+        const bool qk = warp == kUmmaQkWarp;
+        bool ok = __all_sync(0xFFFFFFFFu, !qk || mbar_wait_abortable(bar(kBarQReady, 0), 0, abort));
+        for (int c = 0; ok && c < nch; ++c) {
+            const int b = c & 1;
+            const uint32_t par = (c >> 1) & 1;
             if (lane == 0) {
-                if (nq < nch && mbar_try_wait(bar(kBarKReady, nq & 1), (nq >> 1) & 1) &&
-                    (nq < 2 || mbar_try_wait(bar(kBarSFree, nq & 1), ((nq - 2) >> 1) & 1)))
-                    act |= 1;
-                bool p_ok = false;
-                if (np < nq) {
-                    p_ok = mbar_try_wait(bar(kBarPReady, np & 1), (np >> 1) & 1);
-                    if (p_ok && mbar_try_wait(bar(kBarVReady, np & 1), (np >> 1) & 1)) act |= 2;
-                }
-                if (act == 0) {
-                    // nothing ready: suspend briefly on the oldest pending input, then
-                    // poll again; give up after the wait limit or on the CTA's abort
-                    if (np < nq) {
-                        if (p_ok) mbar_try_wait_suspend(bar(kBarVReady, np & 1), (np >> 1) & 1, kIssuePollNs);
-                        else mbar_try_wait_suspend(bar(kBarPReady, np & 1), (np >> 1) & 1, kIssuePollNs);
-                    } else {
-                        mbar_try_wait_suspend(bar(kBarKReady, nq & 1), (nq >> 1) & 1, kIssuePollNs);
-                    }
-                    if (polls++ == 0) idle_since = global_timer_ns();
-                    if ((polls & 15u) == 0) {
-                        if (*abort) act = 4;
-                        else if (global_timer_ns() - idle_since > kWaitLimitNs) {
-                            *abort = 1u;
-                            act = 4;
-                        }
-                    }
+                if (qk) {
+                    ok = mbar_wait_abortable(bar(kBarKReady, b), par, abort) &&
+                         (c < 2 || mbar_wait_abortable(bar(kBarSFree, b), par ^ 1, abort));
                 } else {
-                    polls = 0;
+                    ok = mbar_wait_abortable(bar(kBarPReady, b), par, abort) &&
+                         mbar_wait_abortable(bar(kBarVReady, b), par, abort);
                 }
             }
-            act = __shfl_sync(0xFFFFFFFFu, act, 0);
-            if (act & 4) break;
-            if (lane == 0 && (act & 1)) {                        // S = Q . K(nq)^T, Q from TMEM
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) {
                 tc_fence_after();
-                const int b = nq & 1;
-                const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
+                if (qk) {                                          // S = Q . K(c)^T, Q from TMEM
+                    const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, 16 * D), IDESC_QK, ks > 0);
-                umma_commit(bar(kBarQk, b));
-                last_commit = kBarQk + b;
-                last_parity = (nq >> 1) & 1;
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, 16 * D), IDESC_QK, ks > 0);
+                    umma_commit(bar(kBarQk, b));
+                    last_commit = kBarQk + b;
+                } else {                                           // O += P(c) . V(c)
+                    const uint32_t aP = aP0 + b * P_BYTES, aV = aV0 + b * V_BYTES;
+                    // V tile: token rows of D dims = the MN-major B layout, 8-token
+                    // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart;
+                    // k-steps 0, 1: tokens 0-15, 16-31
+                    umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, D * 16, 128), IDESC_PV, c > 0);
+                    umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 2 * D * 16, D * 16, 128),
+                             IDESC_PV, true);
+                    umma_commit(bar(kBarPv, b));
+                    last_commit = kBarPv + b;
+                }
+                last_parity = par;
             }
-            if (lane == 0 && (act & 2)) {                        // O += P(np) . V(np)
-                tc_fence_after();
-                const int bj = np & 1;
-                const uint32_t aP = aP0 + bj * P_BYTES, aV = aV0 + bj * V_BYTES;
-                // V tile: token rows of D dims = the MN-major B layout, 8-token
-                // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart;
-                // k-steps 0, 1: tokens 0-15, 16-31
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks)
-                    umma_f16(tO, umma_smem_desc(aP + ks * 256, 128, 512),
-                             umma_smem_desc(aV + ks * 2 * D * 16, D * 16, 128), IDESC_PV, np > 0 || ks > 0);
-                umma_commit(bar(kBarPv, bj));
-                last_commit = kBarPv + bj;
-                last_parity = (np >> 1) & 1;
-            }
-            if (act & 2) ++np;
-            if (act & 1) ++nq;
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ---- conversion: K group (warps 4 .. ) and V group.  A tile is 32
-        // tokens x D / 8 columns of 8 codes; thread g of a group takes token
-        // g % 32 (lane = token: conflict-free reads of the 33-word rows and
-        // 128-byte runs of core-matrix rows) and columns g / 32 + kGW k.
-        const bool kgroup = tid - 128 < kUmmaHalfConv;
-        const int g = (tid - 128) % kUmmaHalfConv;
-        constexpr int kGW = kUmmaHalfConv / 32;                // warps per group
-        constexpr int kCols = D / 8 / kGW;                      // columns per thread and tile
-        static_assert(kCols * kGW * 8 == D, "whole columns per conversion warp");
-        static_assert(kUmmaHalfConv >= 2 * kChunk, "one K-group thread per K scale and per V scale");
+        // ---- conversion: K group (warps 4-5) and V group (warp 6).  A tile
+        // is 32 tokens x D / 8 columns of 8 codes; thread g of a group takes
+        // token g % 32 (lane = token: conflict-free reads of the 33-word rows
+        // and 128-byte runs of core-matrix rows) and columns g / 32 + gw k, gw
+        // the group's warps, eight columns' loads in flight at a time.
+        const bool kgroup = warp < 4 + kUmmaKConvWarps;
+        const int g = kgroup ? tid - 128 : tid - 128 - kUmmaKConvThreads;
+        const int gw = kgroup ? kUmmaKConvWarps : kUmmaVConvWarps;
+        static_assert(kUmmaKConvThreads >= 2 * kChunk, "one K-group thread per K scale and per V scale");
+        static_assert((D / 8) % kUmmaKConvWarps == 0 && (D / 8) % kUmmaVConvWarps == 0, "whole columns per warp");
         const int tok = g % kChunk, col0 = g / kChunk;
         const F16Consts fk;
-        auto convert_tile = [&](const uint32_t *raw, uint8_t *tile) {
+        auto convert_tile = [&](auto ncols_c, const uint32_t *raw, uint8_t *tile) {
+            constexpr int ncols = decltype(ncols_c)::value;      // columns per thread and tile
             const uint32_t *src = raw + tok * W;
             uint8_t *dst = tile + kmaj_off(tok, 0, D);
-            uint32_t wd[2 * kCols];
 #pragma unroll
-            for (int k = 0; k < kCols; ++k) {
-                const int c8 = col0 + kGW * k;
-                wd[2 * k] = src[2 * c8];
-                wd[2 * k + 1] = src[2 * c8 + 1];
-            }
+            for (int k0 = 0; k0 < ncols; k0 += 8) {
+                uint32_t wd[16];
 #pragma unroll
-            for (int k = 0; k < kCols; ++k) {
-                uint32_t a0, a1, a2, a3;
-                codes4_to_f16x2(wd[2 * k], a0, a1, fk);
-                codes4_to_f16x2(wd[2 * k + 1], a2, a3, fk);
-                *reinterpret_cast<uint4 *>(dst + 128 * (col0 + kGW * k)) = make_uint4(a0, a1, a2, a3);
+                for (int k = 0; k < 8; ++k) {
+                    const int c8 = col0 + gw * (k0 + k);
+                    if (k0 + k < ncols) {
+                        wd[2 * k] = src[2 * c8];
+                        wd[2 * k + 1] = src[2 * c8 + 1];
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (k0 + k < ncols) {
+                        uint32_t a0, a1, a2, a3;
+                        codes4_to_f16x2(wd[2 * k], a0, a1, fk);
+                        codes4_to_f16x2(wd[2 * k + 1], a2, a3, fk);
+                        *reinterpret_cast<uint4 *>(dst + 128 * (col0 + gw * (k0 + k))) = make_uint4(a0, a1, a2, a3);
+                    }
+                }
             }
         };
-        int Ew = 12;                                           // weight-scale exponent (K group's second warp)
+        int Ew = 12;                                           // weight-scale exponent (second K warp)
         for (int i = 0; i < nch; ++i) {
             const int b = i & 1, k = i % RING;
             const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
@@ -335,7 +318,7 @@ decode_umma_kernel(Params P) {
             if (kgroup) {
                 if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)))
                     break;                                    // K tile free
-                convert_tile(rawK, sK0 + b * K_BYTES);
+                convert_tile(std::integral_constant<int, D / 8 / kUmmaKConvWarps>(), rawK, sK0 + b * K_BYTES);
                 // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
                 if (i >= 2 &&
                     !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)))
@@ -357,7 +340,8 @@ decode_umma_kernel(Params P) {
                 // V tile b free: PV(i-2) done
                 if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
                     break;
-                convert_tile(rawV, sV0 + b * V_BYTES);          // as K: the PV B operand is MN-major
+                // as K: the PV B operand is MN-major
+                convert_tile(std::integral_constant<int, D / 8 / kUmmaVConvWarps>(), rawV, sV0 + b * V_BYTES);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(kBarVReady, b));
             }
@@ -566,7 +550,7 @@ decode_umma_kernel(Params P) {
     tc_fence_before();
     __syncthreads();
     const bool failed = *abort != 0u;
-    if (failed && warp == kUmmaIssueWarp && lane == 0) {
+    if (failed && (warp == kUmmaQkWarp || warp == kUmmaPvWarp) && lane == 0) {
         // stop only after the newest MMA (and so every earlier one) completed
         if (last_commit >= 0) mbar_wait(bars + 8 * last_commit, last_parity);
     }
