@@ -83,7 +83,8 @@ typedef enum pa_q8_status {
 #define PA_Q8_KERNEL_TENSOR_CORE 2   /* mma.sync f16 tiles with hi/lo split operands */
 #define PA_Q8_KERNEL_TCGEN05 3       /* tcgen05.mma, TMEM accumulators: up to 64 (row, head)
                                         pairs per kv head and CTA; automatic when a kv head
-                                        has > 32 pairs (num_rows * num_heads/num_kv_heads)   */
+                                        has >= 24 pairs (num_rows * num_heads/num_kv_heads),
+                                        > 32 at head size 256                              */
 
 typedef struct pa_q8_decode_options {
     int kernel;            /* PA_Q8_KERNEL_*                                           */

@@ -993,10 +993,10 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     // (query row, head) pairs served per kv head: the rows of one sequence
     // share their kv group's K/V read like the heads of a GQA group
     const int r = a.num_rows * (a.num_heads / a.num_kv_heads);
-    // automatic: tcgen05 above 32 (row, head) pairs per kv head (one CTA
-    // serves up to 64; measured faster from 40 pairs on, slower at <= 32);
-    // the mma.sync tensor-core family otherwise
-    a.kernel = requested_kernel != kAuto ? requested_kernel : (r > kUmmaAutoPairs ? kTcgen05 : kTensorCore);
+    // automatic: tcgen05 from umma_auto_pairs (row, head) pairs per kv head
+    // on (one CTA serves up to 64), the mma.sync tensor-core family below
+    a.kernel = requested_kernel != kAuto ? requested_kernel
+                                         : (r >= umma_auto_pairs(a.head_size) ? kTcgen05 : kTensorCore);
     if (a.kernel == kTcgen05) {
         a.heads_per_cta = r < kUmmaHeads ? r : kUmmaHeads;
     } else if (a.kernel == kTensorCore && a.contiguous) {

@@ -68,10 +68,14 @@ constexpr int kChunk = 32;                 // tokens per warp chunk
 constexpr int kLazy = 8;                   // rescale only when a logit passes the reference max by 2^8
 constexpr int kVScaleBias = 131;           // weights carry 2^(131 - E): p * vs * 2^(131-E) < 2^13
 
-// (row, head) pairs one tcgen05 CTA serves; the automatic plan takes tcgen05
-// above kUmmaAutoPairs pairs per kv head
+// (row, head) pairs one tcgen05 CTA serves
 constexpr int kUmmaHeads = 64;
-constexpr int kUmmaAutoPairs = 32;
+// The automatic plan takes tcgen05 from this many (row, head) pairs per kv
+// head on (measured: 24 pairs at head size 128 tcgen05 0.54 against mma.sync
+// 0.69 ms on the 256-sequence batch, level on 8 long contexts; 16 pairs
+// mma.sync 0.39 against 0.53 ms); at head size 256 above 32 (32 MQA rows:
+// 44.7 against 46.4 us).
+__host__ __device__ constexpr int umma_auto_pairs(int head_size) { return head_size == 256 ? 33 : 24; }
 
 #ifndef PA_Q8_TC_SLOTS
 #define PA_Q8_TC_SLOTS 4                   // token-slot warps per head tile

@@ -72,10 +72,13 @@ constexpr int kUmmaVConvWarps = 1;
 constexpr int kUmmaKConvThreads = 32 * kUmmaKConvWarps;
 constexpr int kUmmaVConvThreads = 32 * kUmmaVConvWarps;
 constexpr int kUmmaConvThreads = kUmmaKConvThreads + kUmmaVConvThreads;
-constexpr int kUmmaPvWarp = 4 + kUmmaKConvWarps + kUmmaVConvWarps;
-constexpr int kUmmaQkWarp = kUmmaPvWarp + 1;
-constexpr int kUmmaRefillWarp = kUmmaQkWarp + 1;
+// (Warp w runs on SM sub-partition w % 4; other placements of the K, V and
+// PV warps measured within 1%.)
+constexpr int kUmmaKWarp0 = 4, kUmmaVWarp = 6, kUmmaPvWarp = 7;
+constexpr int kUmmaQkWarp = 8;
+constexpr int kUmmaRefillWarp = 9;
 constexpr int kUmmaThreads = 32 * (kUmmaRefillWarp + 1);
+static_assert(kUmmaKConvWarps == 2 && kUmmaVConvWarps == 1, "the role table above");
 // instruction-descriptor bit: the B operand is MN-major (N contiguous)
 constexpr uint32_t kUmmaBMnMajor = 1u << 16;
 static_assert(kUmmaHeads == 64, "64 virtual heads: hi and lo rows of one M = 128 tile");
@@ -96,15 +99,19 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
 }
 
 // barrier slots (8 bytes each) after the ring's
-enum UmmaBar { kBarQk = 0, kBarPv = 2, kBarVReady = 4, kBarSFree = 6, kBarPReady = 8, kBarKReady = 10,
-               kBarQReady = 12, kBarSlotFree = 13, kUmmaBars = 17 };   // slot_free: one per raw ring slot (ring <= 4)
+// K tiles and scale tables are kept for kKDepth chunks (their signals qk,
+// k_ready and p_ready too), so the K conversion runs up to four chunks ahead
+// of the softmax; S, P and V tiles are double buffered.
+constexpr int kKDepth = 4;      // measured 1-2% faster than 2 deep (large R = 8, 4, long R = 8)
+enum UmmaBar { kBarQk = 0, kBarPv = 4, kBarVReady = 6, kBarSFree = 8, kBarPReady = 10, kBarKReady = 14,
+               kBarQReady = 18, kBarSlotFree = 19, kUmmaBars = 23 };   // slot_free: one per raw ring slot (ring <= 4)
 
 struct UmmaLayout {
     uint32_t misc, scales, table, ops, ring, slot_bytes, total;
 };
 
 // [barriers: ring, kUmmaBars] [TMEM address, abort flag] [scale tables: K
-// 2 x 32, weighted V 2 x 32, E 2] [block table] [operand tiles K x2, V x2,
+// 4 x 32, weighted V 4 x 32, E 4] [block table] [operand tiles K x4, V x2,
 // P x2] [raw chunk ring].  Total at least a 1/(n+1) share of the
 // shared memory, so no more CTAs share an SM than its TMEM serves.
 template <int D>
@@ -115,9 +122,9 @@ __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
     const int pieces = (PT + ptok - 1) / ptok + 1;
     L.misc = (RING + kUmmaBars) * 8;
     L.scales = align_up(L.misc + 8, 16);
-    L.table = L.scales + align_up(2 * 2 * kChunk * 4 + 2 * 4, 16);
+    L.table = L.scales + align_up(kKDepth * (2 * kChunk * 4 + 4), 16);
     L.ops = align_up(L.table + pieces * 4, 128);
-    const uint32_t ops_bytes = 2u * (32u * D * 2 + (uint32_t)D * 32 * 2 + 128u * kChunk * 2);
+    const uint32_t ops_bytes = kKDepth * 32u * D * 2 + 2u * ((uint32_t)D * 32 * 2 + 128u * kChunk * 2);
     L.ring = align_up(L.ops + ops_bytes, 128);
     L.slot_bytes = align_up(2u * kChunk * (D / 4 + 1) * 4, 128);
     L.total = L.ring + RING * L.slot_bytes;
@@ -151,30 +158,67 @@ decode_umma_kernel(Params P) {
     auto bar = [&](int kind, int b) { return bars + 8 * (kind + b); };
     const uint32_t tmem_slot = s0 + L.misc;
     volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + L.misc + 4);
-    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [2][32] K scales x scale x log2(e)
-    float *vwc = ksc + 2 * kChunk;                                       // [2][32] V scales x 2^(131 - E)
-    int *ecc = reinterpret_cast<int *>(vwc + 2 * kChunk);                // [2] E
+    float *ksc = reinterpret_cast<float *>(smem + L.scales);           // [4][32] K scales x scale x log2(e)
+    float *vwc = ksc + kKDepth * kChunk;                                 // [4][32] V scales x 2^(131 - E)
+    int *ecc = reinterpret_cast<int *>(vwc + kKDepth * kChunk);          // [4] E
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
-    uint8_t *sK0 = smem + L.ops, *sV0 = sK0 + 2 * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
-    const uint32_t aK0 = s0 + L.ops, aV0 = aK0 + 2 * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
+    uint8_t *sK0 = smem + L.ops, *sV0 = sK0 + kKDepth * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
+    const uint32_t aK0 = s0 + L.ops, aV0 = aK0 + kKDepth * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
     const uint32_t ring = s0 + L.ring;
     const uint64_t policy = l2_policy_evict_first();
     const int nquad = min(4, (w.nh + 15) / 16);         // softmax warps that hold a real head
     const int nch = (w.len + kChunk - 1) / kChunk;
 
+    // softmax threads: virtual head hl (M row) and token half of each chunk
+    const int hl = 16 * (warp & 3) + (lane & 15);
+    const int half = lane >> 4;
+    const bool row_ok = warp < 4 && hl < w.nh;
+    const int vh = w.h0 + hl;
+    const int len_row = row_ok ? row_len(P, w, vh) : 0;
     if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
+    // Q rows: the softmax warps load their q elements first, so the loads
+    // overlap the setup below.  Thread t covers, in each 64-element block k
+    // of its head's q, elements 64k + 32 (t / 16) .. + 31, which become TMEM
+    // words 32k + 16 (t / 16) .. + 15 of the head's hi row and of its lo row.
+    // The loads here only give each row's largest magnitude.
+    // q is scaled by 2^-eq, eq the row's largest exponent kept within the
+    // normal range, so the f16 parts keep their bits; logits are
+    // (q 2^-eq . k) (k scale x scale x log2 e) x 2^eq.  The blocks are read
+    // again (from L1) for the split once the TMEM is allocated (keeping the
+    // split words in registers instead measured 1-2% slower: 96 registers).
+    constexpr int NBLK = D / 64;                      // 64-element blocks (head size 64: one)
+    const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D) + 8 * half;
+    float qk2 = 1.0f, qdown = 1.0f;                   // the row's 2^eq and 2^-eq
+    if (warp < 4) {
+        float4 v[8 * NBLK];
+#pragma unroll
+        for (int k = 0; k < NBLK; ++k)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[8 * k + u] = row_ok ? __ldg(qv + 16 * k + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mx = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8 * NBLK; ++c)
+            mx = max3f(mx, fmaxf(fabsf(v[c].x), fabsf(v[c].y)), fmaxf(fabsf(v[c].z), fabsf(v[c].w)));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const int eq = mx > 0.0f ? max(-126, min(126, (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127)) : 0;
+        qdown = __uint_as_float((uint32_t)(127 - eq) << 23);
+        qk2 = __uint_as_float((uint32_t)(127 + eq) << 23);
+    }
     if (tid == 0) {
         for (int k = 0; k < RING; ++k) {
             mbar_init(ring_bars + 8 * k, 1);
             mbar_init(bar(kBarSlotFree, k), kUmmaConvThreads);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kKDepth; ++b) {
             mbar_init(bar(kBarQk, b), 1);
-            mbar_init(bar(kBarPv, b), 1);
             mbar_init(bar(kBarKReady, b), kUmmaKConvThreads);
+            mbar_init(bar(kBarPReady, b), 32 * nquad);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarPv, b), 1);
             mbar_init(bar(kBarVReady, b), kUmmaVConvThreads);
             mbar_init(bar(kBarSFree, b), 32 * nquad);
-            mbar_init(bar(kBarPReady, b), 32 * nquad);
         }
         mbar_init(bar(kBarQReady, 0), 128);
         *abort = 0u;
@@ -194,17 +238,11 @@ decode_umma_kernel(Params P) {
     const uint32_t tO = tmem + 64;
     const uint32_t tQ = tO + D;                       // the Q tile: D / 2 columns
 
-    // softmax threads: virtual head hl (M row) and token half of each chunk
-    const int hl = 16 * (warp & 3) + (lane & 15);
-    const int half = lane >> 4;
-    const bool row_ok = warp < 4 && hl < w.nh;
-    const int vh = w.h0 + hl;
-    const int len_row = row_ok ? row_len(P, w, vh) : 0;
     const uint32_t lane_hi = (uint32_t)(32 * (warp & 3)) << 16;        // the quadrant's hi rows
     const uint32_t lane_lo = (uint32_t)(32 * (warp & 3) + 16) << 16;   // and its lo rows
 
-    // softmax state (warps 0-3) and the issuer's commit record (warp 7, lane 0)
-    float m = -INFINITY, qk2 = 1.0f;   // qk2: the row's 2^eq
+    // softmax state (warps 0-3) and the issuers' commit records (lane 0)
+    float m = -INFINITY;
     float2 lsum = make_float2(0.0f, 0.0f);
     int E = 12;
     int last_commit = -1;            // barrier slot address offset of the newest commit, -1 none
@@ -227,19 +265,20 @@ decode_umma_kernel(Params P) {
         // the inputs and issues:
         //  QK(c) once chunk c's K tile is converted and S buffer c & 1 was read
         //  PV(c) once P(c) is written and V(c) is converted.
+        // (b: the double buffers of S, P, V; b4: those of K tiles and tables)
         // No barrier runs two phases ahead of a wait: each one's next phase
         // needs an MMA of this stream that is not issued yet.
         const bool qk = warp == kUmmaQkWarp;
         bool ok = __all_sync(0xFFFFFFFFu, !qk || mbar_wait_abortable(bar(kBarQReady, 0), 0, abort));
         for (int c = 0; ok && c < nch; ++c) {
-            const int b = c & 1;
-            const uint32_t par = (c >> 1) & 1;
+            const int b = c & 1, b4 = c & (kKDepth - 1);
+            const uint32_t par = (c >> 1) & 1, par4 = (c / kKDepth) & 1;
             if (lane == 0) {
                 if (qk) {
-                    ok = mbar_wait_abortable(bar(kBarKReady, b), par, abort) &&
+                    ok = mbar_wait_abortable(bar(kBarKReady, b4), par4, abort) &&
                          (c < 2 || mbar_wait_abortable(bar(kBarSFree, b), par ^ 1, abort));
                 } else {
-                    ok = mbar_wait_abortable(bar(kBarPReady, b), par, abort) &&
+                    ok = mbar_wait_abortable(bar(kBarPReady, b4), par4, abort) &&
                          mbar_wait_abortable(bar(kBarVReady, b), par, abort);
                 }
             }
@@ -248,12 +287,13 @@ decode_umma_kernel(Params P) {
             if (lane == 0) {
                 tc_fence_after();
                 if (qk) {                                          // S = Q . K(c)^T, Q from TMEM
-                    const uint32_t aK = aK0 + b * K_BYTES, tS = tmem + 32 * b;
+                    const uint32_t aK = aK0 + b4 * K_BYTES, tS = tmem + 32 * b;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         umma_f16_ta(tS, tQ + 8 * ks, umma_smem_desc(aK + ks * 256, 128, 16 * D), IDESC_QK, ks > 0);
-                    umma_commit(bar(kBarQk, b));
-                    last_commit = kBarQk + b;
+                    umma_commit(bar(kBarQk, b4));
+                    last_commit = kBarQk + b4;
+                    last_parity = par4;
                 } else {                                           // O += P(c) . V(c)
                     const uint32_t aP = aP0 + b * P_BYTES, aV = aV0 + b * V_BYTES;
                     // V tile: token rows of D dims = the MN-major B layout, 8-token
@@ -264,8 +304,8 @@ decode_umma_kernel(Params P) {
                              IDESC_PV, true);
                     umma_commit(bar(kBarPv, b));
                     last_commit = kBarPv + b;
+                    last_parity = par;
                 }
-                last_parity = par;
             }
         }
         __syncwarp();
@@ -275,8 +315,8 @@ decode_umma_kernel(Params P) {
         // token g % 32 (lane = token: conflict-free reads of the 33-word rows
         // and 128-byte runs of core-matrix rows) and columns g / 32 + gw k, gw
         // the group's warps, eight columns' loads in flight at a time.
-        const bool kgroup = warp < 4 + kUmmaKConvWarps;
-        const int g = kgroup ? tid - 128 : tid - 128 - kUmmaKConvThreads;
+        const bool kgroup = warp >= kUmmaKWarp0 && warp < kUmmaKWarp0 + kUmmaKConvWarps;
+        const int g = kgroup ? tid - 32 * kUmmaKWarp0 : tid - 32 * kUmmaVWarp;
         const int gw = kgroup ? kUmmaKConvWarps : kUmmaVConvWarps;
         static_assert(kUmmaKConvThreads >= 2 * kChunk, "one K-group thread per K scale and per V scale");
         static_assert((D / 8) % kUmmaKConvWarps == 0 && (D / 8) % kUmmaVConvWarps == 0, "whole columns per warp");
@@ -316,26 +356,28 @@ decode_umma_kernel(Params P) {
             // every wait's outcome is made warp-uniform: a K-group warp reduces over its lanes
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_abortable(ring_bars + 8 * k, (i / RING) & 1, abort))) break;
             if (kgroup) {
-                if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b), ((i - 2) >> 1) & 1, abort)))
-                    break;                                    // K tile free
-                convert_tile(std::integral_constant<int, D / 8 / kUmmaKConvWarps>(), rawK, sK0 + b * K_BYTES);
-                // scale table b free: softmax(i-2) wrote P(i-2), after its last read of the table
-                if (i >= 2 &&
-                    !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b), ((i - 2) >> 1) & 1, abort)))
+                const int b4 = i & (kKDepth - 1);
+                const uint32_t prev4 = ((i / kKDepth) & 1) ^ 1;   // the phase of chunk i - kKDepth
+                if (i >= kKDepth && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarQk, b4), prev4, abort)))
+                    break;                                    // K tile free: QK(i - 4) done
+                convert_tile(std::integral_constant<int, D / 8 / kUmmaKConvWarps>(), rawK, sK0 + b4 * K_BYTES);
+                // scale table b4 free: softmax(i-4) wrote P(i-4), after its last read of the table
+                if (i >= kKDepth &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPReady, b4), prev4, abort)))
                     break;
                 const int tk = i * kChunk;                      // partition-relative first token
                 if (g < kChunk) {                               // K scale x scale x log2(e)
-                    ksc[b * kChunk + g] = tk + g < w.len ? __uint_as_float(rawK[g * W + D / 4]) * P.scale_log2 : 0.0f;
+                    ksc[b4 * kChunk + g] = tk + g < w.len ? __uint_as_float(rawK[g * W + D / 4]) * P.scale_log2 : 0.0f;
                 } else if (g < 2 * kChunk) {                    // one whole warp: the V scales
                     const int t = g - kChunk;
                     const float vs = tk + t < w.len ? __uint_as_float(rawV[t * W + D / 4]) : 0.0f;
                     const int ev = (int)(__float_as_uint(fmaxf(vs, 0.0f)) >> 23);
                     Ew = max(Ew, (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)ev));
-                    vwc[b * kChunk + t] = vs * __uint_as_float((uint32_t)(kVScaleBias + 127 - Ew) << 23);
-                    if (t == 0) ecc[b] = Ew;
+                    vwc[b4 * kChunk + t] = vs * __uint_as_float((uint32_t)(kVScaleBias + 127 - Ew) << 23);
+                    if (t == 0) ecc[b4] = Ew;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(bar(kBarKReady, b));
+                mbar_arrive(bar(kBarKReady, b4));
             } else {
                 // V tile b free: PV(i-2) done
                 if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
@@ -349,53 +391,25 @@ decode_umma_kernel(Params P) {
         }
     } else {
         // ---- softmax warps: the Q tile first (all four warps; rows of heads
-        // that do not exist are written as zeros).  Thread t covers, in each
-        // 64-element block k of its head's q, elements 64k + 32 (t / 16) ..
-        // + 31: TMEM words 32k + 16 (t / 16) .. + 15 of the head's hi row and
-        // of its lo row (16x32bx2 stores at lane bases 32q and 32q + 16).
+        // that do not exist are written as zeros), as 16x32bx2 stores at lane
+        // bases 32q (hi rows) and 32q + 16 (lo rows)
         {
-            constexpr int NBLK = D / 64;                  // 64-element blocks (head size 64: one)
-            const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D) +
-                               8 * half;
-            // all of this thread's D / 2 elements in flight at once for the row
-            // maximum, then block by block again (from L1) for the split
-            float mx = 0.0f;
-            {
-                float4 v[8 * NBLK];
-#pragma unroll
-                for (int k = 0; k < NBLK; ++k)
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        v[8 * k + u] = row_ok ? __ldg(qv + 16 * k + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 8 * NBLK; ++c)
-                    mx = max3f(mx, fmaxf(fabsf(v[c].x), fabsf(v[c].y)), fmaxf(fabsf(v[c].z), fabsf(v[c].w)));
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-            // q scaled by 2^-eq, eq the row's largest exponent kept within the
-            // normal range, so the f16 parts keep their bits; logits are
-            // (q 2^-eq . k) (k scale x scale x log2 e) x 2^eq
-            const int eq = mx > 0.0f ? max(-126, min(126, (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127)) : 0;
-            const float down = __uint_as_float((uint32_t)(127 - eq) << 23);      // 2^-eq
-            qk2 = __uint_as_float((uint32_t)(127 + eq) << 23);                    // 2^eq > 0
 #pragma unroll 1
             for (int k = 0; k < NBLK; ++k) {
                 float4 v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) v[u] = row_ok ? __ldg(qv + 16 * k + u) : make_float4(0.f, 0.f, 0.f, 0.f);
-                float hw[16], lw[16];
+                uint32_t hw[16], lw[16];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float4 a = v[u];
-                    uint32_t h0, l0, h1, l1;
-                    split_f16x2_fma(a.x * down, a.y * down, h0, l0);
-                    split_f16x2_fma(a.z * down, a.w * down, h1, l1);
-                    hw[2 * u] = __uint_as_float(h0); hw[2 * u + 1] = __uint_as_float(h1);
-                    lw[2 * u] = __uint_as_float(l0); lw[2 * u + 1] = __uint_as_float(l1);
+                    split_f16x2_fma(a.x * qdown, a.y * qdown, hw[2 * u], lw[2 * u]);
+                    split_f16x2_fma(a.z * qdown, a.w * qdown, hw[2 * u + 1], lw[2 * u + 1]);
                 }
-                tmem_st16x2(tQ + lane_hi + 32 * k, hw);
-                tmem_st16x2(tQ + lane_lo + 32 * k, lw);
+                tmem_st16x2_nowait(tQ + lane_hi + 32 * k, hw);
+                tmem_st16x2_nowait(tQ + lane_lo + 32 * k, lw);
             }
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(kBarQReady, 0));
         }
@@ -404,11 +418,17 @@ decode_umma_kernel(Params P) {
             // chunks below every row's length in this warp need no masking (0 when a
             // lane holds no head: that warp always masks)
             const int len_full = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)(row_ok ? len_row : 0));
+            // this thread's P tile words: its head's hi row (32q + j) and lo row
+            // (32q + 16 + j) at tokens 16 half .. + 7 and + 8 .. + 15
+            const int row_h = 32 * (warp & 3) + (lane & 15), row_l = row_h + 16;
+            const uint32_t p_off[4] = {kmaj_off(row_h, 16 * half, kChunk), kmaj_off(row_h, 16 * half + 8, kChunk),
+                                       kmaj_off(row_l, 16 * half, kChunk), kmaj_off(row_l, 16 * half + 8, kChunk)};
             bool ok = true;
             for (int i = 0; ok && i < nch; ++i) {
-                const int b = i & 1;
-                ok = mbar_wait_abortable(bar(kBarQk, b), (i >> 1) & 1, abort);
-                ok = ok && mbar_wait_abortable(bar(kBarKReady, b), (i >> 1) & 1, abort);   // the scale table
+                const int b = i & 1, b4 = i & (kKDepth - 1);
+                const uint32_t par4 = (i / kKDepth) & 1;
+                ok = mbar_wait_abortable(bar(kBarQk, b4), par4, abort);
+                ok = ok && mbar_wait_abortable(bar(kBarKReady, b4), par4, abort);   // the scale table
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 tc_fence_after();
                 float zh[16], zl[16];                            // this head's hi and lo rows, 16 tokens
@@ -419,12 +439,12 @@ decode_umma_kernel(Params P) {
                 float ks[16], vw[16];
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 a = reinterpret_cast<const float4 *>(ksc + b * kChunk + 16 * half)[q4];
-                    const float4 c = reinterpret_cast<const float4 *>(vwc + b * kChunk + 16 * half)[q4];
+                    const float4 a = reinterpret_cast<const float4 *>(ksc + b4 * kChunk + 16 * half)[q4];
+                    const float4 c = reinterpret_cast<const float4 *>(vwc + b4 * kChunk + 16 * half)[q4];
                     ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
                     vw[4 * q4] = c.x; vw[4 * q4 + 1] = c.y; vw[4 * q4 + 2] = c.z; vw[4 * q4 + 3] = c.w;
                 }
-                const int Ei = ecc[b];
+                const int Ei = ecc[b4];
                 float2 t2[8];                                    // z x k scale x scale x log2 e; -inf where masked
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
@@ -438,14 +458,11 @@ decode_umma_kernel(Params P) {
                         if (t0 + 2 * u + 1 >= len_row) t2[u].y = -INFINITY;
                     }
                 }
-                float cmax = max3f(t2[0].x, t2[0].y, t2[1].x);
-                cmax = max3f(cmax, t2[1].y, t2[2].x);
-                cmax = max3f(cmax, t2[2].y, t2[3].x);
-                cmax = max3f(cmax, t2[3].y, t2[4].x);
-                cmax = max3f(cmax, t2[4].y, t2[5].x);
-                cmax = max3f(cmax, t2[5].y, t2[6].x);
-                cmax = max3f(cmax, t2[6].y, t2[7].x);
-                cmax = fmaxf(cmax, t2[7].y);
+                // a tree of three-input maxima (depth 3)
+                const float c0 = max3f(t2[0].x, t2[0].y, t2[1].x), c1 = max3f(t2[1].y, t2[2].x, t2[2].y);
+                const float c2 = max3f(t2[3].x, t2[3].y, t2[4].x), c3 = max3f(t2[4].y, t2[5].x, t2[5].y);
+                const float c4 = max3f(t2[6].x, t2[6].y, t2[7].x);
+                float cmax = fmaxf(max3f(c0, c1, c2), max3f(c3, c4, t2[7].y));
                 cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));   // the head's other 16 tokens
                 const float cm = cmax * qk2;                     // qk2 = 2^eq > 0: the max of the logits
                 // the same decision in both threads of a head (same cm, m, E)
@@ -482,28 +499,26 @@ decode_umma_kernel(Params P) {
                 const float m_ref = m == -INFINITY ? 0.0f : m;
                 const float2 q2 = make_float2(qk2, qk2), nm2 = make_float2(-m_ref, -m_ref);
                 uint32_t ph[8], pl[8];
+                float2 pp[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float2 a = fma_f2(t2[u], q2, nm2);        // masked tokens: 2^-inf = 0
-                    const float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                    lsum = add_f2(lsum, p);
-                    const float2 pw = mul_f2(p, make_float2(vw[2 * u], vw[2 * u + 1]));
+                    pp[u] = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                    const float2 pw = mul_f2(pp[u], make_float2(vw[2 * u], vw[2 * u + 1]));
                     split_f16x2_fma(pw.x, pw.y, ph[u], pl[u]);
                 }
+                // the chunk's weights summed as a tree, then added to the row's sum
+                lsum = add_f2(lsum, add_f2(add_f2(add_f2(pp[0], pp[1]), add_f2(pp[2], pp[3])),
+                                           add_f2(add_f2(pp[4], pp[5]), add_f2(pp[6], pp[7]))));
                 // P rows of this head: hi (32q + j) and lo (32q + 16 + j), tokens 16 half ..
                 uint8_t *dP = sP0 + b * P_BYTES;
-                const int row_h = 32 * (warp & 3) + (lane & 15), row_l = row_h + 16;
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_h, 16 * half, kChunk)) =
-                    make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_h, 16 * half + 8, kChunk)) =
-                    make_uint4(ph[4], ph[5], ph[6], ph[7]);
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_l, 16 * half, kChunk)) =
-                    make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                *reinterpret_cast<uint4 *>(dP + kmaj_off(row_l, 16 * half + 8, kChunk)) =
-                    make_uint4(pl[4], pl[5], pl[6], pl[7]);
+                *reinterpret_cast<uint4 *>(dP + p_off[0]) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4 *>(dP + p_off[1]) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+                *reinterpret_cast<uint4 *>(dP + p_off[2]) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                *reinterpret_cast<uint4 *>(dP + p_off[3]) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar(kBarPReady, b));
+                mbar_arrive(bar(kBarPReady, b4));
             }
             // the last PV, then this thread's half of its head's output row (hi +
             // lo rows of O), normalised (one partition) or as the partition's

@@ -267,6 +267,17 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t addr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// The store of the same shape, without waiting (tcgen05.wait::st before the
+// columns are used).
+__device__ __forceinline__ void tmem_st16x2_nowait(uint32_t addr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // The store of the same shape; waits until the columns are written.
 __device__ __forceinline__ void tmem_st16x2(uint32_t addr, const float (&v)[16]) {
     asm volatile("tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, "

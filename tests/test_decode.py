@@ -248,7 +248,7 @@ def test_mixed_per_sequence_splits_against_oracle(kernel, pt):
 @pytest.mark.parametrize("R", [2, 5])
 def test_mixed_per_sequence_splits_multi_row(R):
     """The same batch with R causal query rows per sequence on every family
-    (tcgen05 takes R * r > 32 pairs)."""
+    (the automatic plan takes tcgen05 from R * r = 24 pairs on)."""
     from tests.gpu_helpers import (assert_close, device_status, gpu_decode_rows, oracle_decode_rows,
                                    random_case)
     lens = MIXED_LENS

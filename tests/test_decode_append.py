@@ -193,8 +193,8 @@ def test_large_batch_sampled():
 
 @pytest.mark.parametrize("kernel", [3, 0])
 def test_fused_step_on_tcgen05(kernel):
-    """The tcgen05 family (asked for, and chosen automatically above 32 (row,
-    head) pairs per kv head: R = 8 rows x 8 heads) stores the new tokens too."""
+    """The tcgen05 family (asked for, and chosen automatically from 24 (row,
+    head) pairs per kv head on: R = 8 rows x 8 heads) stores the new tokens too."""
     from tests.gpu_helpers import assert_close, dev_u32, device_status, host_u32
     import int8_paged_kv_gb300 as pk
     lens = [129, 1, 0, 700, 64, 2000]

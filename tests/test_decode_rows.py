@@ -138,9 +138,9 @@ def _sampled_rows_oracle(w, ok_, ov_, q, picks):
 @pytest.mark.parametrize("kernel,R", [(0, 4), (TC, 4), (CC, 4), (T5, 4), (0, 5), (0, 8)])
 def test_large_batch_many_rows_sampled(kernel, R):
     """The large-batch workload with 4, 5 or 8 query rows per sequence (the
-    automatic plan takes the two-tile mma.sync kernel at 4 rows x 8 heads and
-    tcgen05 above 32 pairs: 40 pairs in a partly filled CTA, 64 in a full
-    one), sampled (s, b, h) rows against the oracle."""
+    automatic plan takes tcgen05 from 24 pairs on: 32 and 40 pairs in partly
+    filled CTAs, 64 in a full one), sampled (s, b, h) rows against the
+    oracle."""
     from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows
     w, ok_, ov_, kc, vc = _setup("large")
     q = wl.query_rows(w, R)
