@@ -62,8 +62,10 @@ def oracle_decode(w, kc, vc, rows=None, q=None, bt=None, cl=None):
                          scale=w.scale, rows=rows)
 
 
-def random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0):
-    """A poisoned paged cache written by both writers (checked equal)."""
+def random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0, v_token_mult=None):
+    """A poisoned paged cache written by both writers (checked equal).
+    v_token_mult(position, context) -> factor scales each token's V vectors
+    (magnitudes that change along a context)."""
     rng = np.random.default_rng(seed)
     nblk = [-(-int(c) // B) for c in lens]
     Nb = Nb or max(1, max(nblk))
@@ -77,6 +79,10 @@ def random_case(S, H, Hk, D, B, lens, seed, Nb=None, scale_mult=1.0, dist=1.0):
     T = int(sum(lens))
     key = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
     val = (rng.standard_normal((T, Hk, D)) * dist).astype(np.float32)
+    if v_token_mult is not None and T:
+        pos = np.concatenate([np.arange(c) for c in lens if c > 0])
+        ctx = np.concatenate([np.full(c, c) for c in lens if c > 0])
+        val = (val * np.asarray(v_token_mult(pos, ctx), dtype=np.float64)[:, None, None]).astype(np.float32)
     slots = np.concatenate([(bt[s, np.arange(c) // B].astype(np.int64) * B + np.arange(c) % B)
                             for s, c in enumerate(lens) if c > 0] or [np.zeros(0, np.int64)]).astype(np.uint32)
     W = D // 4 + 1

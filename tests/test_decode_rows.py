@@ -171,3 +171,39 @@ def test_tcgen05_single_row_and_wide_groups(H, Hk, D):
         for pt in (0, 256):
             assert_close(gpu_decode_rows(w, kc, vc, q, kernel=T5, partition_tokens=pt), want,
                          f"H {H} Hk {Hk} D {D} R {R} pt {pt}")
+
+
+@pytest.mark.parametrize("kernel", [TC, CC, T5])
+def test_scale_sign_extreme_q_rows_and_growing_v(kernel):
+    """Every family (tcgen05 at 32 pairs per kv head) against the oracle on:
+    a negative, a zero and a large softmax scale; q rows of very different
+    magnitudes in one kv group (1e-40 (subnormal) .. 1e-30, an all-zero row,
+    and up to 8x), each row scaled by its own largest exponent; and V
+    vectors whose magnitude grows 3 decades along each context, so the
+    weight scale's exponent rises chunk by chunk (lazy rescales of O).
+    The case stays well conditioned for f32 arithmetic: logits within a few
+    hundred (beyond that the weights depend on logit differences below
+    f32's resolution of the logits: a q row scaled by 1e15 failed on every
+    family, the CUDA-core f32 one included), and V growth small enough that
+    the weighted sum does not cancel (12 decades of growth, where large
+    terms cancel to small outputs, failed on every family too)."""
+    import dataclasses
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows, oracle_decode_rows, random_case
+    lens = [1, 33, 700, 2049]
+    grow = lambda pos, ctx: 10.0 ** (-2.0 + 3.0 * pos / np.maximum(ctx - 1, 1))
+    w, ok_, ov_, kc, vc = random_case(4, 16, 2, 128, 16, lens, seed=71, v_token_mult=grow)
+    R = 4
+    q = np.random.default_rng(72).standard_normal((4, R, 16, 128))
+    q[:, :, 0] *= 1e-30
+    q[:, :, 1] = 0.0
+    q[:, :, 2] *= 8.0
+    q[:, :, 3] *= 1e-40                      # subnormal in f32
+    q[:, 1, 5] *= 1e-8
+    q = q.astype(np.float32)
+    for mult in (-1.0, 0.0, 3.0):
+        ws = dataclasses.replace(w, scale=float(np.float32(mult / np.sqrt(128))))
+        want = oracle_decode_rows(ws, ok_, ov_, q)
+        for pt in (0, 256):
+            got = gpu_decode_rows(ws, kc, vc, q, kernel=kernel, partition_tokens=pt)
+            assert_close(got, want, f"kernel {kernel} scale x {mult} pt {pt}")
+    assert device_status() == 0
