@@ -29,7 +29,11 @@ namespace {
 // Each softmax thread owns one virtual head and 16 of a chunk's 32 tokens:
 // two 16x32bx2 loads (lane bases 32q and 32q + 16) give thread t the hi and
 // the lo row of head 16q + t % 16 at tokens 16 (t / 16) .. + 15, so a logit
-// is one paired add, with no exchange between threads.
+// is one paired add, with no exchange between threads.  With 32 heads or
+// fewer, quadrants 2-3 hold the Q rows of quadrants 0-1 again (the M = 128
+// MMAs compute them anyway) and take tokens 16-31 of each chunk, quadrants
+// 0-1 tokens 0-15, each thread 8 tokens: two independent online softmaxes
+// per head, merged in the epilogue.
 //
 // Warp roles, linked only by mbarriers (every wait bounded and abortable):
 //  - warps 0-3, softmax: first the Q tile (row max -> 2^-eq -> hi/lo into
@@ -84,7 +88,9 @@ constexpr uint32_t kUmmaBMnMajor = 1u << 16;
 static_assert(kUmmaHeads == 64, "64 virtual heads: hi and lo rows of one M = 128 tile");
 
 template <int D>
-__host__ __device__ constexpr int umma_ring() { return 3; }
+// raw chunks in flight per CTA (4: 2-3% faster than 3 on the large batch at 32
+// and 64 pairs; 5 no faster)
+__host__ __device__ constexpr int umma_ring() { return 4; }
 // TMEM columns: S twice (64), O (D), the Q tile (D / 2)
 template <int D>
 __host__ __device__ constexpr uint32_t umma_tmem_cols() { return D == 256 ? 512u : 256u; }
@@ -103,8 +109,11 @@ __device__ __forceinline__ uint32_t kmaj_off(int r, int k, int kdim) {
 // k_ready and p_ready too), so the K conversion runs up to four chunks ahead
 // of the softmax; S, P and V tiles are double buffered.
 constexpr int kKDepth = 4;      // measured 1-2% faster than 2 deep (large R = 8, 4, long R = 8)
-enum UmmaBar { kBarQk = 0, kBarPv = 4, kBarVReady = 6, kBarSFree = 8, kBarPReady = 10, kBarKReady = 14,
-               kBarQReady = 18, kBarSlotFree = 19, kUmmaBars = 23 };   // slot_free: one per raw ring slot (ring <= 4)
+// V tiles (and their signals pv, v_ready) are kept for kVDepth chunks (3 or 4
+// deep measured no faster than 2 with the four-chunk ring)
+constexpr int kVDepth = 2;
+enum UmmaBar { kBarQk = 0, kBarPv = 4, kBarVReady = 8, kBarSFree = 12, kBarPReady = 14, kBarKReady = 18,
+               kBarQReady = 22, kBarSlotFree = 23, kUmmaBars = 31 };   // slot_free: one per raw ring slot (ring <= 8)
 
 struct UmmaLayout {
     uint32_t misc, scales, table, ops, ring, slot_bytes, total;
@@ -124,7 +133,7 @@ __host__ __device__ inline UmmaLayout make_umma_layout(int PT, int B) {
     L.scales = align_up(L.misc + 8, 16);
     L.table = L.scales + align_up(kKDepth * (2 * kChunk * 4 + 4), 16);
     L.ops = align_up(L.table + pieces * 4, 128);
-    const uint32_t ops_bytes = kKDepth * 32u * D * 2 + 2u * ((uint32_t)D * 32 * 2 + 128u * kChunk * 2);
+    const uint32_t ops_bytes = kKDepth * 32u * D * 2 + kVDepth * (uint32_t)D * 32 * 2 + 2u * 128u * kChunk * 2;
     L.ring = align_up(L.ops + ops_bytes, 128);
     L.slot_bytes = align_up(2u * kChunk * (D / 4 + 1) * 4, 128);
     L.total = L.ring + RING * L.slot_bytes;
@@ -162,17 +171,19 @@ decode_umma_kernel(Params P) {
     float *vwc = ksc + kKDepth * kChunk;                                 // [4][32] V scales x 2^(131 - E)
     int *ecc = reinterpret_cast<int *>(vwc + kKDepth * kChunk);          // [4] E
     const uint32_t *table = reinterpret_cast<const uint32_t *>(smem + L.table);
-    uint8_t *sK0 = smem + L.ops, *sV0 = sK0 + kKDepth * K_BYTES, *sP0 = sV0 + 2 * V_BYTES;
-    const uint32_t aK0 = s0 + L.ops, aV0 = aK0 + kKDepth * K_BYTES, aP0 = aV0 + 2 * V_BYTES;
+    uint8_t *sK0 = smem + L.ops, *sV0 = sK0 + kKDepth * K_BYTES, *sP0 = sV0 + kVDepth * V_BYTES;
+    const uint32_t aK0 = s0 + L.ops, aV0 = aK0 + kKDepth * K_BYTES, aP0 = aV0 + kVDepth * V_BYTES;
     const uint32_t ring = s0 + L.ring;
     const uint64_t policy = l2_policy_evict_first();
-    const int nquad = min(4, (w.nh + 15) / 16);         // softmax warps that hold a real head
+    const int nsoft = min(4, (w.nh + 15) / 16);          // softmax warps with work
     const int nch = (w.len + kChunk - 1) / kChunk;
 
     // softmax threads: virtual head hl (M row) and token half of each chunk
-    const int hl = 16 * (warp & 3) + (lane & 15);
+    const int qd = warp & 3;                             // TMEM lane quadrant
+    const int hl = 16 * qd + (lane & 15);
     const int half = lane >> 4;
     const bool row_ok = warp < 4 && hl < w.nh;
+    const bool soft_active = warp < nsoft;
     const int vh = w.h0 + hl;
     const int len_row = row_ok ? row_len(P, w, vh) : 0;
     if (warp == 0) tmem_alloc(tmem_slot, TCOLS);
@@ -213,13 +224,13 @@ decode_umma_kernel(Params P) {
         for (int b = 0; b < kKDepth; ++b) {
             mbar_init(bar(kBarQk, b), 1);
             mbar_init(bar(kBarKReady, b), kUmmaKConvThreads);
-            mbar_init(bar(kBarPReady, b), 32 * nquad);
+            mbar_init(bar(kBarPReady, b), 32 * nsoft);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kVDepth; ++b) {
             mbar_init(bar(kBarPv, b), 1);
             mbar_init(bar(kBarVReady, b), kUmmaVConvThreads);
-            mbar_init(bar(kBarSFree, b), 32 * nquad);
         }
+        for (int b = 0; b < 2; ++b) mbar_init(bar(kBarSFree, b), 32 * nsoft);
         mbar_init(bar(kBarQReady, 0), 128);
         *abort = 0u;
         fence_mbar_init();
@@ -279,7 +290,7 @@ decode_umma_kernel(Params P) {
                          (c < 2 || mbar_wait_abortable(bar(kBarSFree, b), par ^ 1, abort));
                 } else {
                     ok = mbar_wait_abortable(bar(kBarPReady, b4), par4, abort) &&
-                         mbar_wait_abortable(bar(kBarVReady, b), par, abort);
+                         mbar_wait_abortable(bar(kBarVReady, c % kVDepth), (c / kVDepth) & 1, abort);
                 }
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -295,16 +306,16 @@ decode_umma_kernel(Params P) {
                     last_commit = kBarQk + b4;
                     last_parity = par4;
                 } else {                                           // O += P(c) . V(c)
-                    const uint32_t aP = aP0 + b * P_BYTES, aV = aV0 + b * V_BYTES;
+                    const uint32_t aP = aP0 + b * P_BYTES, aV = aV0 + (c % kVDepth) * V_BYTES;
                     // V tile: token rows of D dims = the MN-major B layout, 8-token
                     // blocks LBO = D * 16 bytes apart, 8-dim blocks SBO = 128 apart;
                     // k-steps 0, 1: tokens 0-15, 16-31
                     umma_f16(tO, umma_smem_desc(aP, 128, 512), umma_smem_desc(aV, D * 16, 128), IDESC_PV, c > 0);
                     umma_f16(tO, umma_smem_desc(aP + 256, 128, 512), umma_smem_desc(aV + 2 * D * 16, D * 16, 128),
                              IDESC_PV, true);
-                    umma_commit(bar(kBarPv, b));
-                    last_commit = kBarPv + b;
-                    last_parity = par;
+                    umma_commit(bar(kBarPv, c % kVDepth));
+                    last_commit = kBarPv + c % kVDepth;
+                    last_parity = (c / kVDepth) & 1;
                 }
             }
         }
@@ -350,7 +361,7 @@ decode_umma_kernel(Params P) {
         };
         int Ew = 12;                                           // weight-scale exponent (second K warp)
         for (int i = 0; i < nch; ++i) {
-            const int b = i & 1, k = i % RING;
+            const int k = i % RING;
             const uint32_t *rawK = reinterpret_cast<const uint32_t *>(smem + L.ring + k * L.slot_bytes);
             const uint32_t *rawV = rawK + kChunk * W;
             // every wait's outcome is made warp-uniform: a K-group warp reduces over its lanes
@@ -380,12 +391,14 @@ decode_umma_kernel(Params P) {
                 mbar_arrive(bar(kBarKReady, b4));
             } else {
                 // V tile b free: PV(i-2) done
-                if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort)))
+                const int bv = i % kVDepth;                     // V tile bv free: PV(i - kVDepth) done
+                if (i >= kVDepth &&
+                    !__all_sync(0xFFFFFFFFu, mbar_wait_abortable(bar(kBarPv, bv), ((i / kVDepth) & 1) ^ 1, abort)))
                     break;
                 // as K: the PV B operand is MN-major
-                convert_tile(std::integral_constant<int, D / 8 / kUmmaVConvWarps>(), rawV, sV0 + b * V_BYTES);
+                convert_tile(std::integral_constant<int, D / 8 / kUmmaVConvWarps>(), rawV, sV0 + bv * V_BYTES);
                 fence_proxy_async_smem();
-                mbar_arrive(bar(kBarVReady, b));
+                mbar_arrive(bar(kBarVReady, bv));
             }
             mbar_arrive(bar(kBarSlotFree, k));                // raw slot k read for the last time (by this group)
         }
@@ -413,117 +426,129 @@ decode_umma_kernel(Params P) {
             tc_fence_before();
             mbar_arrive(bar(kBarQReady, 0));
         }
-        if (warp < nquad) {
-            // ---- softmax (this warp's 16 virtual heads)
+        if (soft_active) {
+            // ---- softmax (this warp's 16 pairs)
             // chunks below every row's length in this warp need no masking (0 when a
-            // lane holds no head: that warp always masks)
+            // lane holds no pair: that warp always masks)
             const int len_full = (int)__reduce_min_sync(0xFFFFFFFFu, (unsigned)(row_ok ? len_row : 0));
-            // this thread's P tile words: its head's hi row (32q + j) and lo row
-            // (32q + 16 + j) at tokens 16 half .. + 7 and + 8 .. + 15
-            const int row_h = 32 * (warp & 3) + (lane & 15), row_l = row_h + 16;
-            const uint32_t p_off[4] = {kmaj_off(row_h, 16 * half, kChunk), kmaj_off(row_h, 16 * half + 8, kChunk),
-                                       kmaj_off(row_l, 16 * half, kChunk), kmaj_off(row_l, 16 * half + 8, kChunk)};
+            const int row_h = 32 * qd + (lane & 15), row_l = row_h + 16;   // this pair's hi and lo rows
             bool ok = true;
-            for (int i = 0; ok && i < nch; ++i) {
-                const int b = i & 1, b4 = i & (kKDepth - 1);
-                const uint32_t par4 = (i / kKDepth) & 1;
-                ok = mbar_wait_abortable(bar(kBarQk, b4), par4, abort);
-                ok = ok && mbar_wait_abortable(bar(kBarKReady, b4), par4, abort);   // the scale table
-                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                tc_fence_after();
-                float zh[16], zl[16];                            // this head's hi and lo rows, 16 tokens
-                tmem_ld16x2(tmem + 32 * b + lane_hi, zh);
-                tmem_ld16x2(tmem + 32 * b + lane_lo, zl);
-                tc_fence_before();
-                mbar_arrive(bar(kBarSFree, b));
-                float ks[16], vw[16];
+            // NT = 16 tokens of each chunk per thread (tokens 16 half ..)
+            auto run = [&]() {
+                constexpr int NT = 16;
+                constexpr int NP = NT / 2;
+                const int tok0 = 16 * half;
+                // this thread's P tile words: hi row then lo row, 8 tokens per 16 bytes
+                uint32_t p_off[NT / 4];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 a = reinterpret_cast<const float4 *>(ksc + b4 * kChunk + 16 * half)[q4];
-                    const float4 c = reinterpret_cast<const float4 *>(vwc + b4 * kChunk + 16 * half)[q4];
-                    ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
-                    vw[4 * q4] = c.x; vw[4 * q4 + 1] = c.y; vw[4 * q4 + 2] = c.z; vw[4 * q4 + 3] = c.w;
+                for (int k = 0; k < NT / 8; ++k) {
+                    p_off[k] = kmaj_off(row_h, tok0 + 8 * k, kChunk);
+                    p_off[NT / 8 + k] = kmaj_off(row_l, tok0 + 8 * k, kChunk);
                 }
-                const int Ei = ecc[b4];
-                float2 t2[8];                                    // z x k scale x scale x log2 e; -inf where masked
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    t2[u] = mul_f2(add_f2(make_float2(zh[2 * u], zh[2 * u + 1]), make_float2(zl[2 * u], zl[2 * u + 1])),
-                                   make_float2(ks[2 * u], ks[2 * u + 1]));
-                if ((i + 1) * kChunk > len_full) {               // warp-uniform: some row ends in this chunk
-                    const int t0 = i * kChunk + 16 * half;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (t0 + 2 * u >= len_row) t2[u].x = -INFINITY;
-                        if (t0 + 2 * u + 1 >= len_row) t2[u].y = -INFINITY;
-                    }
-                }
-                // a tree of three-input maxima (depth 3)
-                const float c0 = max3f(t2[0].x, t2[0].y, t2[1].x), c1 = max3f(t2[1].y, t2[2].x, t2[2].y);
-                const float c2 = max3f(t2[3].x, t2[3].y, t2[4].x), c3 = max3f(t2[4].y, t2[5].x, t2[5].y);
-                const float c4 = max3f(t2[6].x, t2[6].y, t2[7].x);
-                float cmax = fmaxf(max3f(c0, c1, c2), max3f(c3, c4, t2[7].y));
-                cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));   // the head's other 16 tokens
-                const float cm = cmax * qk2;                     // qk2 = 2^eq > 0: the max of the logits
-                // the same decision in both threads of a head (same cm, m, E)
-                const bool need = cm > m + (float)kLazy || Ei > E;
-                float fa = 1.0f;
-                if (need) {
-                    const float m_new = fmaxf(m, cm);
-                    const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
-                    const float ea = (E - Ei < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - Ei) << 23);
-                    fa = alpha * ea;
-                    lsum.x *= alpha;
-                    lsum.y *= alpha;
-                    m = m_new;
-                    E = Ei;
-                }
-                if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {      // O rows once PV(i-1) is done
-                    ok = mbar_wait_abortable(bar(kBarPv, (i - 1) & 1), ((i - 1) >> 1) & 1, abort);
+                for (int i = 0; ok && i < nch; ++i) {
+                    const int b = i & 1, b4 = i & (kKDepth - 1);
+                    const uint32_t par4 = (i / kKDepth) & 1;
+                    ok = mbar_wait_abortable(bar(kBarQk, b4), par4, abort);
+                    ok = ok && mbar_wait_abortable(bar(kBarKReady, b4), par4, abort);   // the scale table
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {                // hi rows, then lo rows
-                        const uint32_t a = tO + (c & 1 ? lane_lo : lane_hi) + 32 * (c >> 1);
-                        float o[16];
-                        tmem_ld16x2(a, o);
+                    float zh[NT], zl[NT];                        // this pair's hi and lo rows at its tokens
+                    tmem_ld16x2(tmem + 32 * b + lane_hi, zh);
+                    tmem_ld16x2(tmem + 32 * b + lane_lo, zl);
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarSFree, b));
+                    float ks[NT], vw[NT];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) o[j] *= fa;
-                        tmem_st16x2(a, o);
+                    for (int q4 = 0; q4 < NT / 4; ++q4) {
+                        const float4 a = reinterpret_cast<const float4 *>(ksc + b4 * kChunk + tok0)[q4];
+                        const float4 c = reinterpret_cast<const float4 *>(vwc + b4 * kChunk + tok0)[q4];
+                        ks[4 * q4] = a.x; ks[4 * q4 + 1] = a.y; ks[4 * q4 + 2] = a.z; ks[4 * q4 + 3] = a.w;
+                        vw[4 * q4] = c.x; vw[4 * q4 + 1] = c.y; vw[4 * q4 + 2] = c.z; vw[4 * q4 + 3] = c.w;
                     }
-                }
-                if (i >= 2) {                                       // P tile b free: PV(i-2) done
-                    ok = mbar_wait_abortable(bar(kBarPv, b), ((i - 2) >> 1) & 1, abort);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                }
-                const float m_ref = m == -INFINITY ? 0.0f : m;
-                const float2 q2 = make_float2(qk2, qk2), nm2 = make_float2(-m_ref, -m_ref);
-                uint32_t ph[8], pl[8];
-                float2 pp[8];
+                    const int Ei = ecc[b4];
+                    float2 t2[NP];                               // z x k scale x scale x log2 e; -inf where masked
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float2 a = fma_f2(t2[u], q2, nm2);        // masked tokens: 2^-inf = 0
-                    pp[u] = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                    const float2 pw = mul_f2(pp[u], make_float2(vw[2 * u], vw[2 * u + 1]));
-                    split_f16x2_fma(pw.x, pw.y, ph[u], pl[u]);
+                    for (int u = 0; u < NP; ++u)
+                        t2[u] = mul_f2(add_f2(make_float2(zh[2 * u], zh[2 * u + 1]), make_float2(zl[2 * u], zl[2 * u + 1])),
+                                       make_float2(ks[2 * u], ks[2 * u + 1]));
+                    if ((i + 1) * kChunk > len_full) {           // warp-uniform: some row ends in this chunk
+                        const int t0 = i * kChunk + tok0;
+#pragma unroll
+                        for (int u = 0; u < NP; ++u) {
+                            if (t0 + 2 * u >= len_row) t2[u].x = -INFINITY;
+                            if (t0 + 2 * u + 1 >= len_row) t2[u].y = -INFINITY;
+                        }
+                    }
+                    // a tree of three-input maxima
+                    const float c0 = max3f(t2[0].x, t2[0].y, t2[1].x), c1 = max3f(t2[1].y, t2[2].x, t2[2].y);
+                    const float c2 = max3f(t2[3].x, t2[3].y, t2[4].x), c3 = max3f(t2[4].y, t2[5].x, t2[5].y);
+                    const float c4 = max3f(t2[6].x, t2[6].y, t2[7].x);
+                    float cmax = fmaxf(max3f(c0, c1, c2), max3f(c3, c4, t2[7].y));
+                    cmax = fmaxf(cmax, __shfl_xor_sync(0xFFFFFFFFu, cmax, 16));   // the pair's other tokens
+                    const float cm = cmax * qk2;                 // qk2 = 2^eq > 0: the max of the logits
+                    // the same decision in both threads of a pair (same cm, m, E)
+                    const bool need = cm > m + (float)kLazy || Ei > E;
+                    float fa = 1.0f;
+                    if (need) {
+                        const float m_new = fmaxf(m, cm);
+                        const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+                        const float ea = (E - Ei < -126) ? 0.0f : __uint_as_float((uint32_t)(127 + E - Ei) << 23);
+                        fa = alpha * ea;
+                        lsum.x *= alpha;
+                        lsum.y *= alpha;
+                        m = m_new;
+                        E = Ei;
+                    }
+                    if (i >= 1 && __any_sync(0xFFFFFFFFu, need)) {  // O rows once PV(i-1) is done
+                        ok = mbar_wait_abortable(bar(kBarPv, (i - 1) % kVDepth), ((i - 1) / kVDepth) & 1, abort);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c = 0; c < D / 16; ++c) {            // hi rows, then lo rows
+                            const uint32_t a = tO + (c & 1 ? lane_lo : lane_hi) + 32 * (c >> 1);
+                            float o[16];
+                            tmem_ld16x2(a, o);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) o[j] *= fa;
+                            tmem_st16x2(a, o);
+                        }
+                    }
+                    if (i >= 2) {                                   // P tile b free: PV(i-2) done
+                        ok = mbar_wait_abortable(bar(kBarPv, (i - 2) % kVDepth), ((i - 2) / kVDepth) & 1, abort);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    }
+                    const float m_ref = m == -INFINITY ? 0.0f : m;
+                    const float2 q2 = make_float2(qk2, qk2), nm2 = make_float2(-m_ref, -m_ref);
+                    uint32_t ph[NP], pl[NP];
+                    float2 pp[NP];
+#pragma unroll
+                    for (int u = 0; u < NP; ++u) {
+                        const float2 a = fma_f2(t2[u], q2, nm2);    // masked tokens: 2^-inf = 0
+                        pp[u] = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                        const float2 pw = mul_f2(pp[u], make_float2(vw[2 * u], vw[2 * u + 1]));
+                        split_f16x2_fma(pw.x, pw.y, ph[u], pl[u]);
+                    }
+                    // the chunk's weights summed as a tree, then added to the row's sum
+                    lsum = add_f2(lsum, add_f2(add_f2(add_f2(pp[0], pp[1]), add_f2(pp[2], pp[3])),
+                                               add_f2(add_f2(pp[4], pp[5]), add_f2(pp[6], pp[7]))));
+                    uint8_t *dP = sP0 + b * P_BYTES;
+#pragma unroll
+                    for (int k = 0; k < NT / 8; ++k) {
+                        *reinterpret_cast<uint4 *>(dP + p_off[k]) =
+                            make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
+                        *reinterpret_cast<uint4 *>(dP + p_off[NT / 8 + k]) =
+                            make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarPReady, b4));
                 }
-                // the chunk's weights summed as a tree, then added to the row's sum
-                lsum = add_f2(lsum, add_f2(add_f2(add_f2(pp[0], pp[1]), add_f2(pp[2], pp[3])),
-                                           add_f2(add_f2(pp[4], pp[5]), add_f2(pp[6], pp[7]))));
-                // P rows of this head: hi (32q + j) and lo (32q + 16 + j), tokens 16 half ..
-                uint8_t *dP = sP0 + b * P_BYTES;
-                *reinterpret_cast<uint4 *>(dP + p_off[0]) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                *reinterpret_cast<uint4 *>(dP + p_off[1]) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-                *reinterpret_cast<uint4 *>(dP + p_off[2]) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                *reinterpret_cast<uint4 *>(dP + p_off[3]) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(bar(kBarPReady, b4));
-            }
-            // the last PV, then this thread's half of its head's output row (hi +
+            };
+            run();
+            // the last PV, then this thread's half of its pair's output row (hi +
             // lo rows of O), normalised (one partition) or as the partition's
             // record (m, l and the unnormalised row in the V scales' units)
-            if (ok) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) & 1), ((nch - 1) >> 1) & 1, abort);
+            if (ok) ok = mbar_wait_abortable(bar(kBarPv, (nch - 1) % kVDepth), ((nch - 1) / kVDepth) & 1, abort);
             if (__all_sync(0xFFFFFFFFu, ok)) {
                 tc_fence_after();
                 const float l_half = lsum.x + lsum.y;
