@@ -53,19 +53,21 @@ namespace {
 //    O += P.V, each as soon as its inputs are ready.  A thread's MMAs run
 //    one after another (about 25 ns each at these shapes), so the two
 //    streams from two threads overlap.
-//  - warp 9: refills the raw ring, chunk c into the slot of chunk c - ring
-//    once the conversion has read that slot (slot_free[slot]).
-// K, V, P and S are double buffered by chunk parity.  Signals per buffer
-// b = chunk & 1: k_ready[b] (warps 4-5: K tile and scale table written),
-// v_ready[b] (warp 6: V tile written), s_free[b] /
-// p_ready[b] (the active softmax threads), qk[b] / pv[b] (tcgen05.commit),
-// and q_ready once (the 128 softmax threads: Q tile stored).  QK and the
-// softmax wait only for k_ready, so a chunk's logits do not wait for its V
-// tile, whose conversion waits for PV two chunks back.  A waiter never falls
-// two phases behind: the next phase of each barrier needs a step that
-// follows the wait (v_ready(j + 2) needs PV(j), issued after the issue warp
-// saw v_ready(j); slot_free for chunk c + ring needs the refill issued after
-// the wait for chunk c).
+//  - warp 9: refills the raw ring (four chunks), chunk c into the slot of
+//    chunk c - 4 once both conversion groups have read it (slot_free[slot]).
+// S, P and V tiles are double buffered by chunk parity b = chunk & 1; K tiles
+// and scale tables are four deep, b4 = chunk & 3.  Signals: k_ready[b4]
+// (warps 4-5: K tile and scale table written), qk[b4] (tcgen05.commit of
+// QK), p_ready[b4] (the active softmax threads: P written, so the table is
+// free), s_free[b] (S read), v_ready[b] (warp 6: V tile written), pv[b]
+// (commit of PV), and q_ready once (the 128 softmax threads: Q tile stored).
+// QK and the softmax wait only for k_ready, so a chunk's logits do not wait
+// for its V tile, whose conversion waits for PV two chunks back.  A waiter
+// never falls two phases behind: the next phase of each barrier needs a step
+// that follows the wait (v_ready(j + 2) needs PV(j), issued after the issue
+// warp saw v_ready(j); k_ready(j + 4) needs p_ready(j), which the softmax
+// gives after its wait for k_ready(j); slot_free for chunk c + 4 needs the
+// refill issued after the wait for chunk c).
 
 // Warp roles: 0-3 softmax, 4-5 K conversion (and the scale tables), 6 V
 // conversion, 7 PV issue, 8 QK issue, 9 ring refill.  Ten warps: two CTAs
