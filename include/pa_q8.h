@@ -23,6 +23,10 @@
  * ordering pass) is launched to take that chance.  That kernel reads only
  * context_lens before the previous kernel has finished, and waits for it
  * before anything else; every later step of the decode waits for it in turn.
+ * A decode whose split-context grid fits in one wave has no ordering pass;
+ * its partials are merged by a second kernel, launched as a programmatic
+ * dependent of the attention kernel, which waits for that kernel to finish
+ * before it reads anything.
  * So context_lens must be final when the kernel before the decode starts,
  * which stream order gives unless that kernel is itself one (of the caller's)
  * that writes context_lens and allows early dependents.
@@ -236,7 +240,7 @@ int pa_q8_decode_rows(float *out, const float *q,
  * pa_q8_decode_append -- one decode step with the newest tokens' K/V
  * appended inside the attention launch: reshape_and_cache_q8 of those rows
  * followed by pa_q8_decode_rows, in that order (append, then attend), as one
- * kernel launch after the ordering prep.
+ * attention launch (after the ordering prep, when the plan has one).
  *
  * context_lens[s] counts the new tokens: row b (0 <= b < num_rows) of the
  * new K/V rows is position c - num_rows + b of sequence s, c = min(

@@ -34,6 +34,21 @@
 #ifndef PA_Q8_TAIL_CUT_X4
 #define PA_Q8_TAIL_CUT_X4 3
 #endif
+// Split grids that fit in one wave merge their partials in a combine grid of
+// their own (0: always by the last CTA of each group)
+#ifndef PA_Q8_SEP_COMBINE
+#define PA_Q8_SEP_COMBINE 1
+#endif
+// Head size 256: 8-head CTAs when 16-head ones would not fill one wave (0:
+// always 16 heads per CTA)
+#ifndef PA_Q8_TC256_HEADS8
+#define PA_Q8_TC256_HEADS8 1
+#endif
+// With such a combine grid, one-tile tensor-core CTAs store one record per
+// token-slot warp instead of merging their warps (0: CTA merge)
+#ifndef PA_Q8_SLOT_RECORDS
+#define PA_Q8_SLOT_RECORDS 1
+#endif
 
 namespace pa_q8 {
 namespace {
@@ -305,6 +320,34 @@ decode_tc_kernel(Params P) {
     if (__syncthreads_or(!ok)) return;
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+    if (P.rec_slots > 1) {
+        // The combine grid merges every row: each warp stores its own
+        // record (A in true units, m, l) for the rows of its head tile, and
+        // no CTA merge runs.  For a fixed word group jj and column pair half
+        // e, a thread's four accumulators are four consecutive head dims:
+        // one float4.
+        if (row_ok) {
+            const float f = ldexpf(1.0f, E - kVScaleBias);
+            float *rec = P.part + ((qrow(P, w, vh) * P.NP + w.p) * SLOTS + ts) * (D + 4);
+#pragma unroll
+            for (int jj = 0; jj < NJ; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float4 v;
+                    v.x = (acc[4 * jj + 0][e] + acc[4 * jj + 0][e + 2]) * f;
+                    v.y = (acc[4 * jj + 1][e] + acc[4 * jj + 1][e + 2]) * f;
+                    v.z = (acc[4 * jj + 2][e] + acc[4 * jj + 2][e + 2]) * f;
+                    v.w = (acc[4 * jj + 3][e] + acc[4 * jj + 3][e + 2]) * f;
+                    *reinterpret_cast<float4 *>(rec + 4 * vword<D>(2 * cq + e, jj)) = v;
+                }
+            }
+            if (cq == 0) {
+                rec[D] = m;
+                rec[D + 1] = lsum;
+            }
+        }
+        return;
+    }
     float *ml = reinterpret_cast<float *>(smem + L.ring);            // [slot][HT*8][3]
     float *accs = ml + SLOTS * HT * 8 * 3;                            // [slot][HT*8][D]
     static_assert(merge_scratch_bytes(D, SLOTS, HT * 8) <= ring_bytes(D, SLOTS, RING),
@@ -864,6 +907,92 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
         order[i] = ((unsigned long long)(cap - (int64_t)(keys[i] >> 32)) << 32) | (keys[i] & 0xFFFFFFFFull);
 }
 
+// ============================================================== combine
+//
+// The log-sum-exp merge of split-context partials as a grid of its own
+// ("attention.rs", the attn_combine dispatch after the split-T decode), for
+// plans whose split grid fits in one wave: there the merge by the group's
+// last CTA sits at the end of the critical path, one CTA working through
+// every head of its group.  Here one warp (two at head size 256, each with
+// half the dims) merges one output row (sequence, query row, head) from its
+// records -- one per partition, or one per token-slot warp of each partition
+// (rec_slots) --: M = max_r m_r, L = sum_r l_r 2^(m_r - M), out = (1/L)
+// sum_r A_r 2^(m_r - M), summed over r in order, with the first 16 records'
+// A loads in flight while M and L are reduced.  Launched as a programmatic
+// dependent of the attention grid: it waits for that grid's completion and
+// memory before the first load.  With one record per partition, rows of a
+// context that fits one partition were written by the attention CTA and are
+// left alone.
+constexpr int kCombineThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params P) {
+    constexpr int DP = D + 4;                 // floats per partial record
+    constexpr int WPR = D > 128 ? D / 128 : 1;    // warps per row
+    constexpr int V4W = D / 4 / WPR;          // float4 of the row per warp (32, or 16 at head size 64)
+    constexpr int RU = 16;                    // records' loads in flight per thread
+    grid_dependency_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * (kCombineThreads / 32) + warp;
+    const int64_t row = gw / WPR;             // (s * R + b) * H + h
+    if (row >= (int64_t)P.S * P.R * P.H) return;
+    const int s = (int)(row / ((int64_t)P.R * P.H));
+    const int64_t cap = (int64_t)P.Nb * P.B;
+    const int64_t craw = __ldg(P.cl + s);
+    const int c = (int)(craw < cap ? craw : cap);
+    const int nrec = (c + P.PT - 1) / P.PT * P.rec_slots;     // records of this row
+    if (nrec <= 1) return;
+    const float *rec = P.part + row * P.NP * P.rec_slots * DP;
+    const int d4 = (int)(gw % WPR) * V4W + lane;              // this thread's float4 of the row
+    const bool act = lane < V4W;
+
+    float4 v[RU];
+    float mp[RU];
+    auto load = [&](int r0) {
+#pragma unroll
+        for (int j = 0; j < RU; ++j) {
+            const float *r = rec + (size_t)min(r0 + j, nrec - 1) * DP;
+            mp[j] = __ldcg(r + D);
+            if (act) v[j] = __ldcg(reinterpret_cast<const float4 *>(r) + d4);
+        }
+    };
+    load(0);
+    // (m, l) of record lane (and lane + 32, ...), in flight with the A loads
+    const float2 ml0 = lane < nrec ? __ldcg(reinterpret_cast<const float2 *>(rec + (size_t)lane * DP + D))
+                                   : make_float2(-INFINITY, 0.0f);
+    float M = ml0.x;
+    for (int r = lane + 32; r < nrec; r += 32) M = fmaxf(M, __ldcg(rec + (size_t)r * DP + D));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    if (M == -INFINITY) M = 0.0f;             // a query row that sees no token: weights 0, row 0
+    float L = ml0.y * fast_exp2(ml0.x - M);
+    for (int r = lane + 32; r < nrec; r += 32) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(rec + (size_t)r * DP + D));
+        L += ml.y * fast_exp2(ml.x - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r0 = 0;;) {
+#pragma unroll
+        for (int j = 0; j < RU; ++j) {
+            if (r0 + j < nrec) {
+                const float x = fast_exp2(mp[j] - M);
+                a.x = fmaf(v[j].x, x, a.x);
+                a.y = fmaf(v[j].y, x, a.y);
+                a.z = fmaf(v[j].z, x, a.z);
+                a.w = fmaf(v[j].w, x, a.w);
+            }
+        }
+        r0 += RU;
+        if (r0 >= nrec) break;
+        load(r0);
+    }
+    const float il = L > 0.0f ? 1.0f / L : 0.0f;
+    if (act) reinterpret_cast<float4 *>(P.out + row * D)[d4] = make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
+}
+
 // ============================================================== selftest
 __global__ void wait_selftest_kernel(uint64_t limit_ns, uint32_t *status) {
     __shared__ __align__(8) uint64_t bar;
@@ -901,6 +1030,7 @@ Params make_params(const DecodeArgs &a) {
     P.nk_stride = a.new_key_stride; P.nv_stride = a.new_value_stride;
     P.contiguous = a.contiguous;
     P.per_sm = a.per_sm;
+    P.rec_slots = a.rec_slots > 1 ? a.rec_slots : 1;
     P.kc_w = const_cast<uint32_t *>(a.key_cache);      // written only by the fused append
     P.vc_w = const_cast<uint32_t *>(a.value_cache);
     return P;
@@ -947,7 +1077,7 @@ cudaError_t launch_cc(const Params &P, cudaStream_t st) {
 template <int D>
 cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
     if (P.order) {
-        const int64_t n_counters = P.NP > 1 ? (int64_t)P.S * P.Hk * P.head_groups : 0;
+        const int64_t n_counters = P.NP > 1 && P.counters ? (int64_t)P.S * P.Hk * P.head_groups : 0;
         int n = 1;
         while (n < P.S && n < kPrepMaxSort) n <<= 1;
         const size_t smem = (size_t)n * sizeof(unsigned long long);
@@ -969,10 +1099,27 @@ cudaError_t launch_d(const Params &P, int kernel, cudaStream_t st) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (kernel == kF32) return launch_f32_family(P, D, st);
-    if (P.contiguous) return launch_cq_family(P, D, st);
-    if (kernel == kTcgen05) return launch_umma_family(P, D, st);
-    return (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
+    cudaError_t e;
+    if (kernel == kF32) e = launch_f32_family(P, D, st);
+    else if (P.contiguous) e = launch_cq_family(P, D, st);
+    else if (kernel == kTcgen05) e = launch_umma_family(P, D, st);
+    else e = (kernel == kCudaCore) ? launch_cc<D>(P, st) : launch_tc<D>(P, st);
+    if (e != cudaSuccess || P.NP <= 1 || P.counters != nullptr) return e;
+    // split contexts without arrival counters: the combine grid, launched as a
+    // programmatic dependent of the attention grid
+    const int64_t warps = (int64_t)P.S * P.R * P.H * (D > 128 ? D / 128 : 1);     // warps per row: combine_kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32)));
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, combine_kernel<D>, P);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 // CTAs of the chosen kernel resident per SM (registers and shared memory as
@@ -1015,7 +1162,7 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
             // epilogue, finish sooner (32 MQA sequences of up to 4095 tokens:
             // 31.4 us against 33.4 us)
             const int64_t units16 = (int64_t)a.num_seqs * a.num_kv_heads * ((r + 15) / 16);
-            cap = units16 < num_sms ? 8 : 16;
+            cap = PA_Q8_TC256_HEADS8 && units16 < num_sms ? 8 : 16;
         }
         a.heads_per_cta = r < cap ? r : cap;
     } else {
@@ -1068,6 +1215,18 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
     }
     a.per_sm = per_sm;
     a.one_wave = np == 1 && units <= (int64_t)per_sm * num_sms;
+    // A split grid whose expected CTAs (contexts taken at half their maximum)
+    // all fit at once: the partials are merged by a combine grid of its own,
+    // a warp per output row, instead of by the last CTA of each group, whose
+    // merge of every head would end the critical path.  Such a grid needs no
+    // longest-first order and no arrival counters, so no prep kernel.
+    const int64_t expect = units * std::max<int64_t>(1, (max_ctx / 2 + pt - 1) / pt);
+    a.sep_combine = PA_Q8_SEP_COMBINE && np > 1 && expect <= (int64_t)per_sm * num_sms;
+    // The one-tile tensor-core kernel then skips its CTA merge too: each
+    // token-slot warp stores its own record, and the combine grid merges every
+    // row (one partition or several).
+    a.rec_slots = a.sep_combine && PA_Q8_SLOT_RECORDS && a.kernel == kTensorCore && !a.contiguous &&
+                          (a.heads_per_cta <= 8 || a.head_size == 256) ? PA_Q8_TC_SLOTS : 1;
     return true;
 }
 
@@ -1079,7 +1238,7 @@ size_t plan_workspace_bytes(const DecodeArgs &a) {
     const size_t order = round256((size_t)a.num_seqs * sizeof(unsigned long long));
     if (a.num_partitions <= 1) return order;
     const size_t groups = (size_t)a.num_seqs * a.num_kv_heads * a.head_groups;
-    const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions;
+    const size_t rows = (size_t)a.num_seqs * a.num_rows * a.num_heads * a.num_partitions * (a.rec_slots > 1 ? a.rec_slots : 1);
     return order + round256(groups * sizeof(uint32_t)) + rows * (a.head_size + 4) * sizeof(float);
 }
 
@@ -1100,7 +1259,9 @@ int64_t plan_num_ctas(const DecodeArgs &a) {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     Params P = make_params(a);
-    if (a.one_wave) P.order = nullptr;       // every CTA starts at once: no order, no prep kernel
+    // every CTA starts at once: no order, and without counters no prep kernel
+    if (a.one_wave || a.sep_combine) P.order = nullptr;
+    if (a.sep_combine) P.counters = nullptr;
     switch (a.head_size) {
         case 64: return launch_d<64>(P, a.kernel, stream);
         case 128: return launch_d<128>(P, a.kernel, stream);

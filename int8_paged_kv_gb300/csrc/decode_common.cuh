@@ -41,8 +41,11 @@ struct Params {
     int head_groups;
     const unsigned long long *order;  // [S]: (clamped length << 32 | sequence) of grid z,
                                       // longest context first
-    uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far
-    float *part;            // [S][R][H][NP][D + 4]: A, then m, l (and two spare words)
+    uint32_t *counters;     // [S][gridDim.y]: partitions of the group finished so far;
+                            // nullptr: a combine grid of its own merges the partials
+    int rec_slots;          // partial records per (row, partition): 1 (the CTA's merged
+                            // state), or the token-slot warps' own (combine grid only)
+    float *part;            // [S][R][H][NP][rec_slots][D + 4]: A, then m, l (and two spare words)
     uint32_t *status;
     // fused append of the newest R tokens (nk == nullptr: none)
     const float *nk;
@@ -131,6 +134,9 @@ struct Work {
 // are split.  CTAs with p >= np have nothing to stream and return false; so
 // does partition 0 of an empty context, whose rows write_zero_rows writes.
 __device__ __forceinline__ bool setup_work(const Params &P, Work &w) {
+    // a split grid merged by a separate combine grid lets that grid launch
+    // now; its CTAs then wait (griddepcontrol.wait) for this one to finish
+    grid_dependents_launch();
     w.p = blockIdx.x;
     w.g = blockIdx.y / P.head_groups;
     const int hg = blockIdx.y % P.head_groups;
@@ -514,6 +520,7 @@ __device__ __noinline__ void combine_rows_outlined(const Params &P, const Work &
 // memory free up to the end of the dynamic allocation.
 template <int D, bool kOutlineCombine = false>
 __device__ void arrive_and_combine(const Params &P, const Work &w, uint8_t *scratch) {
+    if (P.counters == nullptr) return;       // merged by the combine grid that follows
     __threadfence();
     __syncthreads();
     const int np = w.np;

@@ -59,13 +59,18 @@ struct DecodeArgs {
     int head_groups;       // CTAs per (seq, kv head, partition) along the group
     int one_wave;          // one partition per context and every CTA resident at once: no
                            // ordering and no combine counters, so no prep kernel
+    int sep_combine;       // split contexts merged by a combine grid of its own (launched as a
+                           // programmatic dependent), not by the last CTA of each group: no
+                           // arrival counters, no ordering, so no prep kernel
+    int rec_slots;         // partial records per (row, partition): 1, or the token-slot warps
+                           // of a one-tile tensor-core CTA, each storing its own (combine grid)
     int per_sm;            // CTAs per SM the waves are sized for (selects the contiguous
                            // kernel's register budget)
     // workspace: sequence order [S] (u64: clamped length << 32 | sequence,
     // longest context first); when partitions > 1 also arrival counters
     // [S][Hk * head_groups] (u32) and one partial record per (sequence, query
-    // row, head, partition): [S][R][H][P][head_size + 4] f32, the weighted sum
-    // A followed by m, l and two spare words
+    // row, head, partition) -- or rec_slots of them --: [S][R][H][P][rec_slots]
+    // [head_size + 4] f32, the weighted sum A followed by m, l and two spare words
     unsigned long long *order;
     uint32_t *counters;
     float *partials;

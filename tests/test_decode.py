@@ -278,3 +278,43 @@ def test_combine_of_many_partitions(kernel, D):
         assert_close(got, want, f"D {D} kernel {kernel} pt {pt}")
         assert np.all(got[2] == 0.0)
     assert device_status() == 0
+
+
+# (S, H, Hk, D, B, lens, pt, R): split contexts merged by each route.  The
+# plan takes the separate combine grid when the split grid's expected CTAs
+# (contexts at half the table's capacity) fit in one wave, else the merge by
+# the last CTA of each group (arrival counters, prep kernel).
+COMBINE_CASES = {
+    # one wave, head size 256, 8-head CTAs: one record per token-slot warp,
+    # every row (split or not) merged by the combine grid, 16 records per row
+    "grid_slot_records_256": (6, 16, 1, 256, 32, [0, 1, 33, 700, 3000, 4095], 1024, 1),
+    # one wave, two causal rows per sequence (8 pairs per kv head)
+    "grid_slot_records_rows": (5, 8, 2, 128, 16, [2, 40, 300, 1500, 2600], 256, 2),
+    # one wave, more than 32 records per row (the (m, l) loop past one warp)
+    "grid_many_records": (3, 8, 2, 128, 16, [9000, 1, 4000], 512, 1),
+    # many waves: the last CTA of each group merges
+    "last_cta_merge": (4, 32, 8, 128, 16, [8000, 100, 5000, 0], 128, 1),
+}
+
+
+@pytest.mark.parametrize("kernel", [TC, CC])
+@pytest.mark.parametrize("case", sorted(COMBINE_CASES))
+def test_split_context_merge_routes(case, kernel):
+    """Both merge routes of split contexts against the oracle, on both
+    kernel families (the CUDA-core family keeps one record per partition)."""
+    from tests.gpu_helpers import (assert_close, device_status, gpu_decode, gpu_decode_rows, oracle_decode,
+                                   oracle_decode_rows)
+    S, H, Hk, D, B, lens, pt, R = COMBINE_CASES[case]
+    w, ok_, ov_, kc, vc = _random_case(S, H, Hk, D, B, lens, seed=70 + len(case))
+    if R == 1:
+        got = gpu_decode(w, kc, vc, kernel=kernel, partition_tokens=pt)
+        want = oracle_decode(w, ok_, ov_)
+    else:
+        q = np.random.default_rng(71).standard_normal((S, R, H, D)).astype(np.float32)
+        got = gpu_decode_rows(w, kc, vc, q, kernel=kernel, partition_tokens=pt)
+        want = oracle_decode_rows(w, ok_, ov_, q)
+    assert_close(got, want, f"{case} kernel {kernel}")
+    for s, c in enumerate(lens):
+        if c == 0:
+            assert np.all(got[s] == 0.0)
+    assert device_status() == 0
