@@ -888,6 +888,65 @@ def run_profile_rows(args) -> None:
                       "gbps": round(nbytes / ms / 1e6, 1), "device_status": pk.pa_q8_device_status()}))
 
 
+def run_profile_workload(args) -> None:
+    """A profiler case, not a bench line: pa_q8_decode on one named workload
+    (--profile-workload), automatic plan unless --kernel / --partition-tokens,
+    L2 flushed before every call; prints the median event time of --steps
+    calls after --warmup."""
+    import torch
+
+    import int8_paged_kv_gb300 as pk
+    from int8_paged_kv_gb300 import build as pkbuild
+
+    pkbuild.build()
+    dev = torch.device("cuda", 0)
+    w = wl.build(args.profile_workload, with_append=False)
+    cfg = w.cfg
+    S, H, Hk, D, B = cfg.num_seqs, cfg.num_heads, cfg.num_kv_heads, cfg.head_size, cfg.block_size
+
+    def u32(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int32)).to(dev)
+
+    kc = torch.empty((w.num_blocks, Hk, B, D // 4 + 1), dtype=torch.int32, device=dev)
+    vc = torch.empty_like(kc)
+    for i in range(0, w.key.shape[0], 1 << 18):
+        pk.pa_q8_reshape_and_cache(torch.from_numpy(w.key[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                   torch.from_numpy(w.value[i:i + (1 << 18)].reshape(-1, Hk * D)).to(dev),
+                                   kc, vc, u32(w.slot_mapping[i:i + (1 << 18)]), num_kv_heads=Hk, head_size=D,
+                                   block_size=B)
+    w.key = w.value = None
+    q = torch.from_numpy(w.q).to(dev)
+    out = torch.empty_like(q)
+    bt, cl = u32(w.block_tables), u32(w.context_lens)
+    opts = dict(kernel=args.kernel, partition_tokens=args.partition_tokens)
+    ws = torch.empty(max(16, pk.pa_q8_decode_workspace_size(S, H, Hk, D, B, cfg.max_blocks_per_seq, **opts)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.ones(l2_flush_bytes(dev) // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def run():
+        pk.pa_q8_decode(out, q, kc, vc, bt, cl, num_kv_heads=Hk, block_size=B, scale=w.scale, workspace=ws,
+                        **opts)
+    for _ in range(max(3, args.warmup)):
+        torch.sum(flush, dim=0, out=sink)
+        run()
+    ts = []
+    for _ in range(args.steps):
+        torch.sum(flush, dim=0, out=sink)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    nbytes = wl.algorithmic_decode_bytes(cfg, w.context_lens)
+    ms = float(np.median(ts))
+    print(json.dumps({"kind": "profile case: decode of one workload", "workload": args.profile_workload,
+                      "plan": pk.pa_q8_decode_plan(S, H, Hk, D, B, cfg.max_blocks_per_seq, **opts),
+                      "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "gbps": round(nbytes / ms / 1e6, 1),
+                      "device_status": pk.pa_q8_device_status()}))
+
+
 def run_contig_line(args, name, w, cl, q, flush, sink, peaks) -> None:
     """The same contexts in the contiguous q8 cache (per-sequence code rows +
     side scale region, max_t = the workload's largest context), appended by
@@ -1215,6 +1274,8 @@ def main():
     ap.add_argument("--profile-rows", type=int, default=0,
                     help="profiler case: multi-row decode with this many query rows (not a bench line)")
     ap.add_argument("--profile-f32", action="store_true", help="profiler case: f32-cache decode")
+    ap.add_argument("--profile-workload", choices=["tiny", "llama8b", "long", "large", "edge"], default=None,
+                    help="profiler case: pa_q8_decode on one workload")
     ap.add_argument("--profile-contig", action="store_true", help="profiler case: contiguous-cache decode")
     ap.add_argument("--seqs", type=int, default=0,
                     help="profile-size case: only the first N sequences (not a bench number)")
@@ -1237,6 +1298,8 @@ def main():
         run_configs(args)
     elif args.profile_rows:
         run_profile_rows(args)
+    elif args.profile_workload:
+        run_profile_workload(args)
     elif args.profile_f32 or args.profile_contig:
         run_profile_variant(args)
     elif args.impl == "reference":
