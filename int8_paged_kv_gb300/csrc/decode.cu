@@ -39,11 +39,6 @@
 #ifndef PA_Q8_SEP_COMBINE
 #define PA_Q8_SEP_COMBINE 1
 #endif
-// Head size 256: 8-head CTAs when 16-head ones would not fill one wave (0:
-// always 16 heads per CTA)
-#ifndef PA_Q8_TC256_HEADS8
-#define PA_Q8_TC256_HEADS8 1
-#endif
 // With such a combine grid, one-tile tensor-core CTAs store one record per
 // token-slot warp instead of merging their warps (0: CTA merge)
 #ifndef PA_Q8_SLOT_RECORDS
@@ -83,9 +78,18 @@ __device__ __forceinline__ int vword(int n, int jj) {
     else return 8 * (n & 3) + (n >> 2) + 2 * (jj & 3) + 32 * (jj >> 2);
 }
 
+// Head size 256: the q fragments of every head tile ([HT][D/16][32] uint4),
+// then each head's logit factor ([HT * 8] f32).
+// Head dims (in float4 units) held at float4 slot t of a per-warp record:
+// the slot order of the record store above.
+template <int D>
+__device__ __forceinline__ int tc_record_dim4(int t) {
+    return vword<D>(2 * (t & 3) + ((t >> 2) & 1), t >> 3);
+}
+
 template <int D, int HT>
 __host__ __device__ constexpr uint32_t tc_extra_bytes() {
-    return D == 256 ? (uint32_t)HT * (D / 16) * 32 * 16 : 0u;
+    return D == 256 ? (uint32_t)HT * (D / 16) * 32 * 16 + (uint32_t)HT * 8 * 4 : 0u;
 }
 
 template <int D>
@@ -131,10 +135,12 @@ decode_tc_kernel(Params P) {
     const int nh_tile = max(0, min(8, w.nh - 8 * ht));
     const bool row_ok = gq < nh_tile;
     const int vh = w.h0 + 8 * ht + gq;                      // this thread's virtual head
-    // q is loaded before the block table so the two round trips overlap
-    // (head size 256 then keeps its fragments in shared memory)
+    // q is loaded before the block table so the two round trips overlap.
+    // Head size 256 keeps its fragments in shared memory, built by the
+    // token slot 0 warp of each head tile alone, so only that warp loads q.
+    const bool q_builder = !kQInSmem || ts == 0;
     float4 qraw[NKS];
-    {
+    if (q_builder) {
         const float4 *qv = reinterpret_cast<const float4 *>(P.q + qrow(P, w, row_ok ? vh : w.h0) * D);
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks)
@@ -160,8 +166,9 @@ decode_tc_kernel(Params P) {
     // pairs.  Head size 256 keeps these fragments in shared memory.
     uint32_t aq[kQInSmem ? 1 : NKS][4];
     uint4 *qf = reinterpret_cast<uint4 *>(smem + L.extra);           // [HT][NKS][32]
-    float qk2;
-    {
+    float *qk2s = reinterpret_cast<float *>(qf + HT * NKS * 32);      // [HT * 8]
+    float qk2 = 0.0f;
+    if (q_builder) {
         auto qload = [&](int ks) -> float4 { return qraw[ks]; };
         float mx = 0.0f;
 #pragma unroll
@@ -181,12 +188,16 @@ decode_tc_kernel(Params P) {
             split_f16x2(v.x * down, v.y * down, f0, f1);
             split_f16x2(v.z * down, v.w * down, f2, f3);
             if constexpr (kQInSmem) {
-                if (ts == 0) qf[(ht * NKS + ks) * 32 + lane] = make_uint4(f0, f1, f2, f3);
+                qf[(ht * NKS + ks) * 32 + lane] = make_uint4(f0, f1, f2, f3);
             } else {
                 aq[ks][0] = f0; aq[ks][1] = f1; aq[ks][2] = f2; aq[ks][3] = f3;
             }
         }
-        if constexpr (kQInSmem) __syncthreads();
+        if (kQInSmem && cq == 0) qk2s[ht * 8 + gq] = qk2;
+    }
+    if constexpr (kQInSmem) {
+        __syncthreads();
+        qk2 = qk2s[ht * 8 + gq];
     }
 
     float acc[NT][4];
@@ -324,8 +335,11 @@ decode_tc_kernel(Params P) {
         // The combine grid merges every row: each warp stores its own
         // record (A in true units, m, l) for the rows of its head tile, and
         // no CTA merge runs.  For a fixed word group jj and column pair half
-        // e, a thread's four accumulators are four consecutive head dims:
-        // one float4.
+        // e, a thread's four accumulators are four consecutive head dims
+        // (4 vword(2 cq + e, jj) ..): one float4, stored at float4 slot
+        // (2 jj + e) * 4 + cq of the record, so the four threads of a row
+        // write 64 contiguous bytes; the combine grid maps the slots back to
+        // head dims (tc_record_dim4).
         if (row_ok) {
             const float f = ldexpf(1.0f, E - kVScaleBias);
             float *rec = P.part + ((qrow(P, w, vh) * P.NP + w.p) * SLOTS + ts) * (D + 4);
@@ -338,7 +352,7 @@ decode_tc_kernel(Params P) {
                     v.y = (acc[4 * jj + 1][e] + acc[4 * jj + 1][e + 2]) * f;
                     v.z = (acc[4 * jj + 2][e] + acc[4 * jj + 2][e + 2]) * f;
                     v.w = (acc[4 * jj + 3][e] + acc[4 * jj + 3][e + 2]) * f;
-                    *reinterpret_cast<float4 *>(rec + 4 * vword<D>(2 * cq + e, jj)) = v;
+                    reinterpret_cast<float4 *>(rec)[(2 * jj + e) * 4 + cq] = v;
                 }
             }
             if (cq == 0) {
@@ -917,7 +931,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint32_t *cont
 // half the dims) merges one output row (sequence, query row, head) from its
 // records -- one per partition, or one per token-slot warp of each partition
 // (rec_slots) --: M = max_r m_r, L = sum_r l_r 2^(m_r - M), out = (1/L)
-// sum_r A_r 2^(m_r - M), summed over r in order, with the first 16 records'
+// sum_r A_r 2^(m_r - M), summed over r in order, with the first 32 records'
 // A loads in flight while M and L are reduced.  Launched as a programmatic
 // dependent of the attention grid: it waits for that grid's completion and
 // memory before the first load.  With one record per partition, rows of a
@@ -930,7 +944,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params P) {
     constexpr int DP = D + 4;                 // floats per partial record
     constexpr int WPR = D > 128 ? D / 128 : 1;    // warps per row
     constexpr int V4W = D / 4 / WPR;          // float4 of the row per warp (32, or 16 at head size 64)
-    constexpr int RU = 16;                    // records' loads in flight per thread
+    constexpr int RU = 32;                    // records' loads in flight per thread
     grid_dependency_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * (kCombineThreads / 32) + warp;
@@ -990,7 +1004,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Params P) {
         load(r0);
     }
     const float il = L > 0.0f ? 1.0f / L : 0.0f;
-    if (act) reinterpret_cast<float4 *>(P.out + row * D)[d4] = make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
+    // per-warp records keep the tensor-core fragment order
+    const int o4 = P.rec_slots > 1 ? tc_record_dim4<D>(d4) : d4;
+    if (act) reinterpret_cast<float4 *>(P.out + row * D)[o4] = make_float4(a.x * il, a.y * il, a.z * il, a.w * il);
 }
 
 // ============================================================== selftest
@@ -1156,14 +1172,12 @@ bool make_plan(DecodeArgs &a, int requested_kernel, int requested_partition, int
         const int n8 = (r + 7) / 8, n16 = (r + 15) / 16;
         const bool wide = PA_Q8_TC_WIDE && a.head_size <= 128 && r > 8 && 7 * n16 < 4 * n8;
         int cap = wide ? 16 : PA_Q8_TC_MAX_HEADS;
-        if (a.head_size == 256) {
-            // 16 heads per CTA (one CTA per SM), unless those CTAs would not fill
-            // one wave: then 8-head CTAs, two per group of 16, each with half the
-            // epilogue, finish sooner (32 MQA sequences of up to 4095 tokens:
-            // 31.4 us against 33.4 us)
-            const int64_t units16 = (int64_t)a.num_seqs * a.num_kv_heads * ((r + 15) / 16);
-            cap = PA_Q8_TC256_HEADS8 && units16 < num_sms ? 8 : 16;
-        }
+        // head size 256: 16 heads per CTA (two head tiles, one CTA per SM),
+        // one read of each K/V tile per 16 heads.  Few sequences then take
+        // short partitions (the rule below) rather than two 8-head CTAs per
+        // group: 32 MQA sequences of up to 4095 tokens, 512-token partitions,
+        // 26.3 us against 27.3 us.
+        if (a.head_size == 256) cap = 16;
         a.heads_per_cta = r < cap ? r : cap;
     } else {
         int hp = a.kernel == kF32 ? 8 : 16;

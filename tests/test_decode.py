@@ -285,8 +285,9 @@ def test_combine_of_many_partitions(kernel, D):
 # (contexts at half the table's capacity) fit in one wave, else the merge by
 # the last CTA of each group (arrival counters, prep kernel).
 COMBINE_CASES = {
-    # one wave, head size 256, 8-head CTAs: one record per token-slot warp,
-    # every row (split or not) merged by the combine grid, 16 records per row
+    # one wave, head size 256, 16-head CTAs (two head tiles): one record per
+    # token-slot warp and head tile, every row (split or not) merged by the
+    # combine grid, 16 records per row
     "grid_slot_records_256": (6, 16, 1, 256, 32, [0, 1, 33, 700, 3000, 4095], 1024, 1),
     # one wave, two causal rows per sequence (8 pairs per kv head)
     "grid_slot_records_rows": (5, 8, 2, 128, 16, [2, 40, 300, 1500, 2600], 256, 2),
