@@ -319,3 +319,20 @@ def test_split_context_merge_routes(case, kernel):
         if c == 0:
             assert np.all(got[s] == 0.0)
     assert device_status() == 0
+
+
+@pytest.mark.parametrize("pt,lens", [(256, [1000, 2000, 37]),
+                                     (128, [9000, 8800, 8000, 7000, 6600, 6000, 5000, 4400, 4000, 3000, 200, 20])])
+def test_split_context_merge_routes_tcgen05(pt, lens):
+    """The tcgen05 family (8 causal rows x 8 heads per kv head) on both merge
+    routes: three sequences split at 256 tokens fit one wave (combine grid,
+    one record per partition); twelve sequences at 128 tokens do not (the
+    last CTA of each group merges)."""
+    from tests.gpu_helpers import assert_close, device_status, gpu_decode_rows, oracle_decode_rows
+    S, H, Hk, D, B, R = len(lens), 8, 1, 128, 16, 8
+    w, ok_, ov_, kc, vc = _random_case(S, H, Hk, D, B, lens, seed=90 + pt)
+    q = np.random.default_rng(91).standard_normal((S, R, H, D)).astype(np.float32)
+    got = gpu_decode_rows(w, kc, vc, q, kernel=3, partition_tokens=pt)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    assert_close(got, want, f"tcgen05 pt {pt}")
+    assert device_status() == 0
