@@ -509,7 +509,8 @@ def run_ours(args) -> None:
     rows_w = int(np.count_nonzero(a.slot_mapping != wl.PAD_SLOT))    # token rows the writer stores
     bytes_d = wl.algorithmic_decode_bytes(cfg, w.context_lens)
     # writer, prep (sequence order; skipped when every CTA of a one-partition
-    # plan is resident at once), attention (combine fused in)
+    # plan is resident at once), attention.  A split plan that fits one wave
+    # has no prep but a combine grid after the attention, so it also counts 3.
     per_sm = 3 if plan["kernel"] == 2 else 2
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     one_wave = plan["num_partitions"] == 1 and plan["num_ctas"] <= per_sm * sms
@@ -706,8 +707,8 @@ def run_ours(args) -> None:
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
                      "traffic": (round(traffic["bytes_per_launch"]) if traffic else None),
-                     "kernel": "pa_q8_decode call (prep kernel + attention kernel with its fused "
-                               "combine), CUDA events on the launching stream",
+                     "kernel": "pa_q8_decode call (prep kernel + attention kernel; one partition per "
+                               "context, so no merge runs), CUDA events on the launching stream",
                      "peak_source": f"{peaks['source']} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)"},
         "clocks": clocks,
         "e2e": e2e,
