@@ -29,11 +29,10 @@ namespace {
 // Each softmax thread owns one virtual head and 16 of a chunk's 32 tokens:
 // two 16x32bx2 loads (lane bases 32q and 32q + 16) give thread t the hi and
 // the lo row of head 16q + t % 16 at tokens 16 (t / 16) .. + 15, so a logit
-// is one paired add, with no exchange between threads.  With 32 heads or
-// fewer, quadrants 2-3 hold the Q rows of quadrants 0-1 again (the M = 128
-// MMAs compute them anyway) and take tokens 16-31 of each chunk, quadrants
-// 0-1 tokens 0-15, each thread 8 tokens: two independent online softmaxes
-// per head, merged in the epilogue.
+// is one paired add; the two threads of a head exchange only the chunk
+// maximum and, at the end, their weight sums.  With 32 heads or fewer the
+// softmax warps of quadrants without heads stay idle (giving them tokens
+// 16-31 of each chunk on copies of the Q rows measured 2-4% slower).
 //
 // Warp roles, linked only by mbarriers (every wait bounded and abortable):
 //  - warps 0-3, softmax: first the Q tile (row max -> 2^-eq -> hi/lo into
