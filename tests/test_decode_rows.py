@@ -207,3 +207,26 @@ def test_scale_sign_extreme_q_rows_and_growing_v(kernel):
             got = gpu_decode_rows(ws, kc, vc, q, kernel=kernel, partition_tokens=pt)
             assert_close(got, want, f"kernel {kernel} scale x {mult} pt {pt}")
     assert device_status() == 0
+
+
+@pytest.mark.parametrize("D,R,H", [(64, 8, 8), (128, 4, 8), (256, 2, 16)])
+def test_tcgen05_many_waves_with_empty_contexts(D, R, H):
+    """More (sequence, kv head) CTAs than fit at once, one partition each (the
+    longest-first order across waves), with every 37th context empty (its
+    rows must be zeros) and one of a single token; every row against the
+    oracle."""
+    from tests.gpu_helpers import (assert_close, device_status, gpu_decode_rows, oracle_decode_rows,
+                                   random_case)
+    S, Hk, B = 320, 1, 16
+    rng = np.random.default_rng(D + R)
+    lens = [int(x) for x in rng.integers(2, 300, S)]
+    for s in range(0, S, 37):
+        lens[s] = 0
+    lens[5] = 1
+    w, ok_, ov_, kc, vc = random_case(S, H, Hk, D, B, lens, seed=60 + D)
+    q = rng.standard_normal((S, R, H, D)).astype(np.float32)
+    got = gpu_decode_rows(w, kc, vc, q, kernel=T5, partition_tokens=384)
+    want = oracle_decode_rows(w, ok_, ov_, q)
+    assert_close(got, want, f"persistent D {D} R {R}")
+    assert np.all(got[[s for s in range(S) if lens[s] == 0]] == 0.0)
+    assert device_status() == 0
