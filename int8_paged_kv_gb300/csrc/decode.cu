@@ -25,6 +25,9 @@
 //     8-15 = lo of the same 8 heads), int8 codes are exact in f16;
 //   * CUDA core: f32 FMA dot products (lane = token) and weighted sums
 //     (lane = 4 head dims).
+// Split contexts are merged by the last CTA of each group to finish, or, when
+// the whole split grid fits in one wave, by combine_kernel, a grid of its own
+// launched as a programmatic dependent of the attention grid.
 // Every wait is bounded; a wait that gives up flags the status word, and a
 // warp leaves only after the copies it issued have landed.
 #include "decode_common.cuh"
